@@ -19,7 +19,8 @@
  *
  * Numeric contract of the encoder (fp32, every operation rounded to nearest,
  * no fused multiply-add; build with -ffp-contract=off):
- *   mn = min x, rng = max x - mn, inv_r = rng > 0 ? 1/rng : 0, u = (x-mn)*inv_r
+ *   mn = min x + 0, rng = (max x + 0) - mn (a zero extreme is +0),
+ *   inv_r = rng > 0 ? 1/rng : 0, u = (x-mn)*inv_r
  *   chunk sum = stride-halving pairwise tree over 32 slots (+16, +8, +4, +2, +1),
  *   absent slots hold +0; mean = sum / n_c; mu = fp16 nearest(mean);
  *   v = u - mu; s = fp16 rounded up(max |v|); inv_s = s > 0 ? 1/s : 0; w = v*inv_s
@@ -148,6 +149,7 @@ void orc_codes(const float *w, int64_t n, int8_t *codes)
     float thr[64];
     uint16_t lv[65];
     orc_tables(thr, lv);
+#pragma omp parallel for schedule(static)
     for (int64_t i = 0; i < n; ++i)
         codes[i] = (int8_t)code_of(w[i], thr);
 }
@@ -200,6 +202,10 @@ static void encode_page(const uint16_t *x, int n, const float *thr, uint8_t *anc
                 if (v > mx)
                     mx = v;
             }
+            /* a zero extreme is +0 whichever zero the data held, so that the
+             * metadata bits do not depend on the order of the scan */
+            mn = mn + 0.0f;
+            mx = mx + 0.0f;
             rng = mx - mn;
         }
         float inv_r = rng > 0.0f ? 1.0f / rng : 0.0f;

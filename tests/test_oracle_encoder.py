@@ -220,3 +220,23 @@ def test_layout_of_multi_layer_tensor(orc):
     assert np.array_equal(q["residual"][1:2, 2:3, PAGE:2 * PAGE], sub["residual"])
     assert np.array_equal(q["page_meta"][1:2, 2:3, 1:2], sub["page_meta"])
     assert np.array_equal(q["chunk_meta"][1:2, 2:3, 1:2], sub["chunk_meta"])
+
+
+def test_signed_zero_extremes_store_plus_zero(orc):
+    """A page whose minimum (or maximum) is a zero stores +0 whether the data
+    held +0 or -0, and the codes do not depend on the zero's sign."""
+    xb = _page(91)
+    xf = S.bf16_bits_to_f32(xb).copy()
+    xf[0, 0, :, 7] = np.abs(xf[0, 0, :, 7])          # channel 7 >= 0, minimum at a zero
+    xf[0, 0, 10, 7] = 0.0
+    xf[0, 0, :, 9] = -np.abs(xf[0, 0, :, 9])         # channel 9 <= 0, maximum at a zero
+    xf[0, 0, 20, 9] = 0.0
+    a = S.f32_to_bf16_bits(xf)
+    b = a.copy()
+    b[0, 0, 10, 7] = 0x8000                            # -0 in place of +0
+    b[0, 0, 20, 9] = 0x8000
+    qa, qb = orc.quantize(a), orc.quantize(b)
+    for k in ("anchor", "residual", "page_meta", "chunk_meta"):
+        assert np.array_equal(qa[k].view(np.uint8), qb[k].view(np.uint8)), k
+    assert qa["page_meta"][0, 0, 0, 0, 7].view(np.uint32) == 0       # +0 minimum
+    assert qa["page_meta"][0, 0, 0, 1, 9] > 0
