@@ -1,0 +1,424 @@
+"""Benchmark of the Lynx progressive KV quantizer hot path on one GB300.
+
+One step = one pass of the whole path over the full worked-example cache
+(94 layers x 4 KV heads x 131072 tokens x 128, bf16 K and V, ~23.5 GiB):
+  lynx_quantize_pages (K, V) -> lynx_dequant_anchor (K, V) ->
+  lynx_refine_residual (K, V) -> lynx_decode_attn through all 94 layers, anchor
+  mode and full mode (batch 1, 64 query heads, group 16).
+Inputs are seeded synthetic Laplace values with per-channel scales 10^U(-2,0)
+and 2% outlier channels x100, generated on the device before timing; every
+buffer is larger than L2, so no flush is needed between steps.
+
+value = algorithmic bytes of the whole step / step time (GB/s). Per-kernel
+GB/s, decode tokens/s and roofline fractions are reported alongside.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+For N > 1 run under torchrun: every rank runs the same per-GPU workload (weak
+scaling, no collective on the data path); rank 0 prints the JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import lynx_synth as S  # noqa: E402
+
+METRIC = "quantize/dequant HBM GB/s and decode-attn tokens/s vs HBM roofline (1 GB300)"
+W3 = S.WORKLOADS[3]
+HQ = 64
+D = 128
+# algorithmic bytes per element (K or V) and per (token, KV head)
+B_QUANT = 2 + 0.5 + 0.5 + 8 / 256 + 4 / 32          # 3.15625
+B_DEQ_ANCHOR = 0.5 + 8 / 256 + 4 / 32 + 2            # 2.65625
+B_REFINE = 1.0 + 8 / 256 + 4 / 32 + 2                # 3.15625
+B_ATTN_ANCHOR = 64 + 64 + 16 + 16 + 4 + 4            # 168
+B_ATTN_FULL = B_ATTN_ANCHOR + 128                    # 296
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples while the timed region runs."""
+
+    def __init__(self, index=0):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------
+# reference arm / CPU baseline: the oracle on a bounded sample of the workload
+# --------------------------------------------------------------------------
+
+def oracle_sample(pages=128, heads=4, layer=0):
+    """Inputs of a bounded sample: `heads` KV heads x `pages` pages of one layer."""
+    T = pages * 256
+    ks, vs = W3.scales(S.S_K), W3.scales(S.S_V)
+    kx = S.laplace_bf16(W3.key(S.S_K), ks, W3.L, W3.H, W3.T, layers=[layer], heads=range(heads), t0=0, t1=T)
+    vx = S.laplace_bf16(W3.key(S.S_V), vs, W3.L, W3.H, W3.T, layers=[layer], heads=range(heads), t0=0, t1=T)
+    return kx, vx, W3.queries_bf16()
+
+
+def oracle_step(orc, kx, vx, qb):
+    """The same sequence of operations as one GPU step, on the sample; returns
+    the algorithmic bytes it stands for."""
+    _, H, T, _ = kx.shape
+    k = orc.quantize(kx)
+    v = orc.quantize(vx)
+    for t in (k, v):
+        orc.dequant(t, False)
+        orc.dequant(t, True)
+    table = np.arange(T // 256, dtype=np.int32)[None, :]
+    ctx = np.array([T], np.int32)
+    orc.decode_attn(qb, k, v, 0, table, ctx, D ** -0.5, False)
+    orc.decode_attn(qb, k, v, 0, table, ctx, D ** -0.5, True)
+    el = 2 * H * T * D
+    return el * (B_QUANT + B_DEQ_ANCHOR + B_REFINE) + H * T * (B_ATTN_ANCHOR + B_ATTN_FULL)
+
+
+def run_oracle(steps, warmup, pages):
+    import oracle as orc
+    orc.build()
+    kx, vx, qb = oracle_sample(pages=pages)
+    for _ in range(warmup):
+        oracle_step(orc, kx, vx, qb)
+    t0 = time.perf_counter()
+    nbytes = 0.0
+    for _ in range(steps):
+        nbytes += oracle_step(orc, kx, vx, qb)
+    dt = time.perf_counter() - t0
+    return nbytes / dt / 1e9, dt, orc.num_threads()
+
+
+# --------------------------------------------------------------------------
+# GPU arm
+# --------------------------------------------------------------------------
+
+class Workload:
+    def __init__(self, torch, lx, layers=None, device="cuda"):
+        self.torch, self.lx = torch, lx
+        L = W3.L if layers is None else layers
+        self.L, self.H, self.T = L, W3.H, W3.T
+        dev = torch.device(device)
+        self.dev = dev
+        gen = S.DeviceGenerator(device)
+        self.x = {}
+        for s in (S.S_K, S.S_V):
+            x = torch.empty((L, self.H, self.T, D), dtype=torch.bfloat16, device=dev)
+            gen.fill(x, W3.key(s), W3.scales(s)[:L])
+            self.x[s] = x
+        self.q = {s: lx.QuantizedKV.empty(L, self.H, self.T, dev) for s in (S.S_K, S.S_V)}
+        self.dense = {s: torch.empty((L, self.H, self.T, D), dtype=torch.bfloat16, device=dev)
+                      for s in (S.S_K, S.S_V)}
+        qb = W3.queries_bf16()
+        self.qt = torch.from_numpy(qb.view(np.int16)).to(dev).view(torch.bfloat16)
+        self.table = torch.arange(self.T // 256, dtype=torch.int32, device=dev)[None, :].contiguous()
+        self.ctx = torch.full((1,), self.T, dtype=torch.int32, device=dev)
+        self.ws = torch.empty(lx.decode_attn_workspace(1, HQ, self.T // 256), dtype=torch.uint8, device=dev)
+        self.out = {m: torch.empty((L, 1, HQ, D), dtype=torch.float32, device=dev) for m in (0, 1)}
+        self.elements = L * self.H * self.T * D          # per tensor
+        self.token_heads = L * self.H * self.T           # per attention pass
+
+    def launches_per_step(self):
+        return 6 + 2 * 2 * self.L
+
+    def step(self, ev=None):
+        """ev: optional dict name -> list of (start, end) event pairs to record."""
+        lx, torch = self.lx, self.torch
+        st = torch.cuda.current_stream()
+
+        def mark(name, fn):
+            if ev is None:
+                fn()
+                return
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(st)
+            fn()
+            b.record(st)
+            ev.setdefault(name, []).append((a, b))
+
+        for s in (S.S_K, S.S_V):
+            mark("quantize", lambda s=s: lx.quantize_pages(self.x[s], self.q[s]))
+        for s in (S.S_K, S.S_V):
+            mark("dequant_anchor", lambda s=s: lx.dequant_anchor(self.q[s], self.dense[s]))
+        for s in (S.S_K, S.S_V):
+            mark("refine", lambda s=s: lx.refine_residual(self.q[s], self.dense[s]))
+        for mode, name in ((lx.MODE_ANCHOR, "decode_attn_anchor"), (lx.MODE_FULL, "decode_attn_full")):
+            def attn(mode=mode):
+                for l in range(self.L):
+                    lx.decode_attn(self.qt, self.q[S.S_K], self.q[S.S_V], l, self.table, self.ctx, D ** -0.5,
+                                   mode, out=self.out[mode][l], workspace=self.ws)
+            mark(name, attn)
+
+    def algorithmic_bytes(self):
+        e = self.elements
+        return {
+            "quantize": 2 * e * B_QUANT,
+            "dequant_anchor": 2 * e * B_DEQ_ANCHOR,
+            "refine": 2 * e * B_REFINE,
+            "decode_attn_anchor": self.token_heads * B_ATTN_ANCHOR,
+            "decode_attn_full": self.token_heads * B_ATTN_FULL,
+        }
+
+
+def e2e_measure(torch, lx, layers, steps, warmup):
+    """End to end through the public API with host buffers: per step, the bf16
+    K and V of `layers` layers go host->device from pinned memory, the whole
+    path runs, and the planes, metadata and attention outputs come back."""
+    wl = Workload(torch, lx, layers=layers)
+    hx = {s: torch.empty(wl.x[s].shape, dtype=torch.bfloat16, pin_memory=True) for s in wl.x}
+    for s in hx:
+        hx[s].copy_(wl.x[s])
+    hq = {s: {n: torch.empty(getattr(wl.q[s], n).shape, dtype=getattr(wl.q[s], n).dtype, pin_memory=True)
+              for n in ("anchor", "residual", "page_meta", "chunk_meta")} for s in wl.q}
+    hout = {m: torch.empty(wl.out[m].shape, dtype=torch.float32, pin_memory=True) for m in wl.out}
+    h2d = sum(t.numel() * t.element_size() for t in hx.values())
+    d2h = sum(t.numel() * t.element_size() for d in hq.values() for t in d.values()) + \
+        sum(t.numel() * t.element_size() for t in hout.values())
+
+    def one():
+        for s in hx:
+            wl.x[s].copy_(hx[s], non_blocking=True)
+        wl.step()
+        for s in hq:
+            for n, t in hq[s].items():
+                t.copy_(getattr(wl.q[s], n), non_blocking=True)
+        for m in hout:
+            hout[m].copy_(wl.out[m], non_blocking=True)
+
+    for _ in range(warmup):
+        one()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        one()
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    total = sum(wl.algorithmic_bytes().values())
+    del wl, hx, hq, hout
+    torch.cuda.empty_cache()
+    return {"value": total / (ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms, "layers": layers,
+            "note": f"{layers} of the 94 layers per step (host buffers pinned), same path and byte accounting"}
+
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+
+    import __graft_entry__
+    if rank == 0 or world == 1:
+        __graft_entry__.build()
+    if world > 1:
+        dist.barrier()
+    import progressive_kv_cache_gb300 as lx
+
+    # CPU baseline first (rank 0 only, before any GPU work that could interfere)
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        v, dt, cores = run_oracle(1, 0, args.cpu_pages)
+        cpu = {"value": v, "unit": "GB/s", "cores": cores, "kind": "oracle",
+               "sample": f"layer 0, {W3.H} KV heads x {args.cpu_pages} pages (K and V) of the full cache: "
+                         f"encode, both decodes, decode attention both modes; {dt:.1f} s"}
+
+    wl = Workload(torch, lx)
+    for _ in range(args.warmup):
+        wl.step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+
+    ev = {}
+    with ClockSampler(local) as clk:
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record()
+        for _ in range(args.steps):
+            wl.step(ev)
+        end.record()
+        torch.cuda.synchronize()
+    ms_step = start.elapsed_time(end) / args.steps
+    if world > 1:
+        t = torch.tensor([ms_step], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step = float(t.item())
+        dist.barrier()
+
+    nbytes = wl.algorithmic_bytes()
+    hbm, peak_kind = peaks()
+    per = {}
+    for name, pairs in ev.items():
+        tot = sum(a.elapsed_time(b) for a, b in pairs)            # ms over all steps
+        n_launch = len(pairs)
+        per_launch_ms = tot / n_launch
+        gbs = nbytes[name] * args.steps / (tot * 1e-3) / 1e9
+        rec = {"ms_per_step": tot / args.steps, "GB/s": gbs, "frac_of_measured_hbm": gbs / hbm,
+               "frac_of_8tbs_nominal": gbs / 8000.0, "share": None, "timed_units": n_launch,
+               "ms_per_timed_unit": per_launch_ms}
+        if name.startswith("decode_attn"):
+            rec["tokens_per_s"] = 1.0 / (tot / args.steps * 1e-3)   # batch 1: one token per pass
+            rec["kv_token_heads_per_s"] = wl.token_heads / (tot / args.steps * 1e-3)
+        per[name] = rec
+    tot_all = sum(p["ms_per_step"] for p in per.values())
+    for p in per.values():
+        p["share"] = p["ms_per_step"] / tot_all
+    dom = max(per, key=lambda n: per[n]["ms_per_step"])
+    launches_per_unit = {"quantize": 1, "dequant_anchor": 1, "refine": 1}
+    if dom in launches_per_unit:
+        ach = nbytes[dom] / 2 / (per[dom]["ms_per_timed_unit"] * 1e-3) / 1e9
+    else:
+        ach = per[dom]["GB/s"]
+    total_bytes = sum(nbytes.values())
+    value = world * total_bytes / (ms_step * 1e-3) / 1e9
+
+    e2e = None
+    if not args.no_e2e:
+        del wl
+        torch.cuda.empty_cache()
+        e2e = e2e_measure(torch, lx, args.e2e_layers, max(1, min(args.steps, 3)), 1)
+        e2e["value"] *= world
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": W3.name, "layers": W3.L, "kv_heads": W3.H, "tokens": W3.T, "head_dim": D,
+                       "q_heads": HQ, "batch": 1, "io": "bf16 in, 4+4-bit planes, bf16 dense cache",
+                       "parallelism": f"replicas x{world}", "l2": "every input larger than L2, no flush"},
+            "roofline": {"bound": "hbm", "kernel": dom, "achieved": ach, "peak": hbm, "unit": "GB/s",
+                         "frac": ach / hbm, "peak_kind": peak_kind, "traffic": None},
+            "per_kernel": per,
+            "decode_tokens_per_s": {"anchor": per["decode_attn_anchor"]["tokens_per_s"],
+                                    "full": per["decode_attn_full"]["tokens_per_s"]},
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": wl_launches(args.steps, W3.L),
+            "clocks": clk.summary(),
+        }
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def wl_launches(steps, L):
+    # quantize x2, dequant x2, refine x2, attention split+combine x2 modes x L layers
+    return steps * (6 + 2 * 2 * L)
+
+
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    v, dt, cores = run_oracle(args.steps, args.warmup, args.ref_pages)
+    sample = (f"layer 0, {W3.H} KV heads x {args.ref_pages} pages (K and V) of the full cache per step: "
+              "encode, both decodes, decode attention both modes")
+    line = {
+        "metric": METRIC, "value": v, "unit": "GB/s", "impl": "reference", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": dt / max(args.steps, 1) * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": W3.name, "layers": W3.L, "kv_heads": W3.H, "tokens": W3.T, "head_dim": D,
+                   "q_heads": HQ, "batch": 1, "sample": sample},
+        "cpu_baseline": {"value": v, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-pages", type=int, default=512)
+    ap.add_argument("--ref-pages", type=int, default=64)
+    ap.add_argument("--e2e-layers", type=int, default=12)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

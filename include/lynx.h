@@ -1,0 +1,180 @@
+/*
+ * lynx.h -- C ABI of the GB300 (sm_103a) Lynx progressive KV quantizer.
+ *
+ * The method: "Lynx: the KV cache does not have to arrive whole" (aigenapps
+ * reading of Han et al.). Section 3 "The quantizer" defines the per-page
+ * encoder (page-level normalisation; chunk-wise outlier isolation with C = 32;
+ * an alpha-law log map onto 127 levels with sign-aware mapping; the +7
+ * round-half-down bias and the 4-bit anchor / 4-bit residual cut). Section 4
+ * "Speculation at the communication boundary" defines the two decoders: the
+ * anchor stream alone is the draft cache, and the residual refines the cache
+ * to the full reconstruction. The fused decode attention follows the
+ * "KV-cache quantization" explainer (aicassindra), "Middle row" and
+ * "Bottom-right": the compact cache is read as is and expanded only in
+ * registers inside Q.K^T, softmax and the weighted sum over V.
+ *
+ * Conventions shared by every call
+ *  - Every pointer argument marked "device" is CUDA device memory owned by the
+ *    caller; the library allocates nothing and keeps no pointer after a call.
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream). Every
+ *    compute call is asynchronous on that stream; its status reports host-side
+ *    argument checks and launch errors only.
+ *  - Device pointers must be 16-byte aligned (LYNX_ERR_ALIGN otherwise).
+ *  - head_dim must be 128 and tokens a multiple of 256 (LYNX_ERR_SHAPE).
+ *  - No call traps, asserts or spins on the device. Errors found on the
+ *    device (a page-table entry outside the page pool, a context length
+ *    outside [0, max_pages*256]) set bits in *dev_err (when given) and the
+ *    affected work is skipped or clamped.
+ *
+ * Numeric contract of the encoder (both this library and any conforming
+ * encoder produce identical bytes): fp32 arithmetic, each operation rounded to
+ * nearest, no fused multiply-add:
+ *   stage 1  mn = min x, rng = max x - mn (a zero extreme taken as +0),
+ *            inv_r = rng > 0 ? 1/rng : 0, u = (x - mn) * inv_r   (valid tokens only)
+ *   stage 2  per 32-token chunk: sum = stride-halving pairwise tree over the 32
+ *            slots (+16, +8, +4, +2, +1; absent slots hold +0); mean = sum/n_c;
+ *            mu = fp16 nearest(mean); v = u - mu; s = fp16 rounded toward
+ *            +inf(max |v|); inv_s = s > 0 ? 1/s : 0; w = v * inv_s
+ *   stage 3  q = #{k in 1..63 : |w| >= T_k},
+ *            T_k = fp32 nearest(((1+alpha)^((k-1/2)/63) - 1)/alpha), alpha = 255;
+ *            c = q for w >= 0, c = -max(q, 1) for w < 0      (c in -63..63)
+ *   stage 4  b = c + 7; A = floor(b/16) in -4..4; r = b - 16A in 0..15.
+ * Decoders: Lv[k] = fp16 nearest(((1+alpha)^(k/63) - 1)/alpha), k = 0..64;
+ *   anchor-only code 16A, full code 16A + r - 7 (magnitudes above 64, which
+ *   the encoder never writes, saturate at Lv[64]);
+ *   x = mn + rng * (mu + s * sgn(code) * Lv[|code|]).
+ */
+#ifndef LYNX_H
+#define LYNX_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    LYNX_OK = 0,
+    LYNX_ERR_NULL = 1,        /* a required pointer is NULL */
+    LYNX_ERR_SHAPE = 2,       /* a size is negative, inconsistent or not supported by the layout */
+    LYNX_ERR_ALIGN = 3,       /* a device pointer is not 16-byte aligned */
+    LYNX_ERR_UNSUPPORTED = 4, /* a legal but unsupported configuration (e.g. group size > 32) */
+    LYNX_ERR_WORKSPACE = 5,   /* workspace smaller than lynx_decode_attn_workspace() */
+    LYNX_ERR_CUDA = 6         /* a CUDA launch or query failed */
+} lynx_status;
+
+typedef enum { LYNX_OUT_BF16 = 0, LYNX_OUT_F32 = 1 } lynx_out_dtype;
+typedef enum { LYNX_MODE_ANCHOR = 0, LYNX_MODE_FULL = 1 } lynx_mode;
+
+/* Device-error bits written (OR-ed) into *dev_err by lynx_decode_attn. */
+#define LYNX_DEVERR_PAGE 1u   /* a page-table entry outside [0, tokens/256) */
+#define LYNX_DEVERR_CTX 2u    /* a context length outside [0, max_pages*256] */
+
+/*
+ * One quantized tensor (K or V): a view of caller-owned device memory.
+ * The page pool of a paged cache is the `tokens` axis: physical page p is
+ * rows [256p, 256p + 256). A sub-range of layers is passed as a view with
+ * offset pointers and a smaller `layers`.
+ *   anchor      [layers][kv_heads][tokens][head_dim/2] u8: two 4-bit anchors
+ *               per byte, channel 2i in the low nibble, two's complement
+ *   residual    same shape: two 4-bit residuals per byte; may be NULL where
+ *               only the anchor stream exists (anchor-only calls)
+ *   page_meta   [layers][kv_heads][tokens/256][2][head_dim] fp32: page minimum,
+ *               page range, per channel
+ *   chunk_meta  [layers][kv_heads][tokens/256][8][2][head_dim] fp16 bits: chunk
+ *               mean, chunk scale, per channel
+ */
+typedef struct {
+    int32_t layers, kv_heads, tokens, head_dim;
+    uint8_t *anchor;
+    uint8_t *residual;
+    float *page_meta;
+    uint16_t *chunk_meta;
+} lynx_qkv;
+
+/*
+ * Encode a bf16 tensor page by page (section 3, all four stages, and the 4+4
+ * cut). One call per tensor: K and V take one call each.
+ *   x_bf16      device, [layers][kv_heads][tokens][128] bf16 (layout of `out`)
+ *   page_valid  device, [tokens/256] int32 valid-token counts in 0..256 for
+ *               each page (the ragged last page), shared by every layer and
+ *               head; NULL = every page full. Statistics use valid tokens only;
+ *               invalid tokens store code 0 (anchor 0, residual 7). Counts
+ *               outside 0..256 are clamped.
+ *   out         planes and metadata written; residual must be non-NULL.
+ */
+lynx_status lynx_quantize_pages(const void *x_bf16, const int32_t *page_valid, const lynx_qkv *out,
+                                void *stream);
+
+/*
+ * Anchor-only reconstruction, the draft cache of section 4 ("Anchor stream
+ * lands, decoding starts"): every element decoded from its anchor with the
+ * residual taken at its centre (code 16A).
+ *   in   planes and metadata (residual may be NULL)
+ *   out  device, [layers][kv_heads][tokens][128] in `dt` (bf16 nearest or fp32)
+ */
+lynx_status lynx_dequant_anchor(const lynx_qkv *in, void *out, lynx_out_dtype dt, void *stream);
+
+/*
+ * Residual refinement in place (section 4, "the kernel refines the cache to
+ * Q_full"): overwrites the dense cache that lynx_dequant_anchor wrote with the
+ * full reconstruction from anchor and residual planes (code 16A + r - 7). The
+ * planes are not modified. `inout` has the layout and dtype of the
+ * lynx_dequant_anchor output; in->residual must be non-NULL.
+ */
+lynx_status lynx_refine_residual(const lynx_qkv *in, void *inout, lynx_out_dtype dt, void *stream);
+
+/*
+ * Workspace bytes lynx_decode_attn needs for this batch shape on the current
+ * device (split-K partials). Returns 0 for invalid sizes.
+ */
+size_t lynx_decode_attn_workspace(int32_t batch, int32_t q_heads, int32_t max_pages);
+
+/*
+ * One decode step of attention over one layer of the quantized paged cache,
+ * dequantizing in registers (explainer, "Bottom-right"):
+ *   out[b][h] = sum_t softmax_t(sm_scale * q[b][h] . K[t]) V[t],  t < ctx_lens[b],
+ * where K, V are the anchor-only (LYNX_MODE_ANCHOR) or full (LYNX_MODE_FULL)
+ * reconstructions, token t of request b lives in physical page
+ * page_table[b][t/256], row t%256, and query head h reads KV head
+ * h / (q_heads / kv_heads). The pages of each (request, KV head) are split
+ * across CTAs (split-K) and the partial (max, sum, output) triples are merged
+ * with a log-sum-exp combine.
+ *   q_bf16      device, [batch][q_heads][128] bf16
+ *   k, v        quantized K and V of the whole pool; `layer` selects the layer;
+ *               residual planes required in FULL mode
+ *   page_table  device, [batch][max_pages] int32
+ *   ctx_lens    device, [batch] int32; 0 gives an output of zeros
+ *   out         device, [batch][q_heads][128] fp32
+ *   scores      device or NULL, [batch][q_heads][max_pages*256] fp32: the scaled
+ *               logits sm_scale * q.K for t < ctx, -inf for the rest
+ *   workspace   device, ws_bytes >= lynx_decode_attn_workspace(batch, q_heads, max_pages)
+ *   dev_err     device or NULL, one uint32 (LYNX_DEVERR_* bits OR-ed in)
+ * q_heads must be a multiple of kv_heads with a group size of at most 32.
+ */
+lynx_status lynx_decode_attn(const void *q_bf16, const lynx_qkv *k, const lynx_qkv *v, int32_t layer,
+                             const int32_t *page_table, const int32_t *ctx_lens, int32_t batch,
+                             int32_t q_heads, int32_t max_pages, float sm_scale, lynx_mode mode,
+                             float *out, float *scores, void *workspace, size_t ws_bytes,
+                             uint32_t *dev_err, void *stream);
+
+/* Human-readable name of a status. Never NULL. */
+const char *lynx_status_string(lynx_status s);
+
+/*
+ * Diagnostics (no counterpart in the method: they expose the library's own
+ * tables and its stage-3 code path so that tests can compare them with an
+ * independent implementation).
+ *   lynx_host_tables  host call, no GPU needed: thr[64] (thr[0] = 0) and
+ *                     lv[65] fp16 bits, exactly as the kernels use them
+ *   lynx_level_codes  device: codes[i] = stage-3 code (-63..63) of w[i]
+ */
+void lynx_host_tables(float *thr, uint16_t *lv);
+lynx_status lynx_level_codes(const float *w, int64_t n, int8_t *codes, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LYNX_H */

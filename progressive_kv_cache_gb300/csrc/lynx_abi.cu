@@ -1,0 +1,190 @@
+// lynx_abi.cu -- the extern "C" entry points declared in include/lynx.h:
+// argument checks on the host, then one launch sequence per call. Nothing is
+// allocated here; every buffer belongs to the caller.
+#include <cstring>
+
+#include "lynx_internal.cuh"
+
+using namespace lynx;
+
+namespace {
+
+bool aligned(const void *p, uintptr_t a) { return ((uintptr_t)p & (a - 1)) == 0; }
+
+lynx_status check_qkv(const lynx_qkv *t, bool need_residual)
+{
+    if (!t || !t->anchor || !t->page_meta || !t->chunk_meta || (need_residual && !t->residual))
+        return LYNX_ERR_NULL;
+    if (t->layers < 0 || t->kv_heads < 0 || t->tokens < 0 || t->tokens % kPage || t->head_dim != kD)
+        return LYNX_ERR_SHAPE;
+    if (!aligned(t->anchor, 16) || !aligned(t->page_meta, 16) || !aligned(t->chunk_meta, 16) ||
+        (t->residual && !aligned(t->residual, 16)))
+        return LYNX_ERR_ALIGN;
+    if (!host_tables().ok)
+        return LYNX_ERR_UNSUPPORTED;
+    return LYNX_OK;
+}
+
+lynx_status from_cuda(cudaError_t e) { return e == cudaSuccess ? LYNX_OK : LYNX_ERR_CUDA; }
+
+} // namespace
+
+extern "C" {
+
+const char *lynx_status_string(lynx_status s)
+{
+    switch (s) {
+    case LYNX_OK: return "ok";
+    case LYNX_ERR_NULL: return "a required pointer is NULL";
+    case LYNX_ERR_SHAPE: return "invalid or unsupported shape";
+    case LYNX_ERR_ALIGN: return "a device pointer is not 16-byte aligned";
+    case LYNX_ERR_UNSUPPORTED: return "unsupported configuration";
+    case LYNX_ERR_WORKSPACE: return "workspace too small";
+    case LYNX_ERR_CUDA: return "CUDA error";
+    }
+    return "unknown status";
+}
+
+void lynx_host_tables(float *thr, uint16_t *lv)
+{
+    const HostTables &t = host_tables();
+    if (thr)
+        std::memcpy(thr, t.thr, sizeof t.thr);
+    if (lv)
+        std::memcpy(lv, t.lv, sizeof t.lv);
+}
+
+lynx_status lynx_quantize_pages(const void *x_bf16, const int32_t *page_valid, const lynx_qkv *out, void *stream)
+{
+    lynx_status st = check_qkv(out, true);
+    if (st != LYNX_OK)
+        return st;
+    if (!x_bf16)
+        return LYNX_ERR_NULL;
+    if (!aligned(x_bf16, 16) || (page_valid && !aligned(page_valid, 4)))
+        return LYNX_ERR_ALIGN;
+    return from_cuda(launch_quantize(static_cast<const uint16_t *>(x_bf16), page_valid, *out, (cudaStream_t)stream));
+}
+
+lynx_status lynx_dequant_anchor(const lynx_qkv *in, void *out, lynx_out_dtype dt, void *stream)
+{
+    lynx_status st = check_qkv(in, false);
+    if (st != LYNX_OK)
+        return st;
+    if (!out)
+        return LYNX_ERR_NULL;
+    if (!aligned(out, 16))
+        return LYNX_ERR_ALIGN;
+    if (dt != LYNX_OUT_BF16 && dt != LYNX_OUT_F32)
+        return LYNX_ERR_UNSUPPORTED;
+    return from_cuda(launch_dequant(*in, out, false, dt == LYNX_OUT_F32, (cudaStream_t)stream));
+}
+
+lynx_status lynx_refine_residual(const lynx_qkv *in, void *inout, lynx_out_dtype dt, void *stream)
+{
+    lynx_status st = check_qkv(in, true);
+    if (st != LYNX_OK)
+        return st;
+    if (!inout)
+        return LYNX_ERR_NULL;
+    if (!aligned(inout, 16))
+        return LYNX_ERR_ALIGN;
+    if (dt != LYNX_OUT_BF16 && dt != LYNX_OUT_F32)
+        return LYNX_ERR_UNSUPPORTED;
+    return from_cuda(launch_dequant(*in, inout, true, dt == LYNX_OUT_F32, (cudaStream_t)stream));
+}
+
+size_t lynx_decode_attn_workspace(int32_t batch, int32_t q_heads, int32_t max_pages)
+{
+    if (batch <= 0 || q_heads <= 0 || max_pages <= 0)
+        return 0;
+    int n_splits = 1, pps = 1;
+    attn_split_plan(batch, max_pages, device_sm_count() > 0 ? device_sm_count() : 1, &n_splits, &pps);
+    return attn_workspace_bytes(batch, q_heads, n_splits);
+}
+
+lynx_status lynx_decode_attn(const void *q_bf16, const lynx_qkv *k, const lynx_qkv *v, int32_t layer,
+                             const int32_t *page_table, const int32_t *ctx_lens, int32_t batch, int32_t q_heads,
+                             int32_t max_pages, float sm_scale, lynx_mode mode, float *out, float *scores,
+                             void *workspace, size_t ws_bytes, uint32_t *dev_err, void *stream)
+{
+    const bool full = mode == LYNX_MODE_FULL;
+    if (mode != LYNX_MODE_ANCHOR && mode != LYNX_MODE_FULL)
+        return LYNX_ERR_UNSUPPORTED;
+    lynx_status st = check_qkv(k, full);
+    if (st != LYNX_OK)
+        return st;
+    if ((st = check_qkv(v, full)) != LYNX_OK)
+        return st;
+    if (!q_bf16 || !page_table || !ctx_lens || !out)
+        return LYNX_ERR_NULL;
+    if (batch < 0 || q_heads < 0 || max_pages <= 0 || k->kv_heads <= 0)
+        return LYNX_ERR_SHAPE;
+    if (k->layers != v->layers || k->kv_heads != v->kv_heads || k->tokens != v->tokens)
+        return LYNX_ERR_SHAPE;
+    if (layer < 0 || layer >= k->layers || q_heads % k->kv_heads)
+        return LYNX_ERR_SHAPE;
+    const int G = q_heads / k->kv_heads;
+    if (batch > 0 && G > 32)
+        return LYNX_ERR_UNSUPPORTED;
+    if (!aligned(q_bf16, 16) || !aligned(out, 16) || (scores && !aligned(scores, 16)) ||
+        !aligned(page_table, 4) || !aligned(ctx_lens, 4) || (dev_err && !aligned(dev_err, 4)) ||
+        (workspace && !aligned(workspace, 16)))
+        return LYNX_ERR_ALIGN;
+    if (batch == 0 || q_heads == 0)
+        return LYNX_OK;
+    const int sms = device_sm_count();
+    if (sms <= 0)
+        return LYNX_ERR_CUDA;
+    int n_splits = 1, pps = 1;
+    attn_split_plan(batch, max_pages, sms, &n_splits, &pps);
+    if (!workspace)
+        return LYNX_ERR_NULL;
+    if (ws_bytes < attn_workspace_bytes(batch, q_heads, n_splits))
+        return LYNX_ERR_WORKSPACE;
+
+    const int64_t H = k->kv_heads, T = k->tokens, P = T / kPage;
+    const int64_t plane_off = (int64_t)layer * H * T * (kD / 2);
+    const int64_t pm_off = (int64_t)layer * H * P * (2 * kD);
+    const int64_t cm_off = (int64_t)layer * H * P * (kNChunk * 2 * kD);
+    AttnArgs a{};
+    a.q = static_cast<const uint16_t *>(q_bf16);
+    a.ka = k->anchor + plane_off;
+    a.kr = full ? k->residual + plane_off : nullptr;
+    a.va = v->anchor + plane_off;
+    a.vr = full ? v->residual + plane_off : nullptr;
+    a.kpm = k->page_meta + pm_off;
+    a.vpm = v->page_meta + pm_off;
+    a.kcm = k->chunk_meta + cm_off;
+    a.vcm = v->chunk_meta + cm_off;
+    a.page_table = page_table;
+    a.ctx = ctx_lens;
+    a.out = out;
+    a.scores = scores;
+    a.part = static_cast<float *>(workspace);
+    a.dev_err = dev_err;
+    a.B = batch;
+    a.Hq = q_heads;
+    a.H = (int)H;
+    a.G = G;
+    a.max_pages = max_pages;
+    a.pool_pages = (int)P;
+    a.n_splits = n_splits;
+    a.pages_per_split = pps;
+    a.sm_scale = sm_scale;
+    a.full = full;
+    return from_cuda(launch_decode_attn(a, (cudaStream_t)stream));
+}
+
+lynx_status lynx_level_codes(const float *w, int64_t n, int8_t *codes, void *stream)
+{
+    if (n < 0)
+        return LYNX_ERR_SHAPE;
+    if (n > 0 && (!w || !codes))
+        return LYNX_ERR_NULL;
+    if (!host_tables().ok)
+        return LYNX_ERR_UNSUPPORTED;
+    return from_cuda(launch_level_codes(w, n, codes, (cudaStream_t)stream));
+}
+
+} // extern "C"

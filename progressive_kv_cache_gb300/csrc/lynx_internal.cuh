@@ -1,0 +1,83 @@
+// lynx_internal.cuh -- types shared by the library's translation units.
+//
+// The tables below are built once on the host (lynx_tables.cu) from the
+// written definitions of the Lynx quantizer (section 3 "The quantizer" of the
+// aigenapps reading) and passed to kernels by value, so the library holds no
+// device-global state and needs no initialisation call.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/lynx.h"
+
+namespace lynx {
+
+constexpr int kPage = 256;     // tokens per page
+constexpr int kChunk = 32;     // C = 32 tokens per chunk
+constexpr int kNChunk = kPage / kChunk;
+constexpr int kD = 128;        // head dimension
+constexpr int kQMax = 63;      // codes -63..63 (127 levels)
+constexpr int kBias = 7;       // +7 before the 4-bit cut
+constexpr double kAlpha = 255.0;
+
+// Stage-3 bucket table. The fp32 value |w| in [2^-13, 2) falls in bucket
+// ((bits >> 19) - kBucketBase): 16 buckets per octave, each narrower than the
+// gap between two consecutive thresholds, so at most one threshold lies inside
+// a bucket. Entry = {bits of that threshold (0xFFFFFFFF if none), number of
+// thresholds at or below the bucket's lower edge}. Entry kNBucket catches
+// |w| < 2^-13 (below the first threshold) and non-finite values.
+constexpr uint32_t kBucketBase = (127u - 13u) << 4;
+constexpr int kNBucket = 14 * 16;
+
+struct MapTable {
+    uint2 e[kNBucket + 1];
+};
+
+// Signed level values used by the decoders:
+//   full[(A & 15) << 4 | r] = sgn(c) * Lv[min(|c|, 64)], c = 16A + r - 7
+//   anchor[A & 15]          = sgn(16A) * Lv[min(|16A|, 64)]
+struct LevelTable {
+    float full[256];
+    float anchor[16];
+};
+
+struct HostTables {
+    float thr[64];
+    uint16_t lv[65];
+    MapTable map;
+    LevelTable lev;
+    bool ok;
+};
+
+const HostTables &host_tables();   // built once, thread-safe
+
+int device_sm_count();             // SM count of the current device (cached per device)
+
+// ---- launchers (one per translation unit) -------------------------------
+cudaError_t launch_quantize(const uint16_t *x, const int32_t *page_valid, const lynx_qkv &o,
+                            cudaStream_t s);
+cudaError_t launch_level_codes(const float *w, int64_t n, int8_t *codes, cudaStream_t s);
+cudaError_t launch_dequant(const lynx_qkv &in, void *out, bool full, bool f32, cudaStream_t s);
+
+struct AttnArgs {
+    const uint16_t *q;
+    const uint8_t *ka, *kr, *va, *vr;
+    const float *kpm, *vpm;
+    const uint16_t *kcm, *vcm;
+    const int32_t *page_table, *ctx;
+    float *out, *scores, *part;
+    uint32_t *dev_err;
+    int B, Hq, H, G, max_pages, pool_pages, n_splits, pages_per_split;
+    float sm_scale;
+    bool full;
+};
+void attn_split_plan(int batch, int max_pages, int sms, int *n_splits, int *pages_per_split);
+size_t attn_workspace_bytes(int batch, int q_heads, int n_splits);
+cudaError_t launch_decode_attn(const AttnArgs &a, cudaStream_t s);
+
+// ---- device helpers ------------------------------------------------------
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+} // namespace lynx

@@ -1,0 +1,124 @@
+// lynx_tables.cu -- host-built tables of the Lynx quantizer, and device queries.
+//
+// Thresholds and level values come from section 3 of the aigenapps reading of
+// Lynx ("an alpha-law logarithmic map onto 2^7 - 1 = 127 levels"; "reconstructed
+// magnitude scales as (1+alpha)^q"), evaluated in double on the host and rounded
+// once: thresholds to fp32, levels to fp16.
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include <cuda_fp16.h>
+
+#include "lynx_internal.cuh"
+
+namespace lynx {
+
+namespace {
+
+uint32_t f32_bits(float f)
+{
+    uint32_t u;
+    std::memcpy(&u, &f, 4);
+    return u;
+}
+
+float f32_from_bits(uint32_t u)
+{
+    float f;
+    std::memcpy(&f, &u, 4);
+    return f;
+}
+
+uint16_t half_bits(__half h)
+{
+    uint16_t u;
+    std::memcpy(&u, &h, 2);
+    return u;
+}
+
+void build(HostTables &t)
+{
+    t.ok = true;
+    t.thr[0] = 0.0f;
+    for (int k = 1; k <= kQMax; ++k)
+        t.thr[k] = (float)((std::pow(1.0 + kAlpha, (k - 0.5) / kQMax) - 1.0) / kAlpha);
+    float lvf[65];
+    for (int k = 0; k <= 64; ++k) {
+        __half h = __double2half((std::pow(1.0 + kAlpha, (double)k / kQMax) - 1.0) / kAlpha);
+        t.lv[k] = half_bits(h);
+        lvf[k] = __half2float(h);
+    }
+
+    // stage-3 buckets
+    for (int i = 0; i < kNBucket; ++i) {
+        uint32_t lo = (kBucketBase + (uint32_t)i) << 19;
+        uint32_t hi = lo + (1u << 19);
+        int q0 = 0, inside = 0, next = -1;
+        for (int k = 1; k <= kQMax; ++k) {
+            uint32_t tb = f32_bits(t.thr[k]);
+            if (tb <= lo)
+                ++q0;
+            else if (tb < hi) {
+                ++inside;
+                next = k;
+            }
+        }
+        if (inside > 1)
+            t.ok = false;   // would break the one-compare lookup
+        t.map.e[i] = make_uint2(next > 0 ? f32_bits(t.thr[next]) : 0xFFFFFFFFu, (uint32_t)q0);
+    }
+    // everything below 2^-13 is below the first threshold
+    if (f32_bits(t.thr[1]) < (kBucketBase << 19))
+        t.ok = false;
+    t.map.e[kNBucket] = make_uint2(0xFFFFFFFFu, 0u);
+    (void)f32_from_bits;
+
+    // decoder levels
+    for (int an = 0; an < 16; ++an) {
+        int A = an >= 8 ? an - 16 : an;
+        for (int r = 0; r < 16; ++r) {
+            int c = 16 * A + r - kBias;
+            int m = c < 0 ? -c : c;
+            if (m > 64)
+                m = 64;
+            float v = lvf[m];
+            t.lev.full[(an << 4) | r] = c < 0 ? -v : v;
+        }
+        int c = 16 * A;
+        int m = c < 0 ? -c : c;
+        if (m > 64)
+            m = 64;
+        t.lev.anchor[an] = c < 0 ? -lvf[m] : lvf[m];
+    }
+}
+
+} // namespace
+
+const HostTables &host_tables()
+{
+    static HostTables t;
+    static std::once_flag once;
+    std::call_once(once, [] { build(t); });
+    return t;
+}
+
+int device_sm_count()
+{
+    static std::mutex mu;
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0)
+        return 0;
+    std::lock_guard<std::mutex> g(mu);
+    if (dev < 64 && cache[dev])
+        return cache[dev];
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return 0;
+    if (dev < 64)
+        cache[dev] = sms;
+    return sms;
+}
+
+} // namespace lynx

@@ -1,0 +1,129 @@
+"""The C ABI without a GPU: the library loads, exports every declared symbol,
+builds the same tables as the oracle, and rejects bad arguments on the host
+before touching the device."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "lynx.h")
+
+
+@pytest.fixture(scope="module")
+def lx():
+    from progressive_kv_cache_gb300 import build
+    build.build()
+    import progressive_kv_cache_gb300 as lx
+    return lx
+
+
+def _declared():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(lynx_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(lx):
+    names = _declared()
+    assert {"lynx_quantize_pages", "lynx_dequant_anchor", "lynx_refine_residual", "lynx_decode_attn",
+            "lynx_decode_attn_workspace", "lynx_status_string"} <= set(names)
+    lib = lx.library()
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lx):
+    lib = lx.library()
+    seen = set()
+    for s in range(7):
+        txt = lib.lynx_status_string(s).decode()
+        assert txt and txt not in seen
+        seen.add(txt)
+    assert lib.lynx_status_string(99).decode() == "unknown status"
+
+
+def test_host_tables_equal_the_oracles(lx, orc):
+    thr, lv = lx.host_tables()
+    othr, olv = orc.tables()
+    assert np.array_equal(thr.view(np.uint32), othr.view(np.uint32))
+    assert np.array_equal(lv, olv)
+
+
+def _qkv(lx, L=1, H=1, T=256, base=0x10000, residual=True):
+    return lx.LynxQKV(L, H, T, 128, base, base + 0x100000 if residual else None, base + 0x200000,
+                      base + 0x300000)
+
+
+def _q(lx, d, x=0x400000, pv=None):
+    lib = lx.library()
+    return lib.lynx_quantize_pages(ctypes.c_void_p(x), None if pv is None else ctypes.c_void_p(pv),
+                                   ctypes.byref(d), None)
+
+
+def test_quantize_rejects_bad_arguments(lx):
+    assert _q(lx, _qkv(lx), x=0) == lx.ERR_NULL
+    assert _q(lx, _qkv(lx, residual=False)) == lx.ERR_NULL
+    assert _q(lx, _qkv(lx, T=300)) == lx.ERR_SHAPE
+    d = _qkv(lx)
+    d.head_dim = 64
+    assert _q(lx, d) == lx.ERR_SHAPE
+    assert _q(lx, _qkv(lx, L=-1)) == lx.ERR_SHAPE
+    assert _q(lx, _qkv(lx), x=0x400008) == lx.ERR_ALIGN
+    assert _q(lx, _qkv(lx, base=0x10004)) == lx.ERR_ALIGN
+    assert _q(lx, _qkv(lx), pv=0x500002) == lx.ERR_ALIGN
+
+
+def test_dequant_and_refine_reject_bad_arguments(lx):
+    lib = lx.library()
+    d = _qkv(lx)
+    assert lib.lynx_dequant_anchor(ctypes.byref(d), None, 0, None) == lx.ERR_NULL
+    assert lib.lynx_dequant_anchor(ctypes.byref(d), ctypes.c_void_p(0x400004), 0, None) == lx.ERR_ALIGN
+    assert lib.lynx_dequant_anchor(ctypes.byref(d), ctypes.c_void_p(0x400000), 7, None) == lx.ERR_UNSUPPORTED
+    d2 = _qkv(lx, residual=False)
+    assert lib.lynx_refine_residual(ctypes.byref(d2), ctypes.c_void_p(0x400000), 0, None) == lx.ERR_NULL
+    assert lib.lynx_dequant_anchor(None, ctypes.c_void_p(0x400000), 0, None) == lx.ERR_NULL
+
+
+def _attn(lx, k, v, layer=0, B=1, Hq=4, maxp=1, mode=0, q=0x600000, pt=0x700000, ctx=0x700100,
+          out=0x800000, ws=0x900000, wsb=1 << 30):
+    lib = lx.library()
+    return lib.lynx_decode_attn(ctypes.c_void_p(q) if q else None, ctypes.byref(k), ctypes.byref(v), layer,
+                                ctypes.c_void_p(pt) if pt else None, ctypes.c_void_p(ctx), B, Hq, maxp, 0.1,
+                                mode, ctypes.c_void_p(out), None, ctypes.c_void_p(ws) if ws else None, wsb,
+                                None, None)
+
+
+def test_decode_attn_rejects_bad_arguments(lx):
+    k, v = _qkv(lx, H=2), _qkv(lx, H=2, base=0x20000000)
+    assert _attn(lx, k, v, q=0) == lx.ERR_NULL
+    assert _attn(lx, k, v, pt=0) == lx.ERR_NULL
+    assert _attn(lx, k, v, layer=1) == lx.ERR_SHAPE
+    assert _attn(lx, k, v, Hq=3) == lx.ERR_SHAPE                 # not a multiple of kv_heads
+    assert _attn(lx, k, v, Hq=2 * 33) == lx.ERR_UNSUPPORTED       # group of 33
+    assert _attn(lx, k, v, maxp=0) == lx.ERR_SHAPE
+    assert _attn(lx, k, _qkv(lx, H=1, base=0x20000000)) == lx.ERR_SHAPE
+    assert _attn(lx, k, v, out=0x800004) == lx.ERR_ALIGN
+    assert _attn(lx, k, v, pt=0x700002) == lx.ERR_ALIGN
+    ka, va = _qkv(lx, H=2, residual=False), _qkv(lx, H=2, base=0x20000000, residual=False)
+    assert _attn(lx, ka, va, mode=1) == lx.ERR_NULL              # full mode needs residuals
+    assert _attn(lx, ka, va, mode=5) == lx.ERR_UNSUPPORTED
+    assert _attn(lx, k, v, B=0) == lx.OK                          # nothing to do, no launch
+
+
+def test_workspace_query(lx):
+    lib = lx.library()
+    assert lib.lynx_decode_attn_workspace(0, 64, 10) == 0
+    assert lib.lynx_decode_attn_workspace(1, 64, 0) == 0
+    a = lib.lynx_decode_attn_workspace(1, 64, 512)
+    b = lib.lynx_decode_attn_workspace(2, 64, 512)
+    assert a > 0 and b > 0 and a % 16 == 0
+
+
+def test_level_codes_rejects_bad_arguments(lx):
+    lib = lx.library()
+    assert lib.lynx_level_codes(None, 10, None, None) == lx.ERR_NULL
+    assert lib.lynx_level_codes(None, -1, None, None) == lx.ERR_SHAPE
+    assert lib.lynx_level_codes(None, 0, None, None) == lx.OK

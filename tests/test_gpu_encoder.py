@@ -1,0 +1,101 @@
+"""GPU parity of the encoder (lynx_quantize_pages) and of its stage-3 code path:
+bit-exact against the oracle on seeded inputs."""
+import numpy as np
+import pytest
+import torch
+
+import lynx_synth as S
+from gpu_helpers import assert_planes_equal, bf16_dev, i32_dev, planes_np
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def lx():
+    import __graft_entry__
+    __graft_entry__.build()
+    import progressive_kv_cache_gb300 as lx
+    return lx
+
+
+def test_level_codes_exhaustive_nonnegative(lx, orc):
+    """Every fp32 in [0, 1 + 64 ulp] through the encoder's bucket lookup equals the
+    oracle's threshold count."""
+    top = int(np.float32(1.0).view(np.uint32)) + 64
+    step = 1 << 26
+    for lo in range(0, top + 1, step):
+        hi = min(lo + step, top + 1)
+        w = np.arange(lo, hi, dtype=np.uint32).view(np.float32)
+        got = lx.level_codes(torch.from_numpy(w).cuda()).cpu().numpy()
+        want = orc.codes(w)
+        if not np.array_equal(got, want):
+            i = int(np.argmax(got != want))
+            raise AssertionError(f"w={w[i]!r} bits={w.view(np.uint32)[i]:#x}: gpu {got[i]} oracle {want[i]}")
+
+
+def test_level_codes_negative_and_special(lx, orc):
+    rng = np.random.default_rng(3)
+    w = -np.abs(rng.standard_normal(1 << 22).astype(np.float32)) * 10.0 ** rng.uniform(-8, 0, 1 << 22)
+    thr, _ = orc.tables()
+    near = np.concatenate([np.arange(int(t) - 300, int(t) + 300, dtype=np.uint32) for t in thr[1:].view(np.uint32)])
+    w = np.concatenate([w.astype(np.float32), -near.view(np.float32), near.view(np.float32),
+                        np.array([0.0, -0.0, 1e-40, -1e-40, 1.0, -1.0], np.float32)])
+    got = lx.level_codes(torch.from_numpy(w).cuda()).cpu().numpy()
+    assert np.array_equal(got, orc.codes(w))
+
+
+def _encode(lx, xb, page_valid=None):
+    L, H, T, _ = xb.shape
+    q = lx.QuantizedKV.empty(L, H, T)
+    lx.quantize_pages(bf16_dev(xb), q, None if page_valid is None else i32_dev(page_valid))
+    return planes_np(q)
+
+
+def test_one_page(lx, orc):
+    w = S.WORKLOADS[1]
+    for s in (S.S_K, S.S_V):
+        xb = S.laplace_bf16(w.key(s), w.scales(s), 1, 1, 256)
+        assert_planes_equal(_encode(lx, xb), orc.quantize(xb), f"tensor {s}: ")
+
+
+@pytest.mark.parametrize("valid", [[256, 100, 0, 33], [1, 31, 32, 255], [0, 0, 0, 0]])
+def test_ragged_multi_layer(lx, orc, valid):
+    w = S.Workload("t", 77, L=2, H=3, T=4 * 256, n_outliers_fixed=5, base_log10=(-2, 0))
+    xb = S.laplace_bf16(w.key(S.S_K), w.scales(S.S_K), 2, 3, 4 * 256)
+    pv = np.array(valid, np.int32)
+    assert_planes_equal(_encode(lx, xb, pv), orc.quantize(xb, pv))
+
+
+def test_special_values(lx, orc):
+    """Constant channels, signed-zero extremes, huge and tiny magnitudes."""
+    w = S.Workload("t", 78, L=1, H=1, T=512, n_outliers_fixed=3)
+    xf = S.bf16_bits_to_f32(S.laplace_bf16(w.key(S.S_V), w.scales(S.S_V), 1, 1, 512)).copy()
+    xf[..., 0] = 2.5
+    xf[..., 1] = 0.0
+    xf[..., 2] = np.abs(xf[..., 2])
+    xf[0, 0, 5, 2] = 0.0
+    xf[..., 3] *= 1e30
+    xf[..., 4] *= 1e-30
+    xf[0, 0, 0:32, 5] = 7.0           # a constant chunk inside a varying channel
+    xb = S.f32_to_bf16_bits(xf)
+    xb[0, 0, 7, 1] = 0x8000            # -0 among +0
+    xb[0, 0, 9, 2] = 0x8000
+    assert_planes_equal(_encode(lx, xb), orc.quantize(xb))
+
+
+def test_qwen3_235b_like_layer_every_page(lx, orc):
+    """4 KV heads x 32K tokens, K and V: every page bit-exact."""
+    w = S.WORKLOADS[2]
+    for s in (S.S_K, S.S_V):
+        xb = S.laplace_bf16(w.key(s), w.scales(s), w.L, w.H, w.T)
+        assert_planes_equal(_encode(lx, xb), orc.quantize(xb), f"tensor {s}: ")
+
+
+def test_device_generator_matches_host_generator(lx):
+    w = S.WORKLOADS[2]
+    gen = S.DeviceGenerator()
+    out = torch.empty((1, 4, 2048, 128), dtype=torch.bfloat16, device="cuda")
+    sc = w.scales(S.S_K)
+    gen.fill(out, w.key(S.S_K), sc)
+    host = S.laplace_bf16(w.key(S.S_K), sc, 1, 4, 2048)
+    assert np.array_equal(out.view(torch.int16).cpu().numpy().view(np.uint16), host)
