@@ -168,7 +168,10 @@ const char *lynx_status_string(lynx_status s);
  * independent implementation).
  *   lynx_host_tables  host call, no GPU needed: thr[64] (thr[0] = 0) and
  *                     lv[65] fp16 bits, exactly as the kernels use them
- *   lynx_level_codes  device: codes[i] = stage-3 code (-63..63) of w[i]
+ *   lynx_level_codes  device: codes[i] = stage-3 code (-63..63) of w[i], for
+ *                     finite |w| < 2 (stage 2 only produces |w| <= 1 + 2^-23;
+ *                     larger magnitudes are outside the encoder's domain and
+ *                     their codes are unspecified)
  */
 void lynx_host_tables(float *thr, uint16_t *lv);
 lynx_status lynx_level_codes(const float *w, int64_t n, int8_t *codes, void *stream);

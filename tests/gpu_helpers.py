@@ -58,3 +58,43 @@ def dense_to_np(t):
     if t.dtype == torch.bfloat16:
         return (t.view(torch.int16).cpu().numpy().view(np.uint16).astype(np.uint32) << 16).view(np.float32)
     return t.cpu().numpy()
+
+
+U32 = 2.0 ** -24
+ATTN_SENS_C = 8.0
+
+
+def attn_tolerance(orc, qb, kref, vref, layer, table, ctx, sm_scale, full):
+    """Per-output bound |o_gpu - o| <= 2e-3 + C * E for an fp32 decode attention.
+
+    E[b,h,d] = u32 * sum_t p_t |v_td - o_d| * sm_scale * sum_d' |q_d'| |k_td'| is
+    the first-order change of output (b,h,d) when every score carries a relative
+    fp32 rounding of its magnitude sum_d' |q k|: the error that even correctly
+    rounded fp32 scores leave when logits span hundreds (outlier channels in
+    both K and V). p, o, k, v are the oracle's fp64 quantities; C = 8 covers the
+    error growth of a 128-term fp32 dot product and the fp32 decode of k."""
+    K = orc.dequant(kref, full)[layer]
+    V = orc.dequant(vref, full)[layer]
+    q = (np.asarray(qb, np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    B, Hq, _ = q.shape
+    H = K.shape[0]
+    G = Hq // H
+    tol = np.full((B, Hq, D), ATTN_ATOL)
+    for b in range(B):
+        n = int(ctx[b])
+        if n <= 0:
+            continue
+        rows = np.concatenate([np.arange(p * PAGE, p * PAGE + PAGE) for p in table[b][: (n + PAGE - 1) // PAGE]])[:n]
+        for g in range(H):
+            Kg, Vg = K[g][rows], V[g][rows]
+            Q = q[b, g * G:(g + 1) * G]
+            s = sm_scale * (Q @ Kg.T)
+            p = np.exp(s - s.max(1, keepdims=True))
+            p /= p.sum(1, keepdims=True)
+            o = p @ Vg
+            A = sm_scale * (np.abs(Q) @ np.abs(Kg).T)
+            w = p * A * U32
+            for h in range(G):
+                E = w[h] @ np.abs(Vg - o[h][None, :])
+                tol[b, g * G + h] += ATTN_SENS_C * E
+    return tol

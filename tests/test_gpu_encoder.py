@@ -34,8 +34,10 @@ def test_level_codes_exhaustive_nonnegative(lx, orc):
 
 
 def test_level_codes_negative_and_special(lx, orc):
+    """Negative values, subnormals, signed zeros and threshold neighbourhoods in
+    the stage-3 domain |w| < 2 (stage 2 never produces |w| > 1 + 2^-23)."""
     rng = np.random.default_rng(3)
-    w = -np.abs(rng.standard_normal(1 << 22).astype(np.float32)) * 10.0 ** rng.uniform(-8, 0, 1 << 22)
+    w = -np.minimum(np.abs(rng.standard_normal(1 << 22)) * 10.0 ** rng.uniform(-8, 0, 1 << 22), 1.99)
     thr, _ = orc.tables()
     near = np.concatenate([np.arange(int(t) - 300, int(t) + 300, dtype=np.uint32) for t in thr[1:].view(np.uint32)])
     w = np.concatenate([w.astype(np.float32), -near.view(np.float32), near.view(np.float32),
