@@ -159,6 +159,33 @@ lynx_status lynx_decode_attn(const void *q_bf16, const lynx_qkv *k, const lynx_q
                              float *out, float *scores, void *workspace, size_t ws_bytes,
                              uint32_t *dev_err, void *stream);
 
+/*
+ * Decode attention without a caller-provided workspace. (The Lynx reading has
+ * no counterpart for this call: it serves callers that cannot allocate device
+ * memory, such as a serving engine whose pool has already claimed all free
+ * memory for the KV cache, a plugin that is handed only its input and output
+ * buffers, or a latency-critical path where cudaMalloc, which may synchronise
+ * the device, is not allowed.)
+ * Same arguments and results as lynx_decode_attn, minus the workspace: the
+ * split-K partials go to a fixed array of LYNX_NOALLOC_SCRATCH_BYTES inside
+ * the library, which every GPU that loads the library holds until the process
+ * exits. The call allocates nothing.
+ *  - Returns LYNX_ERR_WORKSPACE, without launching, when this batch shape needs
+ *    more than LYNX_NOALLOC_SCRATCH_BYTES (compare with
+ *    lynx_decode_attn_workspace(batch, q_heads, max_pages)).
+ *  - The first call on each device looks up the array's device address once
+ *    (a host-side query); make that first call before any stream capture.
+ *  - Every call on a device shares the one array, and it keeps whatever the
+ *    previous call left there (nothing in it needs to start at zero: each
+ *    partial is written before it is read). Calls that overlap on the GPU,
+ *    e.g. on two streams at once, race on it; serialise them.
+ */
+#define LYNX_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+lynx_status lynx_decode_attn_noalloc(const void *q_bf16, const lynx_qkv *k, const lynx_qkv *v, int32_t layer,
+                                     const int32_t *page_table, const int32_t *ctx_lens, int32_t batch,
+                                     int32_t q_heads, int32_t max_pages, float sm_scale, lynx_mode mode,
+                                     float *out, float *scores, uint32_t *dev_err, void *stream);
+
 /* Human-readable name of a status. Never NULL. */
 const char *lynx_status_string(lynx_status s);
 

@@ -67,6 +67,10 @@ def _lib():
             L.lynx_decode_attn.argtypes = [vp, ctypes.POINTER(LynxQKV), ctypes.POINTER(LynxQKV), i32, vp, vp,
                                            i32, i32, i32, ctypes.c_float, ctypes.c_int, vp, vp, vp,
                                            ctypes.c_size_t, vp, vp]
+            L.lynx_decode_attn_noalloc.argtypes = [vp, ctypes.POINTER(LynxQKV), ctypes.POINTER(LynxQKV), i32,
+                                                   vp, vp, i32, i32, i32, ctypes.c_float, ctypes.c_int, vp, vp,
+                                                   vp, vp]
+            L.lynx_decode_attn_noalloc.restype = ctypes.c_int
             L.lynx_host_tables.argtypes = [vp, vp]
             L.lynx_host_tables.restype = None
             L.lynx_level_codes.argtypes = [vp, i64, vp, vp]
@@ -216,6 +220,28 @@ def decode_attn(q, k: QuantizedKV, v: QuantizedKV, layer, page_table, ctx_lens, 
                                    _ptr(scores), _ptr(workspace), workspace.numel() * workspace.element_size(),
                                    _ptr(dev_err), _stream(stream)),
            "lynx_decode_attn")
+    return out
+
+
+NOALLOC_SCRATCH_BYTES = 16 << 20
+
+
+def decode_attn_noalloc(q, k: QuantizedKV, v: QuantizedKV, layer, page_table, ctx_lens, sm_scale, mode,
+                        out=None, scores=None, dev_err=None, stream=None):
+    """lynx_decode_attn_noalloc: decode attention for callers that cannot
+    allocate device memory. Its split-K scratch is a fixed 16 MiB array inside
+    the library, shared by every call on the device (serialise calls)."""
+    _dev(q, torch.bfloat16, "q")
+    _dev(page_table, torch.int32, "page_table")
+    _dev(ctx_lens, torch.int32, "ctx_lens")
+    B, Hq, _ = q.shape
+    if out is None:
+        out = torch.empty((B, Hq, HEAD_DIM), dtype=torch.float32, device=q.device)
+    kd, vd = k.desc(), v.desc()
+    _check(_lib().lynx_decode_attn_noalloc(_ptr(q), ctypes.byref(kd), ctypes.byref(vd), layer, _ptr(page_table),
+                                           _ptr(ctx_lens), B, Hq, page_table.shape[1], float(sm_scale), int(mode),
+                                           _ptr(out), _ptr(scores), _ptr(dev_err), _stream(stream)),
+           "lynx_decode_attn_noalloc")
     return out
 
 
