@@ -187,12 +187,15 @@ class Workload:
     def launches_per_step(self):
         return 6 + 2 * 2 * self.L
 
-    def step(self, ev=None):
-        """ev: optional dict name -> list of (start, end) event pairs to record."""
+    def step(self, ev=None, only=None):
+        """ev: optional dict name -> list of (start, end) event pairs to record;
+        only: run just this kernel group (single-kernel measurements)."""
         lx, torch = self.lx, self.torch
         st = torch.cuda.current_stream()
 
         def mark(name, fn):
+            if only is not None and name != only:
+                return
             if ev is None:
                 fn()
                 return
@@ -295,9 +298,10 @@ def run_gpu(args):
                "sample": f"layer 0, {W3.H} KV heads x {args.cpu_pages} pages (K and V) of the full cache: "
                          f"encode, both decodes, decode attention both modes; {dt:.1f} s"}
 
-    wl = Workload(torch, lx)
+    wl = Workload(torch, lx, layers=args.layers)
+    only = args.only
     for _ in range(args.warmup):
-        wl.step()
+        wl.step(only=only)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
@@ -308,7 +312,7 @@ def run_gpu(args):
         start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         start.record()
         for _ in range(args.steps):
-            wl.step(ev)
+            wl.step(ev, only=only)
         end.record()
         torch.cuda.synchronize()
     ms_step = start.elapsed_time(end) / args.steps
@@ -319,6 +323,8 @@ def run_gpu(args):
         dist.barrier()
 
     nbytes = wl.algorithmic_bytes()
+    if only is not None:
+        nbytes = {only: nbytes[only]}
     hbm, peak_kind = peaks()
     per = {}
     for name, pairs in ev.items():
@@ -343,10 +349,11 @@ def run_gpu(args):
     else:
         ach = per[dom]["GB/s"]
     total_bytes = sum(nbytes.values())
+    wl_layers = wl.L
     value = world * total_bytes / (ms_step * 1e-3) / 1e9
 
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and only is None:
         del wl
         torch.cuda.empty_cache()
         e2e = e2e_measure(torch, lx, args.e2e_layers, max(1, min(args.steps, 3)), 1)
@@ -357,17 +364,19 @@ def run_gpu(args):
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": W3.name, "layers": W3.L, "kv_heads": W3.H, "tokens": W3.T, "head_dim": D,
+            "config": {"workload": W3.name if wl_layers == W3.L else f"{W3.name} (first {wl_layers} layers)",
+                       "layers": wl_layers, "kv_heads": W3.H, "tokens": W3.T, "head_dim": D,
+                       "only": only,
                        "q_heads": HQ, "batch": 1, "io": "bf16 in, 4+4-bit planes, bf16 dense cache",
                        "parallelism": f"replicas x{world}", "l2": "every input larger than L2, no flush"},
             "roofline": {"bound": "hbm", "kernel": dom, "achieved": ach, "peak": hbm, "unit": "GB/s",
                          "frac": ach / hbm, "peak_kind": peak_kind, "traffic": None},
             "per_kernel": per,
-            "decode_tokens_per_s": {"anchor": per["decode_attn_anchor"]["tokens_per_s"],
-                                    "full": per["decode_attn_full"]["tokens_per_s"]},
+            "decode_tokens_per_s": {m: per[f"decode_attn_{m}"]["tokens_per_s"] for m in ("anchor", "full")
+                                    if f"decode_attn_{m}" in per},
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": wl_launches(args.steps, W3.L),
+            "gpu_launches": wl_launches(args.steps, wl_layers, only),
             "clocks": clk.summary(),
         }
         print(json.dumps(line))
@@ -375,9 +384,10 @@ def run_gpu(args):
         dist.destroy_process_group()
 
 
-def wl_launches(steps, L):
+def wl_launches(steps, L, only=None):
     # quantize x2, dequant x2, refine x2, attention split+combine x2 modes x L layers
-    return steps * (6 + 2 * 2 * L)
+    per = {"quantize": 2, "dequant_anchor": 2, "refine": 2, "decode_attn_anchor": 2 * L, "decode_attn_full": 2 * L}
+    return steps * (sum(per.values()) if only is None else per[only])
 
 
 def run_reference(args):
@@ -411,6 +421,10 @@ def main():
     ap.add_argument("--e2e-layers", type=int, default=12)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", choices=["quantize", "dequant_anchor", "refine", "decode_attn_anchor",
+                                       "decode_attn_full"], default=None,
+                    help="time one kernel group only (for profiler captures on smaller cases)")
+    ap.add_argument("--layers", type=int, default=None, help="layers of the cache (default: all 94)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
