@@ -13,6 +13,7 @@
 //
 // Work unit: one 32-token chunk of one (layer, head, page) = 4096 elements,
 // owned by one warp; lane l decodes channels 8(l%16)..+7 of rows 2i + l/16.
+// Code bytes are assembled four at a time with word-wide nibble masks.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -34,14 +35,19 @@ struct Params {
 template <bool FULL, bool F32>
 __global__ void __launch_bounds__(kThreads) dequant_kernel(Params p, LevelTable lev)
 {
-    __shared__ float lut[FULL ? 256 : 16];
-    for (int i = threadIdx.x; i < (FULL ? 256 : 16); i += kThreads)
-        lut[i] = FULL ? lev.full[i] : lev.anchor[i];
+    // Full mode: 256 signed level values, replicated 32 times so that lane l
+    // reads only bank l (random codes would otherwise conflict); anchor mode:
+    // 16 values, one word per bank already.
+    constexpr int kLut = FULL ? 256 * 32 : 16;
+    __shared__ float lut[kLut];
+    for (int i = threadIdx.x; i < kLut; i += kThreads)
+        lut[i] = FULL ? lev.full[i >> 5] : lev.anchor[i];
     __syncthreads();
 
     const int lane = threadIdx.x & 31;
     const int cg = lane & 15;        // channel group: channels 8cg..8cg+7
     const int rp = lane >> 4;        // row parity
+    const float *lut_lane = FULL ? lut + lane : lut;
     const int64_t wstride = (int64_t)gridDim.x * (kThreads / 32);
     for (int64_t u = blockIdx.x * (int64_t)(kThreads / 32) + (threadIdx.x >> 5); u < p.units; u += wstride) {
         const int64_t page = u >> 3;
@@ -78,12 +84,23 @@ __global__ void __launch_bounds__(kThreads) dequant_kernel(Params p, LevelTable 
 #pragma unroll
         for (int it = 0; it < 16; ++it) {
             const int64_t row = row0 + 2 * it;
+            // code bytes of the even and of the odd channels, four per word:
+            // full (A << 4 | r), anchor-only A
+            uint32_t ev, od;
+            if (FULL) {
+                ev = ((aw[it] << 4) & 0xF0F0F0F0u) | (rw[it] & 0x0F0F0F0Fu);
+                od = (aw[it] & 0xF0F0F0F0u) | ((rw[it] >> 4) & 0x0F0F0F0Fu);
+            } else {
+                ev = aw[it] & 0x0F0F0F0Fu;
+                od = (aw[it] >> 4) & 0x0F0F0F0Fu;
+            }
             float x[8];
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                const uint32_t an = (aw[it] >> (4 * c)) & 15u;
-                const uint32_t idx = FULL ? ((an << 4) | ((rw[it] >> (4 * c)) & 15u)) : an;
-                x[c] = fmaf(b[c], lut[idx], a[c]);
+            for (int k = 0; k < 4; ++k) {
+                const uint32_t ie = __byte_perm(ev, 0u, 0x4440u | k);
+                const uint32_t io = __byte_perm(od, 0u, 0x4440u | k);
+                x[2 * k] = fmaf(b[2 * k], lut_lane[FULL ? ie * 32 : ie], a[2 * k]);
+                x[2 * k + 1] = fmaf(b[2 * k + 1], lut_lane[FULL ? io * 32 : io], a[2 * k + 1]);
             }
             if (F32) {
                 float4 *o = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + row * kD + cg * 8);

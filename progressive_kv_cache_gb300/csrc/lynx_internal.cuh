@@ -34,6 +34,17 @@ struct MapTable {
     uint2 e[kNBucket + 1];
 };
 
+// The same buckets as the encoder uses them: entry 0 catches |w| below the
+// first bucket (and NaN), entry 1 + i is bucket i. Each entry holds the bits
+// of the threshold inside the bucket (an all-ones NaN pattern when there is
+// none, so the compare fails) and the four possible stored bytes
+// (c + 7) & 0xFF, selected by 2*(w < 0) + (|w| >= threshold):
+//   byte 0: w >= 0 below the threshold   byte 1: w >= 0 at or above it
+//   byte 2: w < 0 below the threshold    byte 3: w < 0 at or above it
+struct CodeTable {
+    uint2 e[kNBucket + 1];
+};
+
 // Signed level values used by the decoders:
 //   full[(A & 15) << 4 | r] = sgn(c) * Lv[min(|c|, 64)], c = 16A + r - 7
 //   anchor[A & 15]          = sgn(16A) * Lv[min(|16A|, 64)]
@@ -46,6 +57,7 @@ struct HostTables {
     float thr[64];
     uint16_t lv[65];
     MapTable map;
+    CodeTable code;
     LevelTable lev;
     bool ok;
 };

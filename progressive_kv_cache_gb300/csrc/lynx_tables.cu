@@ -74,6 +74,16 @@ void build(HostTables &t)
     t.map.e[kNBucket] = make_uint2(0xFFFFFFFFu, 0u);
     (void)f32_from_bits;
 
+    // biased code bytes for the encoder's table (sentinel first)
+    auto byte_of = [](int c) { return (uint32_t)(c + kBias) & 0xFFu; };
+    for (int i = 0; i <= kNBucket; ++i) {
+        const uint2 m = i == 0 ? t.map.e[kNBucket] : t.map.e[i - 1];
+        const int q0 = (int)m.y, q1 = q0 + 1 > kQMax ? kQMax : q0 + 1;
+        const int n0 = -(q0 > 1 ? q0 : 1), n1 = -(q1 > 1 ? q1 : 1);
+        const uint32_t bytes = byte_of(q0) | (byte_of(q1) << 8) | (byte_of(n0) << 16) | (byte_of(n1) << 24);
+        t.code.e[i] = make_uint2(m.x, bytes);
+    }
+
     // decoder levels
     for (int an = 0; an < 16; ++an) {
         int A = an >= 8 ? an - 16 : an;

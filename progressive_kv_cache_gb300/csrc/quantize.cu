@@ -7,14 +7,18 @@
 // alpha-law log map onto 127 levels with sign-aware mapping of negatives;
 // (4) the +7 round-half-down bias and the 4-bit anchor / 4-bit residual cut.
 //
-// Layout of the work: a persistent CTA (one per SM) walks pages; each page
-// (256 x 128 bf16 = 64 KiB, contiguous in [L][H][T][128]) is prefetched into
-// one of two shared-memory buffers with a single bulk copy while the previous
-// page is encoded. Warp j owns chunk j (32 tokens); lane l owns channels
-// 4l..4l+3, so the chunk reduction tree of the numeric contract runs inside one
-// thread's registers. The packed planes are staged in shared memory and leave
-// with two 16 KiB bulk stores; the metadata goes out with direct 8/16-byte
-// stores.
+// Layout of the work: a persistent CTA (one per SM, 16 warps) walks pages;
+// each page (256 x 128 bf16 = 64 KiB, contiguous in [L][H][T][128]) is
+// prefetched into one of two shared-memory buffers with a single bulk copy
+// while the previous page is encoded. Warp w owns chunk w/2 (32 tokens) and
+// half the channels; lane l owns one channel pair, so the chunk reduction tree
+// of the numeric contract runs inside one thread's registers. Stage 3 is one
+// lookup in a 16-way replicated bucket table (a conflict-free 8-byte load per
+// element) whose entry carries the four possible stored bytes, then one
+// compare and one byte permute. The packed planes are staged in shared memory
+// and leave with two 16 KiB bulk stores; the metadata goes out with direct
+// 4/8-byte stores.
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
 #include "lynx_internal.cuh"
@@ -23,18 +27,20 @@
 namespace lynx {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;
+constexpr int kCopies = 16;                            // table replicas (one per half-warp lane)
 constexpr uint32_t kPageBytes = kPage * kD * 2;       // 64 KiB of bf16
 constexpr uint32_t kPlaneBytes = kPage * kD / 2;      // 16 KiB per plane and page
 constexpr uint32_t kWaitLimit = 1u << 22;
+constexpr uint32_t kClampLoBits = (kBucketBase << 19) - 1u;   // largest float below 2^-13
 
 struct Smem {
     uint16_t x[2][kPage * kD];         // double-buffered input page
     uint8_t anc[kPage * kD / 2];       // staged anchor plane of the page
     uint8_t res[kPage * kD / 2];       // staged residual plane of the page
-    float pmin[kNChunk][kD];
-    float pmax[kNChunk][kD];
-    uint2 tab[kNBucket + 1];
+    uint32_t pmin[kNChunk][kD / 2];    // bf16x2 chunk minima of channel pairs
+    uint32_t pmax[kNChunk][kD / 2];
+    uint2 tab[(kNBucket + 1) * kCopies];
     alignas(8) uint64_t bar[2];
 };
 
@@ -48,79 +54,113 @@ struct Params {
     int P;          // pages per (layer, head)
 };
 
-// Stage 3: level count by bucket lookup plus one compare (equal to the count
-// #{k : |w| >= T_k} for every finite w), then the sign-aware code.
-__device__ __forceinline__ int level_code(float w, const uint2 *tab)
+__device__ __forceinline__ uint2 lds_u2(uint32_t addr)
 {
-    const uint32_t ab = __float_as_uint(w) & 0x7FFFFFFFu;
-    const uint32_t idx = min((ab >> 19) - kBucketBase, (uint32_t)kNBucket);
-    const uint2 e = tab[idx];
-    const int q = (int)e.y + (ab >= e.x ? 1 : 0);
-    return (w < 0.0f) ? -max(q, 1) : q;
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+    return v;
 }
 
-// Stages 2-4 for one channel of one chunk held in registers u[0..31].
-// NC = 32 for a full chunk; otherwise nc valid tokens (runtime).
+// Stage 3 + the +7 bias for one value: the stored byte (c + 7) & 0xFF, whose
+// high nibble is the anchor and low nibble the residual. `tab_base` is the
+// shared address of this lane's table replica, offset so that the bucket
+// number (float bits >> 19) indexes it directly.
+__device__ __forceinline__ uint32_t code_byte(float w, uint32_t tab_base)
+{
+    const float a = fabsf(w);
+    const float cl = fmaxf(a, __uint_as_float(kClampLoBits));
+    const uint2 e = lds_u2(tab_base + (__float_as_uint(cl) >> 19) * (kCopies * 8));
+    const uint32_t sel = (a >= __uint_as_float(e.x) ? 1u : 0u) | (w < 0.0f ? 2u : 0u);
+    return __byte_perm(e.y, 0u, sel);
+}
+
+__device__ __forceinline__ uint32_t bf2_min(uint32_t a, uint32_t b)
+{
+    __nv_bfloat162 r = __hmin2(*reinterpret_cast<__nv_bfloat162 *>(&a), *reinterpret_cast<__nv_bfloat162 *>(&b));
+    return *reinterpret_cast<uint32_t *>(&r);
+}
+
+__device__ __forceinline__ uint32_t bf2_max(uint32_t a, uint32_t b)
+{
+    __nv_bfloat162 r = __hmax2(*reinterpret_cast<__nv_bfloat162 *>(&a), *reinterpret_cast<__nv_bfloat162 *>(&b));
+    return *reinterpret_cast<uint32_t *>(&r);
+}
+
+// Stages 2-4 for this thread's two channels of one chunk; `full` chunks have
+// 32 valid tokens, others nc. Writes the staged plane bytes and returns the
+// chunk metadata (mean, scale) of both channels as fp16x2 words.
 template <bool FULL>
-__device__ __forceinline__ void chunk_channel(const float (&u)[kChunk], int nc, const uint2 *tab, int shift,
-                                              uint32_t (&packed)[kChunk], __half &mu_out, __half &s_out)
+__device__ __forceinline__ void encode_chunk(float (&u0)[kChunk], float (&u1)[kChunk], int nc, uint32_t tab_base,
+                                             uint8_t *anc_row0, uint8_t *res_row0, uint32_t &mu2, uint32_t &s2)
 {
     // chunk mean: stride-halving pairwise tree over 32 slots, absent slots +0
-    float t[16];
+    float t0[16], t1[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-        const float a = (FULL || i < nc) ? u[i] : 0.0f;
-        const float b = (FULL || i + 16 < nc) ? u[i + 16] : 0.0f;
-        t[i] = __fadd_rn(a, b);
+        t0[i] = __fadd_rn((FULL || i < nc) ? u0[i] : 0.0f, (FULL || i + 16 < nc) ? u0[i + 16] : 0.0f);
+        t1[i] = __fadd_rn((FULL || i < nc) ? u1[i] : 0.0f, (FULL || i + 16 < nc) ? u1[i + 16] : 0.0f);
     }
 #pragma unroll
     for (int h = 8; h >= 1; h >>= 1)
 #pragma unroll
-        for (int i = 0; i < h; ++i)
-            t[i] = __fadd_rn(t[i], t[i + h]);
-    const float mean = FULL ? __fdiv_rn(t[0], 32.0f) : __fdiv_rn(t[0], (float)nc);
-    const __half mu_h = __float2half_rn(mean);
-    const float mu = __half2float(mu_h);
+        for (int i = 0; i < h; ++i) {
+            t0[i] = __fadd_rn(t0[i], t0[i + h]);
+            t1[i] = __fadd_rn(t1[i], t1[i + h]);
+        }
+    const float ncf = (float)nc;
+    const __half mh0 = __float2half_rn(FULL ? __fdiv_rn(t0[0], 32.0f) : __fdiv_rn(t0[0], ncf));
+    const __half mh1 = __float2half_rn(FULL ? __fdiv_rn(t1[0], 32.0f) : __fdiv_rn(t1[0], ncf));
+    const float mu0 = __half2float(mh0), mu1 = __half2float(mh1);
 
-    float s = 0.0f;
+    float s0 = 0.0f, s1 = 0.0f;
 #pragma unroll
-    for (int i = 0; i < kChunk; ++i)
-        if (FULL || i < nc)
-            s = fmaxf(s, fabsf(__fsub_rn(u[i], mu)));
-    const __half s_h = __float2half_ru(s);
-    const float sf = __half2float(s_h);
-    const float inv_s = sf > 0.0f ? __frcp_rn(sf) : 0.0f;
+    for (int i = 0; i < kChunk; ++i) {
+        u0[i] = __fsub_rn(u0[i], mu0);   // u becomes v = u - mu
+        u1[i] = __fsub_rn(u1[i], mu1);
+        if (FULL || i < nc) {
+            s0 = fmaxf(s0, fabsf(u0[i]));
+            s1 = fmaxf(s1, fabsf(u1[i]));
+        }
+    }
+    const __half sh0 = __float2half_ru(s0), sh1 = __float2half_ru(s1);
+    const float sf0 = __half2float(sh0), sf1 = __half2float(sh1);
+    const float is0 = sf0 > 0.0f ? __frcp_rn(sf0) : 0.0f;
+    const float is1 = sf1 > 0.0f ? __frcp_rn(sf1) : 0.0f;
 
 #pragma unroll
     for (int i = 0; i < kChunk; ++i) {
-        int c = 0;
-        if (FULL || i < nc)
-            c = level_code(__fmul_rn(__fsub_rn(u[i], mu), inv_s), tab);
-        const uint32_t b = (uint32_t)(c + kBias) & 0xFFu;   // anchor nibble high, residual low
-        // bits 0..15: anchor nibbles of the thread's 4 channels; 16..31: residual nibbles
-        packed[i] |= ((b >> 4) << shift) | ((b & 15u) << (16 + shift));
+        uint32_t ab = 0x00u, rb = 0x77u;                 // code 0: anchor 0, residual 7
+        if (FULL || i < nc) {
+            const uint32_t b0 = code_byte(__fmul_rn(u0[i], is0), tab_base);
+            const uint32_t b1 = code_byte(__fmul_rn(u1[i], is1), tab_base);
+            ab = ((b0 >> 4) & 0x0Fu) | (b1 & 0xF0u);
+            rb = (b0 & 0x0Fu) | ((b1 << 4) & 0xF0u);
+        }
+        anc_row0[i * (kD / 2)] = (uint8_t)ab;
+        res_row0[i * (kD / 2)] = (uint8_t)rb;
     }
-    mu_out = mu_h;
-    s_out = s_h;
+    mu2 = (uint32_t)__half_as_ushort(mh0) | ((uint32_t)__half_as_ushort(mh1) << 16);
+    s2 = (uint32_t)__half_as_ushort(sh0) | ((uint32_t)__half_as_ushort(sh1) << 16);
 }
 
-__global__ void __launch_bounds__(kThreads, 1) quantize_kernel(Params p, MapTable map)
+__global__ void __launch_bounds__(kThreads, 1) quantize_kernel(Params p, CodeTable table)
 {
     extern __shared__ __align__(128) unsigned char smem_raw[];
     Smem &sm = *reinterpret_cast<Smem *>(smem_raw);
     const int tid = threadIdx.x;
-    const int j = tid >> 5;         // chunk of this warp
-    const int lane = tid & 31;
-    const int d0 = lane * 4;        // first of this thread's 4 channels
+    const int warp = tid >> 5, lane = tid & 31;
+    const int j = warp >> 1;                       // chunk of this warp
+    const int pi = (warp & 1) * 32 + lane;         // channel pair: channels 2pi, 2pi+1
 
-    for (int i = tid; i <= kNBucket; i += kThreads)
-        sm.tab[i] = map.e[i];
+    for (int i = tid; i < (kNBucket + 1) * kCopies; i += kThreads)
+        sm.tab[i] = table.e[i / kCopies];
     if (tid == 0) {
         mbar_init(&sm.bar[0], 1);
         mbar_init(&sm.bar[1], 1);
         fence_mbar_init();
     }
     __syncthreads();
+    const uint32_t tab_base = smem_u32(&sm.tab[lane & (kCopies - 1)]) - (kBucketBase - 1u) * (kCopies * 8);
 
     const int64_t first = blockIdx.x, stride = gridDim.x;
     if (tid == 0 && first < p.pages) {
@@ -129,11 +169,10 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_kernel(Params p, MapTabl
     }
 
     int k = 0;
-    bool prefetched = false;
     for (int64_t page = first; page < p.pages; page += stride, ++k) {
         const int buf = k & 1;
         const int64_t next = page + stride;
-        prefetched = false;
+        bool prefetched = false;
         if (tid == 0 && next < p.pages) {
             fence_proxy_async_smem();
             mbar_arrive_expect_tx(&sm.bar[buf ^ 1], kPageBytes);
@@ -152,108 +191,78 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_kernel(Params p, MapTabl
         n = min(max(n, 0), kPage);
         const int nc = min(max(n - j * kChunk, 0), kChunk);
 
-        // (a) this thread's 32 tokens x 4 channels
-        const uint16_t *xs = sm.x[buf];
-        uint2 xr[kChunk];
+        // (a) this thread's 32 tokens x 2 channels, and their chunk min/max
+        const uint16_t *xs = sm.x[buf] + j * kChunk * kD + 2 * pi;
+        uint32_t xw[kChunk];
 #pragma unroll
         for (int i = 0; i < kChunk; ++i)
-            xr[i] = *reinterpret_cast<const uint2 *>(xs + (j * kChunk + i) * kD + d0);
-
-        // (b) stage 1 statistics: chunk-local min/max, then across the page
+            xw[i] = *reinterpret_cast<const uint32_t *>(xs + i * kD);
         {
-            float lmin[4], lmax[4];
+            uint32_t mn2 = 0x7F807F80u, mx2 = 0xFF80FF80u;   // +inf, -inf pairs
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                lmin[c] = __int_as_float(0x7F800000);
-                lmax[c] = -__int_as_float(0x7F800000);
-            }
-#pragma unroll
-            for (int i = 0; i < kChunk; ++i) {
+            for (int i = 0; i < kChunk; ++i)
                 if (i < nc) {
-                    const float v0 = bf16_lo(xr[i].x), v1 = bf16_hi(xr[i].x);
-                    const float v2 = bf16_lo(xr[i].y), v3 = bf16_hi(xr[i].y);
-                    lmin[0] = fminf(lmin[0], v0); lmax[0] = fmaxf(lmax[0], v0);
-                    lmin[1] = fminf(lmin[1], v1); lmax[1] = fmaxf(lmax[1], v1);
-                    lmin[2] = fminf(lmin[2], v2); lmax[2] = fmaxf(lmax[2], v2);
-                    lmin[3] = fminf(lmin[3], v3); lmax[3] = fmaxf(lmax[3], v3);
+                    mn2 = bf2_min(mn2, xw[i]);
+                    mx2 = bf2_max(mx2, xw[i]);
                 }
-            }
-            *reinterpret_cast<float4 *>(&sm.pmin[j][d0]) = make_float4(lmin[0], lmin[1], lmin[2], lmin[3]);
-            *reinterpret_cast<float4 *>(&sm.pmax[j][d0]) = make_float4(lmax[0], lmax[1], lmax[2], lmax[3]);
+            sm.pmin[j][pi] = mn2;
+            sm.pmax[j][pi] = mx2;
         }
         if (tid == 0)
             bulk_wait_read_all();   // the previous page's planes have left the staging tile
         __syncthreads();
 
-        float mn[4], rng[4], inv_r[4];
+        // (b) stage 1 over the page
+        uint32_t mn2 = sm.pmin[0][pi], mx2 = sm.pmax[0][pi];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            float a = sm.pmin[0][d0 + c], b = sm.pmax[0][d0 + c];
-#pragma unroll
-            for (int jj = 1; jj < kNChunk; ++jj) {
-                a = fminf(a, sm.pmin[jj][d0 + c]);
-                b = fmaxf(b, sm.pmax[jj][d0 + c]);
-            }
-            if (n == 0)
-                a = b = 0.0f;
-            a = __fadd_rn(a, 0.0f);   // a zero minimum or maximum is +0
-            b = __fadd_rn(b, 0.0f);
-            mn[c] = a;
-            rng[c] = __fsub_rn(b, a);
-            inv_r[c] = rng[c] > 0.0f ? __frcp_rn(rng[c]) : 0.0f;
+        for (int jj = 1; jj < kNChunk; ++jj) {
+            mn2 = bf2_min(mn2, sm.pmin[jj][pi]);
+            mx2 = bf2_max(mx2, sm.pmax[jj][pi]);
         }
+        float mn0 = bf16_lo(mn2), mn1 = bf16_hi(mn2), mx0 = bf16_lo(mx2), mx1 = bf16_hi(mx2);
+        if (n == 0)
+            mn0 = mn1 = mx0 = mx1 = 0.0f;
+        mn0 = __fadd_rn(mn0, 0.0f);   // a zero extreme is +0
+        mn1 = __fadd_rn(mn1, 0.0f);
+        mx0 = __fadd_rn(mx0, 0.0f);
+        mx1 = __fadd_rn(mx1, 0.0f);
+        const float rg0 = __fsub_rn(mx0, mn0), rg1 = __fsub_rn(mx1, mn1);
+        const float ir0 = rg0 > 0.0f ? __frcp_rn(rg0) : 0.0f;
+        const float ir1 = rg1 > 0.0f ? __frcp_rn(rg1) : 0.0f;
 
-        // stages 2-4, channel by channel; codes packed per token
-        uint32_t packed[kChunk];
-#pragma unroll
-        for (int i = 0; i < kChunk; ++i)
-            packed[i] = 0;
-        __half mu_h[4], s_h[4];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            float u[kChunk];
-#pragma unroll
-            for (int i = 0; i < kChunk; ++i) {
-                const uint32_t w = (c < 2) ? xr[i].x : xr[i].y;
-                const float x = (c & 1) ? bf16_hi(w) : bf16_lo(w);
-                u[i] = __fmul_rn(__fsub_rn(x, mn[c]), inv_r[c]);
-            }
-            if (nc == kChunk) {
-                chunk_channel<true>(u, nc, sm.tab, 4 * c, packed, mu_h[c], s_h[c]);
-            } else if (nc > 0) {
-                chunk_channel<false>(u, nc, sm.tab, 4 * c, packed, mu_h[c], s_h[c]);
-            } else {
-#pragma unroll
-                for (int i = 0; i < kChunk; ++i)
-                    packed[i] |= (uint32_t)kBias << (16 + 4 * c);   // code 0: anchor 0, residual 7
-                mu_h[c] = __ushort_as_half(0);
-                s_h[c] = __ushort_as_half(0);
-            }
-        }
-
-        // stage the planes: anchor bytes (d0, d0+1), (d0+2, d0+3) of each token
+        float u0[kChunk], u1[kChunk];
 #pragma unroll
         for (int i = 0; i < kChunk; ++i) {
-            const int row = j * kChunk + i;
-            *reinterpret_cast<uint16_t *>(&sm.anc[row * (kD / 2) + lane * 2]) = (uint16_t)(packed[i] & 0xFFFFu);
-            *reinterpret_cast<uint16_t *>(&sm.res[row * (kD / 2) + lane * 2]) = (uint16_t)(packed[i] >> 16);
+            u0[i] = __fmul_rn(__fsub_rn(bf16_lo(xw[i]), mn0), ir0);
+            u1[i] = __fmul_rn(__fsub_rn(bf16_hi(xw[i]), mn1), ir1);
         }
 
-        // metadata: page (min, range) from warp 0; chunk (mean, scale) from every thread
+        // (c) stages 2-4
+        uint8_t *anc_row0 = sm.anc + j * kChunk * (kD / 2) + pi;
+        uint8_t *res_row0 = sm.res + j * kChunk * (kD / 2) + pi;
+        uint32_t mu2 = 0, s2 = 0;
+        if (nc == kChunk) {
+            encode_chunk<true>(u0, u1, nc, tab_base, anc_row0, res_row0, mu2, s2);
+        } else if (nc > 0) {
+            encode_chunk<false>(u0, u1, nc, tab_base, anc_row0, res_row0, mu2, s2);
+        } else {
+#pragma unroll
+            for (int i = 0; i < kChunk; ++i) {
+                anc_row0[i * (kD / 2)] = 0x00u;
+                res_row0[i * (kD / 2)] = 0x77u;
+            }
+        }
+
+        // metadata: page (min, range) from chunk 0's warps; chunk (mean, scale) from every thread
         if (j == 0) {
-            float *pm = p.pm + page * (int64_t)(2 * kD);
-            *reinterpret_cast<float4 *>(pm + d0) = make_float4(mn[0], mn[1], mn[2], mn[3]);
-            *reinterpret_cast<float4 *>(pm + kD + d0) = make_float4(rng[0], rng[1], rng[2], rng[3]);
+            float *pm = p.pm + page * (int64_t)(2 * kD) + 2 * pi;
+            *reinterpret_cast<float2 *>(pm) = make_float2(mn0, mn1);
+            *reinterpret_cast<float2 *>(pm + kD) = make_float2(rg0, rg1);
         }
         {
-            uint16_t *cm = p.cm + (page * kNChunk + j) * (int64_t)(2 * kD);
-            uint2 mu2, s2;
-            mu2.x = (uint32_t)__half_as_ushort(mu_h[0]) | ((uint32_t)__half_as_ushort(mu_h[1]) << 16);
-            mu2.y = (uint32_t)__half_as_ushort(mu_h[2]) | ((uint32_t)__half_as_ushort(mu_h[3]) << 16);
-            s2.x = (uint32_t)__half_as_ushort(s_h[0]) | ((uint32_t)__half_as_ushort(s_h[1]) << 16);
-            s2.y = (uint32_t)__half_as_ushort(s_h[2]) | ((uint32_t)__half_as_ushort(s_h[3]) << 16);
-            *reinterpret_cast<uint2 *>(cm + d0) = mu2;
-            *reinterpret_cast<uint2 *>(cm + kD + d0) = s2;
+            uint16_t *cm = p.cm + (page * kNChunk + j) * (int64_t)(2 * kD) + 2 * pi;
+            *reinterpret_cast<uint32_t *>(cm) = mu2;
+            *reinterpret_cast<uint32_t *>(cm + kD) = s2;
         }
         __syncthreads();
         if (tid == 0) {
@@ -267,15 +276,22 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_kernel(Params p, MapTabl
         bulk_wait_all();
 }
 
+// The encoder's stage-3 path on arbitrary values (a diagnostic): the same
+// table and code_byte(), with |w| clamped below 2 first so that any input
+// stays inside the table (the encoder itself never sees |w| > 1 + 2^-23).
 __global__ void level_codes_kernel(const float *__restrict__ w, int64_t n, int8_t *__restrict__ codes,
-                                   MapTable map)
+                                   CodeTable table)
 {
-    __shared__ uint2 tab[kNBucket + 1];
-    for (int i = threadIdx.x; i <= kNBucket; i += blockDim.x)
-        tab[i] = map.e[i];
+    __shared__ uint2 tab[(kNBucket + 1) * kCopies];
+    for (int i = threadIdx.x; i < (kNBucket + 1) * kCopies; i += blockDim.x)
+        tab[i] = table.e[i / kCopies];
     __syncthreads();
-    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
-        codes[i] = (int8_t)level_code(w[i], tab);
+    const uint32_t tab_base = smem_u32(&tab[threadIdx.x & (kCopies - 1)]) - (kBucketBase - 1u) * (kCopies * 8);
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        const float v = w[i];
+        const float c = copysignf(fminf(fabsf(v), 1.99999988f), v);
+        codes[i] = (int8_t)((int)(int8_t)code_byte(v == v ? c : v, tab_base) - kBias);
+    }
 }
 
 } // namespace
@@ -295,7 +311,7 @@ cudaError_t launch_quantize(const uint16_t *x, const int32_t *page_valid, const 
         return e;
     Params p{x, page_valid, o.anchor, o.residual, o.page_meta, o.chunk_meta, pages, P};
     const int64_t grid = pages < sms ? pages : sms;
-    quantize_kernel<<<(unsigned)grid, kThreads, smem, s>>>(p, host_tables().map);
+    quantize_kernel<<<(unsigned)grid, kThreads, smem, s>>>(p, host_tables().code);
     return cudaGetLastError();
 }
 
@@ -309,7 +325,7 @@ cudaError_t launch_level_codes(const float *w, int64_t n, int8_t *codes, cudaStr
     int64_t blocks = (n + 255) / 256;
     if (blocks > (int64_t)sms * 8)
         blocks = (int64_t)sms * 8;
-    level_codes_kernel<<<(unsigned)blocks, 256, 0, s>>>(w, n, codes, host_tables().map);
+    level_codes_kernel<<<(unsigned)blocks, 256, 0, s>>>(w, n, codes, host_tables().code);
     return cudaGetLastError();
 }
 
