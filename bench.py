@@ -187,36 +187,56 @@ class Workload:
     def launches_per_step(self):
         return 6 + 2 * 2 * self.L
 
-    def step(self, ev=None, only=None):
-        """ev: optional dict name -> list of (start, end) event pairs to record;
-        only: run just this kernel group (single-kernel measurements)."""
-        lx, torch = self.lx, self.torch
-        st = torch.cuda.current_stream()
+    GROUPS = ("quantize", "dequant_anchor", "refine", "decode_attn_anchor", "decode_attn_full")
 
-        def mark(name, fn):
-            if only is not None and name != only:
-                return
-            if ev is None:
-                fn()
-                return
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(st)
-            fn()
-            b.record(st)
-            ev.setdefault(name, []).append((a, b))
-
+    def units(self):
+        """Each timed unit: (group name, callable issuing its library calls)."""
+        lx = self.lx
+        out = []
         for s in (S.S_K, S.S_V):
-            mark("quantize", lambda s=s: lx.quantize_pages(self.x[s], self.q[s]))
+            out.append(("quantize", lambda s=s: lx.quantize_pages(self.x[s], self.q[s])))
         for s in (S.S_K, S.S_V):
-            mark("dequant_anchor", lambda s=s: lx.dequant_anchor(self.q[s], self.dense[s]))
+            out.append(("dequant_anchor", lambda s=s: lx.dequant_anchor(self.q[s], self.dense[s])))
         for s in (S.S_K, S.S_V):
-            mark("refine", lambda s=s: lx.refine_residual(self.q[s], self.dense[s]))
+            out.append(("refine", lambda s=s: lx.refine_residual(self.q[s], self.dense[s])))
         for mode, name in ((lx.MODE_ANCHOR, "decode_attn_anchor"), (lx.MODE_FULL, "decode_attn_full")):
             def attn(mode=mode):
                 for l in range(self.L):
                     lx.decode_attn(self.qt, self.q[S.S_K], self.q[S.S_V], l, self.table, self.ctx, D ** -0.5,
                                    mode, out=self.out[mode][l], workspace=self.ws)
-            mark(name, attn)
+            out.append((name, attn))
+        return out
+
+    def capture(self, only=None):
+        """One CUDA graph per timed unit (the same library calls, replayed
+        without per-call host overhead)."""
+        torch = self.torch
+        self.graphs = []
+        for name, fn in self.units():
+            if only is not None and name != only:
+                continue
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                fn()
+            self.graphs.append((name, g))
+        torch.cuda.synchronize()
+
+    def step(self, ev=None, only=None, graphs=True):
+        """ev: optional dict name -> list of (start, end) event pairs to record;
+        only: run just this kernel group (single-kernel measurements)."""
+        torch = self.torch
+        st = torch.cuda.current_stream()
+        seq = self.graphs if graphs else [(n, f) for n, f in self.units() if only is None or n == only]
+        for name, item in seq:
+            run = item.replay if graphs else item
+            if ev is None:
+                run()
+                continue
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(st)
+            run()
+            b.record(st)
+            ev.setdefault(name, []).append((a, b))
 
     def algorithmic_bytes(self):
         e = self.elements
@@ -244,16 +264,23 @@ def e2e_measure(torch, lx, layers, steps, warmup):
     d2h = sum(t.numel() * t.element_size() for d in hq.values() for t in d.values()) + \
         sum(t.numel() * t.element_size() for t in hout.values())
 
-    def one():
+    def body():
         for s in hx:
             wl.x[s].copy_(hx[s], non_blocking=True)
-        wl.step()
+        for _, fn in wl.units():
+            fn()
         for s in hq:
             for n, t in hq[s].items():
                 t.copy_(getattr(wl.q[s], n), non_blocking=True)
         for m in hout:
             hout[m].copy_(wl.out[m], non_blocking=True)
 
+    body()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        body()
+    one = graph.replay
     for _ in range(warmup):
         one()
     torch.cuda.synchronize()
@@ -300,8 +327,13 @@ def run_gpu(args):
 
     wl = Workload(torch, lx, layers=args.layers)
     only = args.only
+    use_graphs = not args.no_graph
+    wl.step(only=only, graphs=False)          # first calls: module load, kernel attributes
+    torch.cuda.synchronize()
+    if use_graphs:
+        wl.capture(only=only)
     for _ in range(args.warmup):
-        wl.step(only=only)
+        wl.step(only=only, graphs=use_graphs)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
@@ -312,7 +344,7 @@ def run_gpu(args):
         start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         start.record()
         for _ in range(args.steps):
-            wl.step(ev, only=only)
+            wl.step(ev, only=only, graphs=use_graphs)
         end.record()
         torch.cuda.synchronize()
     ms_step = start.elapsed_time(end) / args.steps
@@ -365,6 +397,7 @@ def run_gpu(args):
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": W3.name if wl_layers == W3.L else f"{W3.name} (first {wl_layers} layers)",
+                       "launch": "CUDA graph per kernel group" if use_graphs else "eager",
                        "layers": wl_layers, "kv_heads": W3.H, "tokens": W3.T, "head_dim": D,
                        "only": only,
                        "q_heads": HQ, "batch": 1, "io": "bf16 in, 4+4-bit planes, bf16 dense cache",
@@ -425,6 +458,8 @@ def main():
                                        "decode_attn_full"], default=None,
                     help="time one kernel group only (for profiler captures on smaller cases)")
     ap.add_argument("--layers", type=int, default=None, help="layers of the cache (default: all 94)")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="issue every library call from Python instead of replaying CUDA graphs of them")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)

@@ -243,7 +243,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_split_kernel(AttnArgs a, Lev
     }
     if (tid < G) {
         float *pp = part + (((int64_t)b * a.Hq + g * G + tid) * a.n_splits + split) * kPart;
-        pp[kD] = sm.m[tid];
+        pp[kD] = sm.m[tid] * 1.4426950408889634f;   // partials carry m in the base-2 log domain
         pp[kD + 1] = sm.l[tid];
     }
 }
@@ -262,7 +262,7 @@ __global__ void __launch_bounds__(kD) attn_combine_kernel(const float *__restric
         for (int s = 0; s < n_splits; ++s) {
             const float l = pp[s * kPart + kD + 1];
             if (l > 0.0f) {
-                const float w = expf(pp[s * kPart + kD] - M);
+                const float w = exp2f(pp[s * kPart + kD] - M);
                 L = fmaf(l, w, L);
                 o = fmaf(pp[s * kPart + d], w, o);
             }
@@ -281,29 +281,45 @@ cudaError_t run(const AttnArgs &a, cudaStream_t s)
         return e;
     dim3 grid((unsigned)a.n_splits, (unsigned)a.H, (unsigned)a.B);
     attn_split_kernel<GMAX, FULL><<<grid, kThreads, smem, s>>>(a, host_tables().lev);
-    e = cudaGetLastError();
-    if (e != cudaSuccess)
-        return e;
-    attn_combine_kernel<<<(unsigned)(a.B * a.Hq), kD, 0, s>>>(a.part, a.n_splits, a.out);
     return cudaGetLastError();
 }
 
 } // namespace
 
-void attn_split_plan(int batch, int max_pages, int sms, int *n_splits, int *pages_per_split)
+void attn_split_plan(int batch, int kv_heads, int max_pages, int sms, int *n_splits, int *pages_per_split)
 {
-    int want = batch > 0 ? (2 * sms + batch - 1) / batch : 1;
-    if (want < 1)
-        want = 1;
-    if (want > max_pages)
-        want = max_pages;
-    if (want < 1)
-        want = 1;
-    int pps = (max_pages + want - 1) / want;
+    // One CTA per SM runs at a time. When the (request, KV head) pairs are
+    // fewer than the SMs, cut each context into as many ranges as fill one
+    // wave; otherwise use short ranges so that many waves balance ragged
+    // context lengths.
+    const long units = (long)(batch > 0 ? batch : 1) * (kv_heads > 0 ? kv_heads : 1);
+    int pps;
+    if (units <= sms) {
+        const int want = (int)(sms / units);
+        pps = (max_pages + want - 1) / want;
+    } else {
+        pps = 8;
+    }
     if (pps < 1)
         pps = 1;
+    if (pps > max_pages)
+        pps = max_pages > 0 ? max_pages : 1;
     *pages_per_split = pps;
     *n_splits = max_pages > 0 ? (max_pages + pps - 1) / pps : 1;
+}
+
+int attn_max_splits(int batch, int q_heads, int max_pages, int sms)
+{
+    int best = 1;
+    for (int h = 1; h <= q_heads; ++h) {
+        if (q_heads % h || q_heads / h > 32)
+            continue;
+        int n = 1, pps = 1;
+        attn_split_plan(batch, h, max_pages, sms, &n, &pps);
+        if (n > best)
+            best = n;
+    }
+    return best;
 }
 
 size_t attn_workspace_bytes(int batch, int q_heads, int n_splits)
@@ -311,15 +327,24 @@ size_t attn_workspace_bytes(int batch, int q_heads, int n_splits)
     return (size_t)batch * (size_t)q_heads * (size_t)n_splits * kPart * sizeof(float);
 }
 
+cudaError_t launch_attn_combine(const AttnArgs &a, cudaStream_t s)
+{
+    attn_combine_kernel<<<(unsigned)(a.B * a.Hq), kD, 0, s>>>(a.part, a.n_splits, a.out);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_decode_attn(const AttnArgs &a, cudaStream_t s)
 {
     if (a.B == 0 || a.Hq == 0)
         return cudaSuccess;
-    if (a.G <= 8)
-        return a.full ? run<8, true>(a, s) : run<8, false>(a, s);
+    cudaError_t e;
     if (a.G <= 16)
-        return a.full ? run<16, true>(a, s) : run<16, false>(a, s);
-    return a.full ? run<32, true>(a, s) : run<32, false>(a, s);
+        e = launch_attn_mma(a, s);
+    else
+        e = a.full ? run<32, true>(a, s) : run<32, false>(a, s);
+    if (e != cudaSuccess)
+        return e;
+    return launch_attn_combine(a, s);
 }
 
 } // namespace lynx

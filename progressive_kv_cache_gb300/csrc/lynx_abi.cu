@@ -98,9 +98,8 @@ size_t lynx_decode_attn_workspace(int32_t batch, int32_t q_heads, int32_t max_pa
 {
     if (batch <= 0 || q_heads <= 0 || max_pages <= 0)
         return 0;
-    int n_splits = 1, pps = 1;
-    attn_split_plan(batch, max_pages, device_sm_count() > 0 ? device_sm_count() : 1, &n_splits, &pps);
-    return attn_workspace_bytes(batch, q_heads, n_splits);
+    const int sms = device_sm_count() > 0 ? device_sm_count() : 1;
+    return attn_workspace_bytes(batch, q_heads, attn_max_splits(batch, q_heads, max_pages, sms));
 }
 
 lynx_status lynx_decode_attn(const void *q_bf16, const lynx_qkv *k, const lynx_qkv *v, int32_t layer,
@@ -137,7 +136,7 @@ lynx_status lynx_decode_attn(const void *q_bf16, const lynx_qkv *k, const lynx_q
     if (sms <= 0)
         return LYNX_ERR_CUDA;
     int n_splits = 1, pps = 1;
-    attn_split_plan(batch, max_pages, sms, &n_splits, &pps);
+    attn_split_plan(batch, k->kv_heads, max_pages, sms, &n_splits, &pps);
     if (!workspace)
         return LYNX_ERR_NULL;
     if (ws_bytes < attn_workspace_bytes(batch, q_heads, n_splits))

@@ -84,9 +84,15 @@ struct AttnArgs {
     float sm_scale;
     bool full;
 };
-void attn_split_plan(int batch, int max_pages, int sms, int *n_splits, int *pages_per_split);
+// Split-K plan: pages of each (request, KV head) are cut into n_splits ranges
+// of pages_per_split pages. Partials are (o[128], m, l) with m in the base-2
+// log domain (scores pre-multiplied by log2(e)).
+void attn_split_plan(int batch, int kv_heads, int max_pages, int sms, int *n_splits, int *pages_per_split);
+int attn_max_splits(int batch, int q_heads, int max_pages, int sms);   // over every valid kv_heads
 size_t attn_workspace_bytes(int batch, int q_heads, int n_splits);
 cudaError_t launch_decode_attn(const AttnArgs &a, cudaStream_t s);
+cudaError_t launch_attn_mma(const AttnArgs &a, cudaStream_t s);        // tensor-core path, G <= 16
+cudaError_t launch_attn_combine(const AttnArgs &a, cudaStream_t s);
 
 // ---- device helpers ------------------------------------------------------
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }

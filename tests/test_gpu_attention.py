@@ -133,3 +133,18 @@ def test_same_cache_through_views_and_layers(lx, orc):
     a = lx.decode_attn(qb, kq, vq, 2, t, c, 0.1, lx.MODE_FULL)
     b = lx.decode_attn(qb, kq.layers(2, 3), vq.layers(2, 3), 0, t, c, 0.1, lx.MODE_FULL)
     assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("G", [2, 12, 24, 32])
+@pytest.mark.parametrize("mode", [0, 1])
+def test_group_sizes(lx, orc, G, mode):
+    """Groups other than 8 and 16: padded tensor-core rows (2, 12) and the
+    CUDA-core kernel for groups above 16 (24, 32)."""
+    w = S.Workload("t", 310 + G, L=1, H=2, T=5 * 256, n_outliers_fixed=3, factor_log10=(1, 2))
+    cache = _cache(lx, orc, w, 1, 2, 5 * 256)
+    qb = w.queries_bf16(2, 2 * G)
+    table = np.array([[4, 0, 2, 1, 3], [1, 2, 3, 4, 0]], np.int32)
+    ctx = np.array([1100, 77], np.int32)
+    out, ref, _, e, tol = _run(lx, orc, cache, qb, 0, table, ctx, mode)
+    _check(out, ref, tol)
+    assert e == 0
