@@ -47,6 +47,40 @@ B_ATTN_ANCHOR = 64 + 64 + 16 + 16 + 4 + 4            # 168
 B_ATTN_FULL = B_ATTN_ANCHOR + 128                    # 296
 
 
+def max_over_ranks(ms_step, world, device):
+    """Per-step time of the whole job: the slowest rank's (every rank runs its
+    own replica of the workload; no collective touches the data path)."""
+    if world <= 1:
+        return float(ms_step)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(ms_step)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(bytes_per_rank, world, ms_step):
+    """Weak scaling: every rank moves bytes_per_rank per step."""
+    return world * bytes_per_rank / (ms_step * 1e-3) / 1e9
+
+
+def measured_traffic(group, units_per_launch):
+    """DRAM bytes per launch of `group` from the committed ncu capture, or None
+    when there is none or the kernel source changed since it was taken."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f).get(group)
+    if not rec:
+        return None
+    src = os.path.join(ROOT, rec["source"])
+    if not os.path.exists(src) or hashlib.sha256(open(src, "rb").read()).hexdigest() != rec["sha256"]:
+        return None
+    return rec["bytes_per_unit"] * units_per_launch / 1e9
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -299,6 +333,77 @@ def e2e_measure(torch, lx, layers, steps, warmup):
             "note": f"{layers} of the 94 layers per step (host buffers pinned), same path and byte accounting"}
 
 
+def progressive_arrival(torch, lx, w=None, top=32, keep=False):
+    """Progressive arrival: every layer starts as the anchor-only draft; residual
+    planes land layer by layer in a seeded order. On each arrival the layer's
+    dense K and V caches are refined in place and decode attention reruns over
+    all layers, full mode for arrived layers and anchor mode for the rest.
+    Returns a report per arrival: the arrived layer's output change (anchor ->
+    full, max abs and relative L2) and the agreement of its top-`top` keys by
+    score between the anchor and the full pass, plus per-arrival GPU time."""
+    w = S.WORKLOADS[5] if w is None else w
+    L, H, T, B, Hq = w.L, w.H, w.T, w.B, w.Hq
+    dev = torch.device("cuda")
+    gen = S.DeviceGenerator()
+    x = torch.empty((L, H, T, D), dtype=torch.bfloat16, device=dev)
+    qkv, dense = {}, {}
+    for s in (S.S_K, S.S_V):
+        gen.fill(x, w.key(s), w.scales(s))
+        qkv[s] = lx.QuantizedKV.empty(L, H, T, dev)
+        lx.quantize_pages(x, qkv[s])
+        dense[s] = torch.empty((L, H, T, D), dtype=torch.bfloat16, device=dev)
+        lx.dequant_anchor(qkv[s], dense[s])            # the draft cache
+    del x
+    qb = w.queries_bf16()
+    qt = torch.from_numpy(qb.view(np.int16)).to(dev).view(torch.bfloat16)
+    table = torch.arange(T // 256, dtype=torch.int32, device=dev)[None, :].repeat(B, 1).contiguous()
+    ctx = torch.full((B,), T, dtype=torch.int32, device=dev)
+    ws = torch.empty(lx.decode_attn_workspace(B, Hq, T // 256), dtype=torch.uint8, device=dev)
+    sm = D ** -0.5
+
+    def attn(l, mode, scores=None):
+        return lx.decode_attn(qt, qkv[S.S_K], qkv[S.S_V], l, table, ctx, sm, mode, scores=scores, workspace=ws)
+
+    def topk_set(sc):
+        return torch.topk(sc, top, dim=-1).indices
+
+    out_anchor, top_anchor = [], []
+    sc = torch.empty((B, Hq, T), dtype=torch.float32, device=dev)
+    for l in range(L):
+        out_anchor.append(attn(l, lx.MODE_ANCHOR, sc).clone())
+        top_anchor.append(topk_set(sc))
+    order = [int(v) for v in S.arrival_order(w)]
+    arrived, report = set(), []
+    for l in order:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for s in (S.S_K, S.S_V):
+            lx.refine_residual(qkv[s].layers(l, l + 1), dense[s][l:l + 1])
+        arrived.add(l)
+        outs = [attn(m, lx.MODE_FULL if m in arrived else lx.MODE_ANCHOR) for m in range(L)]
+        e1.record()
+        torch.cuda.synchronize()
+        full = outs[l]
+        attn(l, lx.MODE_FULL, sc)
+        tf = topk_set(sc)
+        agree = (tf[..., :, None] == top_anchor[l][..., None, :]).any(-1).float().sum(-1) / top
+        d = (full - out_anchor[l]).double()
+        report.append({
+            "layer": l,
+            "ms_refine_plus_attention": e0.elapsed_time(e1),
+            "delta_max_abs": float(d.abs().max()),
+            "delta_rel_l2": float(d.norm() / out_anchor[l].double().norm()),
+            "top_agreement_mean": float(agree.mean()),
+            "top_agreement_min": float(agree.min()),
+            "pending_layers_unchanged": all(torch.equal(outs[m], out_anchor[m]) for m in range(L)
+                                            if m not in arrived),
+        })
+    result = {"workload": w.name, "order": order, "top": top, "arrivals": report}
+    if keep:
+        result.update(qkv=qkv, dense=dense, qb=qb, outs=outs, out_anchor=out_anchor)
+    return result
+
+
 def run_gpu(args):
     import torch
     import torch.distributed as dist
@@ -347,11 +452,8 @@ def run_gpu(args):
             wl.step(ev, only=only, graphs=use_graphs)
         end.record()
         torch.cuda.synchronize()
-    ms_step = start.elapsed_time(end) / args.steps
+    ms_step = max_over_ranks(start.elapsed_time(end) / args.steps, world, "cuda")
     if world > 1:
-        t = torch.tensor([ms_step], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step = float(t.item())
         dist.barrier()
 
     nbytes = wl.algorithmic_bytes()
@@ -375,14 +477,18 @@ def run_gpu(args):
     for p in per.values():
         p["share"] = p["ms_per_step"] / tot_all
     dom = max(per, key=lambda n: per[n]["ms_per_step"])
-    launches_per_unit = {"quantize": 1, "dequant_anchor": 1, "refine": 1}
-    if dom in launches_per_unit:
-        ach = nbytes[dom] / 2 / (per[dom]["ms_per_timed_unit"] * 1e-3) / 1e9
+    # one launch: one tensor (quantize, decoders) or one layer (attention, split + combine)
+    if dom in ("quantize", "dequant_anchor", "refine"):
+        launch_units, launch_bytes = wl.elements, nbytes[dom] / 2
+        launch_ms = per[dom]["ms_per_timed_unit"]
     else:
-        ach = per[dom]["GB/s"]
+        launch_units, launch_bytes = wl.H * wl.T, nbytes[dom] / wl.L
+        launch_ms = per[dom]["ms_per_step"] / wl.L
+    ach = launch_bytes / (launch_ms * 1e-3) / 1e9
+    traffic = measured_traffic(dom, launch_units)
     total_bytes = sum(nbytes.values())
     wl_layers = wl.L
-    value = world * total_bytes / (ms_step * 1e-3) / 1e9
+    value = whole_job_gbs(total_bytes, world, ms_step)
 
     e2e = None
     if not args.no_e2e and only is None:
@@ -403,7 +509,8 @@ def run_gpu(args):
                        "q_heads": HQ, "batch": 1, "io": "bf16 in, 4+4-bit planes, bf16 dense cache",
                        "parallelism": f"replicas x{world}", "l2": "every input larger than L2, no flush"},
             "roofline": {"bound": "hbm", "kernel": dom, "achieved": ach, "peak": hbm, "unit": "GB/s",
-                         "frac": ach / hbm, "peak_kind": peak_kind, "traffic": None},
+                         "frac": ach / hbm, "peak_kind": peak_kind, "traffic": traffic,
+                         "traffic_unit": "GB per launch", "algorithmic": launch_bytes / 1e9},
             "per_kernel": per,
             "decode_tokens_per_s": {m: per[f"decode_attn_{m}"]["tokens_per_s"] for m in ("anchor", "full")
                                     if f"decode_attn_{m}" in per},
@@ -458,6 +565,8 @@ def main():
                                        "decode_attn_full"], default=None,
                     help="time one kernel group only (for profiler captures on smaller cases)")
     ap.add_argument("--layers", type=int, default=None, help="layers of the cache (default: all 94)")
+    ap.add_argument("--report", choices=["progressive"], default=None,
+                    help="progressive: residual layers arriving one by one (8 layers, 64K tokens)")
     ap.add_argument("--no-graph", action="store_true",
                     help="issue every library call from Python instead of replaying CUDA graphs of them")
     args = ap.parse_args()
@@ -465,6 +574,12 @@ def main():
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
     if args.impl == "reference":
         run_reference(args)
+    elif args.report == "progressive":
+        import torch
+        import __graft_entry__
+        __graft_entry__.build()
+        import progressive_kv_cache_gb300 as lx
+        print(json.dumps(progressive_arrival(torch, lx)))
     else:
         run_gpu(args)
 

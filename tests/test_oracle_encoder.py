@@ -240,3 +240,24 @@ def test_signed_zero_extremes_store_plus_zero(orc):
         assert np.array_equal(qa[k].view(np.uint8), qb[k].view(np.uint8)), k
     assert qa["page_meta"][0, 0, 0, 0, 7].view(np.uint32) == 0       # +0 minimum
     assert qa["page_meta"][0, 0, 0, 1, 9] > 0
+
+
+def test_ragged_chunk_metadata_against_fp64_statistics(orc):
+    """A page with 77 valid tokens: chunk 2 holds 13 of them; its mean and scale
+    are statistics of those 13 values only."""
+    n = 77
+    w = S.Workload("t", 95, L=1, H=1, T=PAGE, n_outliers_fixed=4)
+    xb = S.laplace_bf16(w.key(S.S_K), w.scales(S.S_K), 1, 1, PAGE)
+    q = orc.quantize(xb, np.array([n], np.int32))
+    x = _x_f64(xb)[0, 0, :n]
+    mn, rng = x.min(0), x.max(0) - x.min(0)
+    u = (x - mn) / rng
+    cm = q["chunk_meta"][0, 0, 0].view(np.float16).astype(np.float64)
+    for j in range(3):
+        uj = u[j * CH:min((j + 1) * CH, n)]
+        mean = uj.mean(0)
+        ulp = np.spacing(np.abs(mean).astype(np.float16)).astype(np.float64)
+        assert np.all(np.abs(cm[j, 0] - mean) <= 0.5 * ulp + 1e-6), j
+        smax = np.abs(uj - cm[j, 0]).max(0)
+        assert np.all(cm[j, 1] >= smax - 1e-6) and np.all(cm[j, 1] - smax <= np.spacing(
+            cm[j, 1].astype(np.float16)).astype(np.float64) + 1e-6), j
