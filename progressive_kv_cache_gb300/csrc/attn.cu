@@ -248,26 +248,58 @@ __global__ void __launch_bounds__(kThreads, 1) attn_split_kernel(AttnArgs a, Lev
     }
 }
 
+// Log-sum-exp merge of the page ranges' partials (base-2 log domain): one block
+// per (request, query head), 128 threads. The maxima and the weights of all
+// partials are reduced once in parallel and kept in shared memory, so the
+// weighted sum over partials is a run of independent loads per channel.
 __global__ void __launch_bounds__(kD) attn_combine_kernel(const float *__restrict__ part, int n_splits,
                                                           float *__restrict__ out)
 {
+    extern __shared__ float wgt[];   // [n_splits]
+    __shared__ float red[kD / 32];
     const int64_t bh = blockIdx.x;
-    const int d = threadIdx.x;
+    const int d = threadIdx.x, lane = d & 31, warp = d >> 5;
     const float *pp = part + bh * n_splits * kPart;
-    float M = -__int_as_float(0x7F800000);
-    for (int s = 0; s < n_splits; ++s)
-        M = fmaxf(M, pp[s * kPart + kD]);
-    float L = 0.0f, o = 0.0f;
-    if (M > -__int_as_float(0x7F800000)) {
-        for (int s = 0; s < n_splits; ++s) {
-            const float l = pp[s * kPart + kD + 1];
-            if (l > 0.0f) {
-                const float w = exp2f(pp[s * kPart + kD] - M);
-                L = fmaf(l, w, L);
-                o = fmaf(pp[s * kPart + d], w, o);
-            }
-        }
+    const float ninf = -__int_as_float(0x7F800000);
+
+    float mx = ninf;
+    for (int s = d; s < n_splits; s += kD)
+        if (pp[s * kPart + kD + 1] > 0.0f)
+            mx = fmaxf(mx, pp[s * kPart + kD]);
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1)
+        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+    if (lane == 0)
+        red[warp] = mx;
+    __syncthreads();
+    const float M = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+    __syncthreads();
+
+    float lsum = 0.0f;
+    for (int s = d; s < n_splits; s += kD) {
+        const float l = pp[s * kPart + kD + 1];
+        const float w = (l > 0.0f && M > ninf) ? exp2f(pp[s * kPart + kD] - M) : 0.0f;
+        wgt[s] = w;
+        lsum = fmaf(l, w, lsum);
     }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1)
+        lsum += __shfl_xor_sync(0xFFFFFFFFu, lsum, o);
+    if (lane == 0)
+        red[warp] = lsum;
+    __syncthreads();
+    const float L = (red[0] + red[1]) + (red[2] + red[3]);
+
+    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    int s = 0;
+    for (; s + 4 <= n_splits; s += 4) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            acc[u] = fmaf(pp[(s + u) * kPart + d], wgt[s + u], acc[u]);
+    }
+    for (; s < n_splits; ++s)
+        acc[0] = fmaf(pp[s * kPart + d], wgt[s], acc[0]);
+    const float o = (acc[0] + acc[1]) + (acc[2] + acc[3]);
     out[bh * kD + d] = L > 0.0f ? o / L : 0.0f;
 }
 
@@ -302,6 +334,8 @@ void attn_split_plan(int batch, int kv_heads, int max_pages, int sms, int *n_spl
     }
     if (pps < 1)
         pps = 1;
+    if (max_pages / pps > 8192)   // the combine keeps one weight per range in shared memory
+        pps = (max_pages + 8191) / 8192;
     if (pps > max_pages)
         pps = max_pages > 0 ? max_pages : 1;
     *pages_per_split = pps;
@@ -329,7 +363,8 @@ size_t attn_workspace_bytes(int batch, int q_heads, int n_splits)
 
 cudaError_t launch_attn_combine(const AttnArgs &a, cudaStream_t s)
 {
-    attn_combine_kernel<<<(unsigned)(a.B * a.Hq), kD, 0, s>>>(a.part, a.n_splits, a.out);
+    attn_combine_kernel<<<(unsigned)(a.B * a.Hq), kD, (size_t)a.n_splits * sizeof(float), s>>>(a.part, a.n_splits,
+                                                                                               a.out);
     return cudaGetLastError();
 }
 

@@ -14,16 +14,22 @@
 //   o_d += sum_j [ a_jd sum_{t in j} p_t + b_jd sum_{t in j} p_t L_td ],
 // so the tensor-core operands on the cache side are the level values
 // themselves (no rounding), and the dense operand (q b, or p) is split into an
-// fp16 hi/lo pair to keep fp32-level accuracy. mma.sync m16n8k16 with the
-// rows of A = 8 query heads' hi parts over the same heads' lo parts, so one
-// MMA carries both halves of the split.
+// fp16 hi/lo pair to keep fp32-level accuracy (mma.sync m16n8k16, fp32
+// accumulation).
 //
-// Work: a CTA per (page range, KV head, request) with 8 warps per 8 query
-// heads of the group; warp w owns chunk w % 8 of every page for heads
-// 8 (w / 8) .. +7. Pages arrive by bulk copy into two shared-memory stages.
-// V codes are re-laid out once per page with an 8x8 nibble transpose (token
-// pairs per byte, swizzled) so that each P.V B fragment is one 16-bit load.
-// The warps' running (max, sum, output) are merged in shared memory into one
+// Work: a CTA per (page range, KV head, request). Pages arrive by bulk copy
+// into two shared-memory stages; V codes are re-laid out once per page with an
+// 8x8 nibble transpose (token pairs per byte, swizzled) so that each P.V B
+// fragment is one 16-bit load. Two variants:
+//  - groups of up to 8 query heads: 8 warps, warp j owns chunk j of every
+//    page; the MMA rows are the 8 heads' hi parts over their lo parts, so one
+//    MMA carries both halves of the split;
+//  - groups of up to 16: 16 warps, warps j and j + 8 share chunk j and each
+//    decodes half of the channels (Q.K^T halves are summed through shared
+//    memory, P.V covers its own channels); MMA rows are the 16 heads, hi and lo
+//    in two MMAs; each warp runs the softmax of one head row and the pair swaps
+//    the resulting P fragments.
+// The chunks' running (max, sum, output) are merged in shared memory into one
 // partial per query head; a second kernel merges the partials of the ranges.
 #include <cuda_fp16.h>
 
@@ -56,11 +62,15 @@ struct Smem {
     Stage<FULL> st[2];
     uint8_t vta[kD * (kPage / 2)];            // V anchors: byte k of channel c holds tokens 2k, 2k+1 (swizzled)
                                               // (V residuals, same layout, go to the stage's va slot)
-    float2 kab[kNChunk][kD];                  // K chunk affine (mn + rng mu, rng s * 2^-guard)
-    float2 vab[kNChunk][kD];                  // V chunk affine (mn + rng mu, rng s)
+    // chunk affines of channel pairs: (a_2i, a_2i+1, b_2i, b_2i+1), K's b times 2^-guard
+    float4 kab[kNChunk][kD / 2];
+    float4 vab[kNChunk][kD / 2];
     float qs[16][kD + 8];                     // the group's queries times sm_scale log2(e); unused rows 0
                                               // (rows padded: 8 heads x 4 lanes read distinct banks)
-    float xch[kNChunk][18][32];               // Q.K^T halves exchanged between the two warps of a chunk
+    float xch[kNChunk][19][32];               // Q.K^T halves exchanged between the two warps of a chunk;
+                                              // row 18: per quad, each warp's sum of P and rescale
+                                              // (the P fragments are swapped through the stage's consumed
+                                              // V plane: 8 pairs x 2 warps x 8 words x 32 lanes = 16 KiB)
     // level table, one copy per lane (conflict-free lookups): anchor mode maps a
     // byte of two anchors to the half2 of their levels, full mode a code byte
     // (A << 4 | r) to the fp16 level
@@ -84,12 +94,12 @@ __device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], 
                  : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// x0, x1 -> fp16 pairs hi and lo with hi + lo = (x0, x1) to ~22 bits.
-__device__ __forceinline__ void split2(float x0, float x1, uint32_t &hi, uint32_t &lo)
+// (x0, x1) -> fp16 pairs hi and lo with hi + lo = (x0, x1) to ~22 bits.
+__device__ __forceinline__ void split2(float2 x, uint32_t &hi, uint32_t &lo)
 {
-    const __half2 h = __floats2half2_rn(x0, x1);
+    const __half2 h = __floats2half2_rn(x.x, x.y);
     const float2 hf = __half22float2(h);
-    const __half2 l = __floats2half2_rn(x0 - hf.x, x1 - hf.y);
+    const __half2 l = __floats2half2_rn(x.x - hf.x, x.y - hf.y);
     hi = *reinterpret_cast<const uint32_t *>(&h);
     lo = *reinterpret_cast<const uint32_t *>(&l);
 }
@@ -149,23 +159,24 @@ __device__ __forceinline__ void transpose_v(const uint8_t *src, uint8_t *dst, in
 
 __device__ __forceinline__ float neg_inf() { return -__int_as_float(0x7F800000); }
 
-// NW = 8 warps for groups of up to 8 query heads: warp j owns chunk j, and its
-// MMA rows 0-7 are the 8 heads' hi parts, rows 8-15 their lo parts.
-// NW = 16 warps for groups of up to 16: warps j and j + 8 share chunk j, each
-// decoding half the channels; rows are the 16 heads, hi and lo in two MMAs, and
-// the two halves of Q.K^T are summed through shared memory.
+__device__ __forceinline__ void pair_sync(int j)
+{
+    asm volatile("bar.sync %0, 64;" ::"r"(1 + j) : "memory");
+}
+
 template <int NW, bool FULL>
 __global__ void __launch_bounds__(NW * 32, 1) attn_mma_kernel(AttnArgs a, LevelTable lev)
 {
     constexpr int NT = NW * 32;
+    constexpr bool PAIR = NW == 16;         // two warps per chunk, split by channels
+    constexpr int NH = PAIR ? 2 : 1;        // query heads (MMA row pairs) per lane
+    constexpr int NTO = PAIR ? 8 : 16;      // output n-tiles per warp
     extern __shared__ __align__(128) unsigned char smem_raw[];
     Smem<FULL> &sm = *reinterpret_cast<Smem<FULL> *>(smem_raw);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int n = lane >> 2, q = lane & 3;
-    constexpr bool PAIR = NW == 16;         // two warps per chunk, split by channels
     const int j = warp & 7;                 // chunk of this warp
-    const int hc = warp >> 3;               // PAIR: channels 64hc .. 64hc + 63
-    const int head = n;                     // this lane's head (and n + 8 in PAIR mode)
+    const int hc = warp >> 3;               // PAIR: channels 64hc .. 64hc + 63, softmax of head row n + 8hc
     const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
     const int G = a.G;
     const int64_t T = (int64_t)a.pool_pages * kPage;
@@ -194,6 +205,7 @@ __global__ void __launch_bounds__(NW * 32, 1) attn_mma_kernel(AttnArgs a, LevelT
     }
     if (tid == 0) {
         sm.qmax = 0.0f;
+        sm.guard = 0;
         mbar_init(&sm.bar[0], 1);
         mbar_init(&sm.bar[1], 1);
         fence_mbar_init();
@@ -260,22 +272,15 @@ __global__ void __launch_bounds__(NW * 32, 1) attn_mma_kernel(AttnArgs a, LevelT
                 a.scores[(qrow0 + i / kPage) * score_stride + (int64_t)lp * kPage + i % kPage] = neg_inf();
     }
 
-    // running softmax state of this warp's chunk: NH heads per lane (n, n + 8),
-    // output channels: STACK all 128 (16 n-tiles), PAIR its 64 (8 n-tiles)
-    constexpr int NH = PAIR ? 2 : 1;
-    constexpr int NTO = PAIR ? 8 : 16;
-    float m_run[NH], l_run[NH];
-    float O[NTO][NH][2];
-#pragma unroll
-    for (int i2 = 0; i2 < NH; ++i2) {
-        m_run[i2] = neg_inf();
-        l_run[i2] = 0.0f;
-    }
+    // Running softmax state. STACK: head n. PAIR: head row n + 8hc (this warp's
+    // softmax); the output of both head rows n and n + 8 for its channels.
+    float m_run = neg_inf(), l_run = 0.0f;
+    float2 O[NTO][NH];
 #pragma unroll
     for (int nt = 0; nt < NTO; ++nt)
 #pragma unroll
         for (int i2 = 0; i2 < NH; ++i2)
-            O[nt][i2][0] = O[nt][i2][1] = 0.0f;
+            O[nt][i2] = make_float2(0.0f, 0.0f);
     const uint32_t *lut_lane = sm.lut + (FULL ? 0 : lane);
     const uint16_t *lut16_lane = reinterpret_cast<const uint16_t *>(sm.lut) + lane;
 
@@ -312,40 +317,46 @@ __global__ void __launch_bounds__(NW * 32, 1) attn_mma_kernel(AttnArgs a, LevelT
         phase[s] ^= 1u;
         const Stage<FULL> &st = sm.st[s];
 
-        // ---- per-page preparation: chunk affines, fp16 guard, V transpose ----
+        // ---- per-page preparation: chunk affines, V transpose, fp16 guard ----
         {
             float rmax = 0.0f;
-            for (int e = tid; e < kNChunk * kD; e += NT) {
-                const int jj = e >> 7, d = e & (kD - 1);
-                const float kmn = st.kpm[d], krg = st.kpm[kD + d];
-                const float vmn = st.vpm[d], vrg = st.vpm[kD + d];
-                const float kmu = __half2float(__ushort_as_half(st.kcm[(jj * 2) * kD + d]));
-                const float ksc = __half2float(__ushort_as_half(st.kcm[(jj * 2 + 1) * kD + d]));
-                const float vmu = __half2float(__ushort_as_half(st.vcm[(jj * 2) * kD + d]));
-                const float vsc = __half2float(__ushort_as_half(st.vcm[(jj * 2 + 1) * kD + d]));
-                sm.kab[jj][d] = make_float2(fmaf(krg, kmu, kmn), krg * ksc);
-                sm.vab[jj][d] = make_float2(fmaf(vrg, vmu, vmn), vrg * vsc);
-                rmax = fmaxf(rmax, fabsf(krg * ksc));
+            for (int e = tid; e < kNChunk * (kD / 2); e += NT) {
+                const int jj = e >> 6, d = 2 * (e & 63);
+                const float2 kmn = *reinterpret_cast<const float2 *>(st.kpm + d);
+                const float2 krg = *reinterpret_cast<const float2 *>(st.kpm + kD + d);
+                const float2 vmn = *reinterpret_cast<const float2 *>(st.vpm + d);
+                const float2 vrg = *reinterpret_cast<const float2 *>(st.vpm + kD + d);
+                const float2 kmu = __half22float2(*reinterpret_cast<const __half2 *>(st.kcm + (jj * 2) * kD + d));
+                const float2 ksc = __half22float2(*reinterpret_cast<const __half2 *>(st.kcm + (jj * 2 + 1) * kD + d));
+                const float2 vmu = __half22float2(*reinterpret_cast<const __half2 *>(st.vcm + (jj * 2) * kD + d));
+                const float2 vsc = __half22float2(*reinterpret_cast<const __half2 *>(st.vcm + (jj * 2 + 1) * kD + d));
+                const float2 kb = __fmul2_rn(krg, ksc), vb = __fmul2_rn(vrg, vsc);
+                const float2 ka2 = __ffma2_rn(krg, kmu, kmn), va2 = __ffma2_rn(vrg, vmu, vmn);
+                sm.kab[jj][e & 63] = make_float4(ka2.x, ka2.y, kb.x, kb.y);
+                sm.vab[jj][e & 63] = make_float4(va2.x, va2.y, vb.x, vb.y);
+                rmax = fmaxf(rmax, fmaxf(fabsf(kb.x), fabsf(kb.y)));
             }
-            if (tid == 0)
-                sm.guard = 0;
             transpose_v<NT>(st.va, sm.vta, tid);
-            __syncthreads();
+            // q b must stay a finite fp16 pair: if qmax * max|b| reaches 2^14 on
+            // this page, scale K's b by 2^-e (and the scores back by 2^e)
+            const bool need_guard = __syncthreads_or(rmax * sm.qmax >= 16384.0f);
             if (FULL) {   // the residual plane goes where the anchor plane was
                 transpose_v<NT>(st.vr, sm.st[s].va, tid);
                 __syncthreads();
             }
-            // exponent e with qmax * max|b| * 2^-e < 2^14: q b stays a finite fp16 pair
-            if (rmax * sm.qmax >= 16384.0f) {
-                int e2;
-                frexpf(rmax * sm.qmax, &e2);
-                atomicMax(&sm.guard, e2 - 14);
-            }
-            __syncthreads();
-            if (sm.guard > 0) {
+            if (need_guard) {
+                if (rmax * sm.qmax >= 16384.0f) {
+                    int e2;
+                    frexpf(rmax * sm.qmax, &e2);
+                    atomicMax(&sm.guard, e2 - 14);
+                }
+                __syncthreads();
                 const float sc = exp2f((float)-sm.guard);
-                for (int e = tid; e < kNChunk * kD; e += NT)
-                    sm.kab[e >> 7][e & (kD - 1)].y *= sc;
+                for (int e = tid; e < kNChunk * (kD / 2); e += NT) {
+                    float4 &kk = sm.kab[e >> 6][e & 63];
+                    kk.z *= sc;
+                    kk.w *= sc;
+                }
                 __syncthreads();
             }
         }
@@ -381,7 +392,7 @@ __global__ void __launch_bounds__(NW * 32, 1) attn_mma_kernel(AttnArgs a, LevelT
             };
             // B fragments of V for channel column c and k-step ks (tokens 16ks ..)
             auto v_frag = [&](int c, int ks, uint32_t &b0, uint32_t &b1) {
-                const int pos = c * (kPage / 2) + (((2 * j + ks + c + (c >> 3)) & 15) << 3) + 2 * q;
+                const int pos = vt_group(c, 2 * j + ks) + 2 * q;
                 const uint32_t a16 = *reinterpret_cast<const uint16_t *>(sm.vta + pos);
                 if (FULL) {
                     const uint32_t r16 = *reinterpret_cast<const uint16_t *>(st.va + pos);
@@ -401,40 +412,36 @@ __global__ void __launch_bounds__(NW * 32, 1) attn_mma_kernel(AttnArgs a, LevelT
 #pragma unroll
             for (int nt = 0; nt < 4; ++nt)
                 S[nt][0] = S[nt][1] = S[nt][2] = S[nt][3] = 0.0f;
-            float beta[NH];
+            float2 beta2[NH];
 #pragma unroll
             for (int i2 = 0; i2 < NH; ++i2)
-                beta[i2] = 0.0f;
+                beta2[i2] = make_float2(0.0f, 0.0f);
 #pragma unroll
             for (int m = 0; m < (PAIR ? 2 : 4); ++m) {
                 uint32_t Ahi[2][4], Alo[2][4];
 #pragma unroll
                 for (int kx = 0; kx < 2; ++kx) {
                     const int c0 = (PAIR ? 64 * hc : 0) + 32 * m + 16 * kx + 2 * q;
-                    const float4 k01 = *reinterpret_cast<const float4 *>(&sm.kab[j][c0]);
-                    const float4 k89 = *reinterpret_cast<const float4 *>(&sm.kab[j][c0 + 8]);
-                    float x[NH][4];
+                    const float4 k01 = sm.kab[j][c0 >> 1];          // channels c0, c0 + 1
+                    const float4 k89 = sm.kab[j][(c0 >> 1) + 4];    // channels c0 + 8, c0 + 9
+                    float2 x[NH][2];
 #pragma unroll
                     for (int i2 = 0; i2 < NH; ++i2) {
-                        const float2 q01 = *reinterpret_cast<const float2 *>(&sm.qs[head + 8 * i2][c0]);
-                        const float2 q89 = *reinterpret_cast<const float2 *>(&sm.qs[head + 8 * i2][c0 + 8]);
-                        beta[i2] = fmaf(q01.x, k01.x, beta[i2]);
-                        beta[i2] = fmaf(q01.y, k01.z, beta[i2]);
-                        beta[i2] = fmaf(q89.x, k89.x, beta[i2]);
-                        beta[i2] = fmaf(q89.y, k89.z, beta[i2]);
-                        x[i2][0] = q01.x * k01.y;
-                        x[i2][1] = q01.y * k01.w;
-                        x[i2][2] = q89.x * k89.y;
-                        x[i2][3] = q89.y * k89.w;
+                        const float2 q01 = *reinterpret_cast<const float2 *>(&sm.qs[n + 8 * i2][c0]);
+                        const float2 q89 = *reinterpret_cast<const float2 *>(&sm.qs[n + 8 * i2][c0 + 8]);
+                        beta2[i2] = __ffma2_rn(q01, make_float2(k01.x, k01.y), beta2[i2]);
+                        beta2[i2] = __ffma2_rn(q89, make_float2(k89.x, k89.y), beta2[i2]);
+                        x[i2][0] = __fmul2_rn(q01, make_float2(k01.z, k01.w));
+                        x[i2][1] = __fmul2_rn(q89, make_float2(k89.z, k89.w));
                     }
                     if (PAIR) {
-                        split2(x[0][0], x[0][1], Ahi[kx][0], Alo[kx][0]);
-                        split2(x[NH - 1][0], x[NH - 1][1], Ahi[kx][1], Alo[kx][1]);
-                        split2(x[0][2], x[0][3], Ahi[kx][2], Alo[kx][2]);
-                        split2(x[NH - 1][2], x[NH - 1][3], Ahi[kx][3], Alo[kx][3]);
+                        split2(x[0][0], Ahi[kx][0], Alo[kx][0]);
+                        split2(x[NH - 1][0], Ahi[kx][1], Alo[kx][1]);
+                        split2(x[0][1], Ahi[kx][2], Alo[kx][2]);
+                        split2(x[NH - 1][1], Ahi[kx][3], Alo[kx][3]);
                     } else {
-                        split2(x[0][0], x[0][1], Ahi[kx][0], Ahi[kx][1]);
-                        split2(x[0][2], x[0][3], Ahi[kx][2], Ahi[kx][3]);
+                        split2(x[0][0], Ahi[kx][0], Ahi[kx][1]);
+                        split2(x[0][1], Ahi[kx][2], Ahi[kx][3]);
                     }
                 }
 #pragma unroll
@@ -449,8 +456,10 @@ __global__ void __launch_bounds__(NW * 32, 1) attn_mma_kernel(AttnArgs a, LevelT
                     }
                 }
             }
+            float beta[NH];
 #pragma unroll
             for (int i2 = 0; i2 < NH; ++i2) {
+                beta[i2] = beta2[i2].x + beta2[i2].y;
                 beta[i2] += __shfl_xor_sync(0xFFFFFFFFu, beta[i2], 1);
                 beta[i2] += __shfl_xor_sync(0xFFFFFFFFu, beta[i2], 2);
             }
@@ -468,7 +477,7 @@ __global__ void __launch_bounds__(NW * 32, 1) attn_mma_kernel(AttnArgs a, LevelT
                     xc[16 * 32] = beta[0];
                     xc[17 * 32] = beta[NH - 1];
                 }
-                asm volatile("bar.sync %0, 64;" ::"r"(1 + j) : "memory");
+                pair_sync(j);
                 if (hc == 0) {
 #pragma unroll
                     for (int nt = 0; nt < 4; ++nt)
@@ -482,7 +491,7 @@ __global__ void __launch_bounds__(NW * 32, 1) attn_mma_kernel(AttnArgs a, LevelT
                     xc[16 * 32] = beta[0];
                     xc[17 * 32] = beta[NH - 1];
                 }
-                asm volatile("bar.sync %0, 64;" ::"r"(1 + j) : "memory");
+                pair_sync(j);
                 if (hc == 1) {
 #pragma unroll
                     for (int nt = 0; nt < 4; ++nt)
@@ -494,53 +503,95 @@ __global__ void __launch_bounds__(NW * 32, 1) attn_mma_kernel(AttnArgs a, LevelT
                 }
             }
 
-            // scores (base-2 log domain), masking, online softmax per head
-            float P[4][NH][2];
-            float psum[NH];
+            // scores of this warp's softmax head (base-2 log domain), masking, online softmax
+            const int sh = PAIR ? hc : 0;          // head row: n + 8 sh
+            const float bsh = PAIR ? (hc ? beta[NH - 1] : beta[0]) : beta[0];
+            float P[4][2];
+            float mx = neg_inf();
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int tt = nt * 8 + 2 * q + e;
+                    const float raw = PAIR ? S[nt][2 * sh + e] : S[nt][e] + S[nt][e + 2];
+                    const float v = tt < nv ? fmaf(raw, gscale, bsh) : neg_inf();
+                    P[nt][e] = v;
+                    mx = fmaxf(mx, v);
+                }
+            if (a.scores && n + 8 * sh < G) {
+                float *srow = a.scores + (qrow0 + n + 8 * sh) * score_stride + (int64_t)lp * kPage + j * kChunk;
+#pragma unroll
+                for (int nt = 0; nt < 4; ++nt)
+                    *reinterpret_cast<float2 *>(srow + nt * 8 + 2 * q) = make_float2(P[nt][0] * kLn2, P[nt][1] * kLn2);
+            }
+            mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
+            mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));
+            const float m_new = fmaxf(m_run, mx);
+            const float alpha = exp2f(m_run - m_new);
+            m_run = m_new;
+            float ps = 0.0f;
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const float pv = exp2f(P[nt][e] - m_new);
+                    P[nt][e] = pv;
+                    ps += pv;
+                }
+            l_run = fmaf(l_run, alpha, ps);
+            ps += __shfl_xor_sync(0xFFFFFFFFu, ps, 1);
+            ps += __shfl_xor_sync(0xFFFFFFFFu, ps, 2);
+
+            // this head row's P as hi/lo fp16 pairs for n-tiles 0..3 (tokens 8nt + 2q + e)
+            uint32_t ph[4], pl[4];
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt)
+                split2(make_float2(P[nt][0], P[nt][1]), ph[nt], pl[nt]);
+
+            // PAIR: swap P fragments, sums and rescales with the partner warp
+            uint32_t oph[4], opl[4];
+            float ops = ps, oalpha = alpha;
+            if (PAIR) {
+                // the V plane this page's transpose consumed (the anchor plane in
+                // anchor mode, the residual plane in full mode) is free until the
+                // end of the page
+                uint32_t *xpb = reinterpret_cast<uint32_t *>(const_cast<uint8_t *>(FULL ? st.vr : st.va));
+                uint32_t *mine = xpb + ((j * 2 + hc) * 8) * 32 + lane;
+                const uint32_t *theirs = xpb + ((j * 2 + (hc ^ 1)) * 8) * 32 + lane;
+#pragma unroll
+                for (int nt = 0; nt < 4; ++nt) {
+                    mine[nt * 32] = ph[nt];
+                    mine[(4 + nt) * 32] = pl[nt];
+                }
+                float *qrow = &sm.xch[j][18][0];
+                if (q == 0) {
+                    qrow[n * 4 + hc * 2] = ps;
+                    qrow[n * 4 + hc * 2 + 1] = alpha;
+                }
+                pair_sync(j);
+#pragma unroll
+                for (int nt = 0; nt < 4; ++nt) {
+                    oph[nt] = theirs[nt * 32];
+                    opl[nt] = theirs[(4 + nt) * 32];
+                }
+                ops = qrow[n * 4 + (hc ^ 1) * 2];
+                oalpha = qrow[n * 4 + (hc ^ 1) * 2 + 1];
+            }
+            // per output head row i2 (row n + 8 i2): its sum of P and rescale
+            float psum[NH], alph[NH];
+            psum[0] = (PAIR && hc == 1) ? ops : ps;
+            alph[0] = (PAIR && hc == 1) ? oalpha : alpha;
+            if (PAIR) {
+                psum[NH - 1] = hc == 1 ? ps : ops;
+                alph[NH - 1] = hc == 1 ? alpha : oalpha;
+            }
 #pragma unroll
             for (int i2 = 0; i2 < NH; ++i2) {
-                float mx = neg_inf();
+                if (alph[i2] != 1.0f) {
+                    const float2 al = make_float2(alph[i2], alph[i2]);
 #pragma unroll
-                for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int tt = nt * 8 + 2 * q + e;
-                        const float raw = PAIR ? S[nt][2 * i2 + e] : S[nt][e] + S[nt][e + 2];
-                        const float v = tt < nv ? fmaf(raw, gscale, beta[i2]) : neg_inf();
-                        P[nt][i2][e] = v;
-                        mx = fmaxf(mx, v);
-                    }
-                if (a.scores && head + 8 * i2 < G && hc == 0) {
-                    float *srow = a.scores + (qrow0 + head + 8 * i2) * score_stride + (int64_t)lp * kPage + j * kChunk;
-#pragma unroll
-                    for (int nt = 0; nt < 4; ++nt)
-                        *reinterpret_cast<float2 *>(srow + nt * 8 + 2 * q) =
-                            make_float2(P[nt][i2][0] * kLn2, P[nt][i2][1] * kLn2);
-                }
-                mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
-                mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));
-                const float m_new = fmaxf(m_run[i2], mx);
-                const float alpha = exp2f(m_run[i2] - m_new);
-                m_run[i2] = m_new;
-                float ps = 0.0f;
-#pragma unroll
-                for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const float pv = exp2f(P[nt][i2][e] - m_new);
-                        P[nt][i2][e] = pv;
-                        ps += pv;
-                    }
-                l_run[i2] = fmaf(l_run[i2], alpha, ps);
-                ps += __shfl_xor_sync(0xFFFFFFFFu, ps, 1);
-                ps += __shfl_xor_sync(0xFFFFFFFFu, ps, 2);
-                psum[i2] = ps;
-                if (alpha != 1.0f) {
-#pragma unroll
-                    for (int nt = 0; nt < NTO; ++nt) {
-                        O[nt][i2][0] *= alpha;
-                        O[nt][i2][1] *= alpha;
-                    }
+                    for (int nt = 0; nt < NTO; ++nt)
+                        O[nt][i2] = __fmul2_rn(O[nt][i2], al);
                 }
             }
 
@@ -549,13 +600,20 @@ __global__ void __launch_bounds__(NW * 32, 1) attn_mma_kernel(AttnArgs a, LevelT
 #pragma unroll
             for (int ks = 0; ks < 2; ++ks) {
                 if (PAIR) {
-                    split2(P[2 * ks][0][0], P[2 * ks][0][1], Phi[ks][0], Plo[ks][0]);
-                    split2(P[2 * ks][NH - 1][0], P[2 * ks][NH - 1][1], Phi[ks][1], Plo[ks][1]);
-                    split2(P[2 * ks + 1][0][0], P[2 * ks + 1][0][1], Phi[ks][2], Plo[ks][2]);
-                    split2(P[2 * ks + 1][NH - 1][0], P[2 * ks + 1][NH - 1][1], Phi[ks][3], Plo[ks][3]);
+                    const bool lower = hc == 0;   // this warp's softmax row is n (else n + 8)
+                    Phi[ks][0] = lower ? ph[2 * ks] : oph[2 * ks];
+                    Phi[ks][1] = lower ? oph[2 * ks] : ph[2 * ks];
+                    Phi[ks][2] = lower ? ph[2 * ks + 1] : oph[2 * ks + 1];
+                    Phi[ks][3] = lower ? oph[2 * ks + 1] : ph[2 * ks + 1];
+                    Plo[ks][0] = lower ? pl[2 * ks] : opl[2 * ks];
+                    Plo[ks][1] = lower ? opl[2 * ks] : pl[2 * ks];
+                    Plo[ks][2] = lower ? pl[2 * ks + 1] : opl[2 * ks + 1];
+                    Plo[ks][3] = lower ? opl[2 * ks + 1] : pl[2 * ks + 1];
                 } else {
-                    split2(P[2 * ks][0][0], P[2 * ks][0][1], Phi[ks][0], Phi[ks][1]);
-                    split2(P[2 * ks + 1][0][0], P[2 * ks + 1][0][1], Phi[ks][2], Phi[ks][3]);
+                    Phi[ks][0] = ph[2 * ks];
+                    Phi[ks][1] = pl[2 * ks];
+                    Phi[ks][2] = ph[2 * ks + 1];
+                    Phi[ks][3] = pl[2 * ks + 1];
                 }
             }
 
@@ -572,13 +630,13 @@ __global__ void __launch_bounds__(NW * 32, 1) attn_mma_kernel(AttnArgs a, LevelT
                     if (PAIR)
                         mma16816(acc, Plo[ks], b0, b1);
                 }
-                const float4 vv = *reinterpret_cast<const float4 *>(&sm.vab[j][cb + 2 * q]);
+                const float4 vv = sm.vab[j][(cb >> 1) + q];    // channels cb + 2q, cb + 2q + 1
+                const float2 va2 = make_float2(vv.x, vv.y), vb2 = make_float2(vv.z, vv.w);
 #pragma unroll
                 for (int i2 = 0; i2 < NH; ++i2) {
-                    const float d0 = PAIR ? acc[2 * i2] : acc[0] + acc[2];
-                    const float d1 = PAIR ? acc[2 * i2 + 1] : acc[1] + acc[3];
-                    O[nt][i2][0] = fmaf(vv.y, d0, fmaf(psum[i2], vv.x, O[nt][i2][0]));
-                    O[nt][i2][1] = fmaf(vv.w, d1, fmaf(psum[i2], vv.z, O[nt][i2][1]));
+                    const float2 dd = PAIR ? make_float2(acc[2 * i2], acc[2 * i2 + 1])
+                                           : make_float2(acc[0] + acc[2], acc[1] + acc[3]);
+                    O[nt][i2] = __ffma2_rn(vb2, dd, __ffma2_rn(make_float2(psum[i2], psum[i2]), va2, O[nt][i2]));
                 }
             }
         } else if (a.scores && hc == 0) {
@@ -596,21 +654,21 @@ __global__ void __launch_bounds__(NW * 32, 1) attn_mma_kernel(AttnArgs a, LevelT
     // ---- merge the chunks' states, write this range's partial ------------
     __syncthreads();
     Merge &mg = *reinterpret_cast<Merge *>(smem_raw);
-#pragma unroll
-    for (int i2 = 0; i2 < NH; ++i2) {
-        float l = l_run[i2];
+    {
+        float l = l_run;
         l += __shfl_xor_sync(0xFFFFFFFFu, l, 1);
         l += __shfl_xor_sync(0xFFFFFFFFu, l, 2);
-        const int h = head + 8 * i2;
-        if (q == 0 && hc == 0) {
-            mg.m[j][h] = m_run[i2];
+        if (q == 0) {
+            const int h = n + (PAIR ? 8 * hc : 0);
+            mg.m[j][h] = m_run;
             mg.l[j][h] = l;
         }
+    }
+#pragma unroll
+    for (int i2 = 0; i2 < NH; ++i2)
 #pragma unroll
         for (int nt = 0; nt < NTO; ++nt)
-            *reinterpret_cast<float2 *>(&mg.o[j][h][(PAIR ? 64 * hc : 0) + nt * 8 + 2 * q]) =
-                make_float2(O[nt][i2][0], O[nt][i2][1]);
-    }
+            *reinterpret_cast<float2 *>(&mg.o[j][n + 8 * i2][(PAIR ? 64 * hc : 0) + nt * 8 + 2 * q]) = O[nt][i2];
     __syncthreads();
     for (int e = tid; e < G * kD; e += NT) {
         const int h = e / kD, d = e % kD;
@@ -640,6 +698,7 @@ template <int NW, bool FULL>
 cudaError_t run(const AttnArgs &a, cudaStream_t s)
 {
     static_assert(sizeof(Merge) <= sizeof(Stage<FULL>) * 2, "merge area overlays the stages");
+    static_assert(sizeof(Smem<FULL>) <= 227 * 1024, "shared memory per CTA");
     const size_t smem = sizeof(Smem<FULL>);
     cudaError_t e = cudaFuncSetAttribute(attn_mma_kernel<NW, FULL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);

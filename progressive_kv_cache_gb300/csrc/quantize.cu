@@ -86,53 +86,59 @@ __device__ __forceinline__ uint32_t bf2_max(uint32_t a, uint32_t b)
     return *reinterpret_cast<uint32_t *>(&r);
 }
 
-// Stages 2-4 for this thread's two channels of one chunk; `full` chunks have
-// 32 valid tokens, others nc. Writes the staged plane bytes and returns the
-// chunk metadata (mean, scale) of both channels as fp16x2 words.
+// Stages 2-4 for this thread's two channels of one chunk, held as float2
+// lanes (x = channel 2pi, y = channel 2pi + 1) so that each packed fp32
+// instruction performs the contract's operation for both channels (every lane
+// of __fadd2_rn / __fmul2_rn is one IEEE round-to-nearest operation, and
+// x - y is computed as x + (-y), which is the same operation). `full` chunks
+// have 32 valid tokens, others nc. Writes the staged plane bytes and returns
+// the chunk metadata (mean, scale) of both channels as fp16x2 words.
 template <bool FULL>
-__device__ __forceinline__ void encode_chunk(float (&u0)[kChunk], float (&u1)[kChunk], int nc, uint32_t tab_base,
-                                             uint8_t *anc_row0, uint8_t *res_row0, uint32_t &mu2, uint32_t &s2)
+__device__ __forceinline__ void encode_chunk(float2 (&u)[kChunk], int nc, uint32_t tab_base, uint8_t *anc_row0,
+                                             uint8_t *res_row0, uint32_t &mu2, uint32_t &s2)
 {
     // chunk mean: stride-halving pairwise tree over 32 slots, absent slots +0
-    float t0[16], t1[16];
+    const float2 zero = make_float2(0.0f, 0.0f);
+    float2 t[16];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        t0[i] = __fadd_rn((FULL || i < nc) ? u0[i] : 0.0f, (FULL || i + 16 < nc) ? u0[i + 16] : 0.0f);
-        t1[i] = __fadd_rn((FULL || i < nc) ? u1[i] : 0.0f, (FULL || i + 16 < nc) ? u1[i + 16] : 0.0f);
-    }
+    for (int i = 0; i < 16; ++i)
+        t[i] = __fadd2_rn((FULL || i < nc) ? u[i] : zero, (FULL || i + 16 < nc) ? u[i + 16] : zero);
 #pragma unroll
     for (int h = 8; h >= 1; h >>= 1)
 #pragma unroll
-        for (int i = 0; i < h; ++i) {
-            t0[i] = __fadd_rn(t0[i], t0[i + h]);
-            t1[i] = __fadd_rn(t1[i], t1[i + h]);
-        }
-    const float ncf = (float)nc;
-    const __half mh0 = __float2half_rn(FULL ? __fdiv_rn(t0[0], 32.0f) : __fdiv_rn(t0[0], ncf));
-    const __half mh1 = __float2half_rn(FULL ? __fdiv_rn(t1[0], 32.0f) : __fdiv_rn(t1[0], ncf));
-    const float mu0 = __half2float(mh0), mu1 = __half2float(mh1);
+        for (int i = 0; i < h; ++i)
+            t[i] = __fadd2_rn(t[i], t[i + h]);
+    float2 mean;
+    if (FULL) {
+        mean = __fmul2_rn(t[0], make_float2(0.03125f, 0.03125f));   // exact: division by 32
+    } else {
+        const float ncf = (float)nc;
+        mean = make_float2(__fdiv_rn(t[0].x, ncf), __fdiv_rn(t[0].y, ncf));
+    }
+    const __half mh0 = __float2half_rn(mean.x);
+    const __half mh1 = __float2half_rn(mean.y);
+    const float2 negmu = make_float2(-__half2float(mh0), -__half2float(mh1));
 
     float s0 = 0.0f, s1 = 0.0f;
 #pragma unroll
     for (int i = 0; i < kChunk; ++i) {
-        u0[i] = __fsub_rn(u0[i], mu0);   // u becomes v = u - mu
-        u1[i] = __fsub_rn(u1[i], mu1);
+        u[i] = __fadd2_rn(u[i], negmu);   // u becomes v = u - mu
         if (FULL || i < nc) {
-            s0 = fmaxf(s0, fabsf(u0[i]));
-            s1 = fmaxf(s1, fabsf(u1[i]));
+            s0 = fmaxf(s0, fabsf(u[i].x));
+            s1 = fmaxf(s1, fabsf(u[i].y));
         }
     }
     const __half sh0 = __float2half_ru(s0), sh1 = __float2half_ru(s1);
     const float sf0 = __half2float(sh0), sf1 = __half2float(sh1);
-    const float is0 = sf0 > 0.0f ? __frcp_rn(sf0) : 0.0f;
-    const float is1 = sf1 > 0.0f ? __frcp_rn(sf1) : 0.0f;
+    const float2 inv_s = make_float2(sf0 > 0.0f ? __frcp_rn(sf0) : 0.0f, sf1 > 0.0f ? __frcp_rn(sf1) : 0.0f);
 
 #pragma unroll
     for (int i = 0; i < kChunk; ++i) {
         uint32_t ab = 0x00u, rb = 0x77u;                 // code 0: anchor 0, residual 7
         if (FULL || i < nc) {
-            const uint32_t b0 = code_byte(__fmul_rn(u0[i], is0), tab_base);
-            const uint32_t b1 = code_byte(__fmul_rn(u1[i], is1), tab_base);
+            const float2 w = __fmul2_rn(u[i], inv_s);
+            const uint32_t b0 = code_byte(w.x, tab_base);
+            const uint32_t b1 = code_byte(w.y, tab_base);
             ab = ((b0 >> 4) & 0x0Fu) | (b1 & 0xF0u);
             rb = (b0 & 0x0Fu) | ((b1 << 4) & 0xF0u);
         }
@@ -230,11 +236,12 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_kernel(Params p, CodeTab
         const float ir0 = rg0 > 0.0f ? __frcp_rn(rg0) : 0.0f;
         const float ir1 = rg1 > 0.0f ? __frcp_rn(rg1) : 0.0f;
 
-        float u0[kChunk], u1[kChunk];
+        float2 u[kChunk];
+        {
+            const float2 negmn = make_float2(-mn0, -mn1), ir = make_float2(ir0, ir1);
 #pragma unroll
-        for (int i = 0; i < kChunk; ++i) {
-            u0[i] = __fmul_rn(__fsub_rn(bf16_lo(xw[i]), mn0), ir0);
-            u1[i] = __fmul_rn(__fsub_rn(bf16_hi(xw[i]), mn1), ir1);
+            for (int i = 0; i < kChunk; ++i)
+                u[i] = __fmul2_rn(__fadd2_rn(make_float2(bf16_lo(xw[i]), bf16_hi(xw[i])), negmn), ir);
         }
 
         // (c) stages 2-4
@@ -242,9 +249,9 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_kernel(Params p, CodeTab
         uint8_t *res_row0 = sm.res + j * kChunk * (kD / 2) + pi;
         uint32_t mu2 = 0, s2 = 0;
         if (nc == kChunk) {
-            encode_chunk<true>(u0, u1, nc, tab_base, anc_row0, res_row0, mu2, s2);
+            encode_chunk<true>(u, nc, tab_base, anc_row0, res_row0, mu2, s2);
         } else if (nc > 0) {
-            encode_chunk<false>(u0, u1, nc, tab_base, anc_row0, res_row0, mu2, s2);
+            encode_chunk<false>(u, nc, tab_base, anc_row0, res_row0, mu2, s2);
         } else {
 #pragma unroll
             for (int i = 0; i < kChunk; ++i) {
