@@ -27,10 +27,17 @@
  *   q = #{k in 1..63 : |w| >= T_k}, T_k = fp32(((1+alpha)^((k-1/2)/63) - 1)/alpha)
  *   c = q for w >= 0, c = -max(q,1) for w < 0
  *   b = c + 7, A = floor(b/16), r = b - 16A; stored nibbles A & 15 and r.
+ * Statistics fp32 cannot carry (the pages are silent; reading taken here): a
+ *   NaN among a channel's valid values makes its stored min and range the
+ *   quiet NaN 0x7FC00000 (any NaN range is stored as that pattern); when the
+ *   range or its reciprocal is not finite (a NaN or infinite value, a range
+ *   beyond fp32, a subnormal range whose reciprocal overflows) every u of the
+ *   channel is 0, so its chunk means and scales are 0 and its codes 0.
  * Decode (fp64 here): Lv[k] = fp16 nearest(((1+alpha)^(k/63) - 1)/alpha);
  *   anchor-only code 16A, full code 16A + r - 7;
  *   x = mn + rng * (mu + s * sgn(code) * Lv[min(|code|, 64)]).
  */
+#include <float.h>
 #include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
@@ -50,6 +57,14 @@
 /* ------------------------------------------------------------------ */
 /* number formats                                                     */
 /* ------------------------------------------------------------------ */
+
+static float qnan_f32(void)
+{
+    uint32_t b = 0x7FC00000u;
+    float f;
+    memcpy(&f, &b, 4);
+    return f;
+}
 
 static float bf16_to_f32(uint16_t b)
 {
@@ -193,10 +208,15 @@ static void encode_page(const uint16_t *x, int n, const float *thr, uint8_t *anc
         /* stage 1: page-level normalisation over the valid tokens */
         float mn = 0.0f, rng = 0.0f;
         if (n > 0) {
-            float mx = bf16_to_f32(x[d]);
-            mn = mx;
-            for (int t = 1; t < n; ++t) {
+            float mx = -INFINITY;
+            int has_nan = 0;
+            mn = INFINITY;
+            for (int t = 0; t < n; ++t) {
                 float v = bf16_to_f32(x[(size_t)t * ORC_D + d]);
+                if (v != v) {
+                    has_nan = 1;
+                    continue;
+                }
                 if (v < mn)
                     mn = v;
                 if (v > mx)
@@ -207,10 +227,16 @@ static void encode_page(const uint16_t *x, int n, const float *thr, uint8_t *anc
             mn = mn + 0.0f;
             mx = mx + 0.0f;
             rng = mx - mn;
+            if (has_nan)
+                mn = rng = qnan_f32();
+            if (rng != rng)
+                rng = qnan_f32();
         }
         float inv_r = rng > 0.0f ? 1.0f / rng : 0.0f;
+        /* statistics fp32 cannot carry: the channel is coded as constant */
+        int degenerate = !(rng <= FLT_MAX) || !(inv_r <= FLT_MAX);
         for (int t = 0; t < n; ++t)
-            u[t] = (bf16_to_f32(x[(size_t)t * ORC_D + d]) - mn) * inv_r;
+            u[t] = degenerate ? 0.0f : (bf16_to_f32(x[(size_t)t * ORC_D + d]) - mn) * inv_r;
         pm[d] = mn;
         pm[ORC_D + d] = rng;
 

@@ -261,3 +261,47 @@ def test_ragged_chunk_metadata_against_fp64_statistics(orc):
         smax = np.abs(uj - cm[j, 0]).max(0)
         assert np.all(cm[j, 1] >= smax - 1e-6) and np.all(cm[j, 1] - smax <= np.spacing(
             cm[j, 1].astype(np.float16)).astype(np.float64) + 1e-6), j
+
+
+def _special_page():
+    """A page with channels whose statistics fp32 cannot carry, and the same page
+    without them."""
+    base = _page(97)
+    xf = S.bf16_bits_to_f32(base).copy()
+    xf[0, 0, :, 4] = np.abs(xf[0, 0, :, 4])
+    xf[0, 0, 9, 4] = np.inf                             # infinite value: range inf
+    xf[0, 0, :, 5] = 1.0
+    xf[0, 0, 3, 5], xf[0, 0, 200, 5] = -3.0e38, 3.0e38  # finite values, range beyond fp32
+    xf[0, 0, :, 6] = 0.0
+    xf[0, 0, 17, 6] = 2.0 ** -130                       # subnormal range, 1/range overflows
+    xf[0, 0, :, 8] = 0.0
+    xf[0, 0, 40, 8] = 2.0 ** -126                       # smallest normal range: representable
+    xb = S.f32_to_bf16_bits(xf)
+    xb[0, 0, 5, 3] = 0x7FC1                             # a NaN (non-canonical payload)
+    return base, xb
+
+
+def test_unrepresentable_statistics_code_the_channel_as_constant(orc):
+    """Reading for inputs the pages leave open: a NaN value stores min and range
+    as the quiet NaN 0x7FC00000; a range (or reciprocal) that fp32 cannot carry
+    codes every value of the channel as 0 with chunk mean and scale 0; other
+    channels, and a tiny but representable range, are untouched."""
+    base, xb = _special_page()
+    q, qb = orc.quantize(xb), orc.quantize(base)
+    A, r, c = _codes_from_planes(q)
+    pm, cm = q["page_meta"][0, 0, 0], q["chunk_meta"][0, 0, 0]
+    assert pm[0, 3].view(np.uint32) == 0x7FC00000 and pm[1, 3].view(np.uint32) == 0x7FC00000
+    assert np.isinf(pm[1, 4]) and np.isfinite(pm[0, 4])
+    assert np.isinf(pm[1, 5]) and pm[0, 5] == np.float32(S.bf16_bits_to_f32(xb)[0, 0, 3, 5])
+    assert pm[0, 6] == 0.0 and pm[1, 6] == np.float32(2.0 ** -130)
+    for ch in (3, 4, 5, 6):
+        assert np.all(c[0, 0, :, ch] == 0), ch
+        assert np.all(A[0, 0, :, ch] == 0) and np.all(r[0, 0, :, ch] == 7), ch
+        assert np.all(cm[:, :, ch] == 0), ch
+    # the smallest normal range is an ordinary channel: u = 1 at token 40, 0 elsewhere
+    assert pm[1, 8] == np.float32(2.0 ** -126)
+    assert c[0, 0, 40, 8] == 63 and np.count_nonzero(c[0, 0, :, 8]) >= 1
+    others = [d for d in range(D) if d not in (3, 4, 5, 6, 8)]
+    cb = _codes_from_planes(qb)[2]
+    assert np.array_equal(c[..., others], cb[..., others])
+    assert np.array_equal(q["page_meta"][..., others].view(np.uint32), qb["page_meta"][..., others].view(np.uint32))
