@@ -109,17 +109,18 @@ lynx_status lynx_quantize_pages(const void *x_bf16, const int32_t *page_valid, c
                                 void *stream);
 
 /*
- * Anchor-only reconstruction, the draft cache of section 4 ("Anchor stream
- * lands, decoding starts"): every element decoded from its anchor with the
- * residual taken at its centre (code 16A).
+ * Anchor-only reconstruction, the draft cache of section 4 (decoding begins
+ * as soon as the anchor planes are in, its tokens marked as drafts): every
+ * element decoded from its anchor with the residual taken at its centre
+ * (code 16A).
  *   in   planes and metadata (residual may be NULL)
  *   out  device, [layers][kv_heads][tokens][128] in `dt` (bf16 nearest or fp32)
  */
 lynx_status lynx_dequant_anchor(const lynx_qkv *in, void *out, lynx_out_dtype dt, void *stream);
 
 /*
- * Residual refinement in place (section 4, "the kernel refines the cache to
- * Q_full"): overwrites the dense cache that lynx_dequant_anchor wrote with the
+ * Residual refinement in place (section 4: once the residual planes are in,
+ * the cache is brought to the full quantization): overwrites the dense cache that lynx_dequant_anchor wrote with the
  * full reconstruction from anchor and residual planes (code 16A + r - 7). The
  * planes are not modified. `inout` has the layout and dtype of the
  * lynx_dequant_anchor output; in->residual must be non-NULL.

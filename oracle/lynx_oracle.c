@@ -144,8 +144,8 @@ void orc_tables(float *thr, uint16_t *lv)
 }
 
 /* Stage 3 for one value: level count, then the sign-aware code.
- * Reading: the map rounds half up in the log domain (a threshold count), and
- * "negative zero" -- a negative w whose level rounds to 0 -- becomes -1, so a
+ * Reading: the map rounds half up in the log domain (a threshold count), and a
+ * negative w whose level rounds to 0 becomes -1 (the sign-aware rule), so a
  * small negative value decodes below the chunk mean; other negatives keep -q. */
 static int code_of(float w, const float *thr)
 {

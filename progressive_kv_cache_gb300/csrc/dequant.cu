@@ -2,9 +2,9 @@
 // refinement (K3) for sm_103a.
 //
 // "Lynx: the KV cache does not have to arrive whole" (aigenapps reading),
-// section 4: the anchor stream alone is the draft cache ("Anchor stream lands,
-// decoding starts"); when the residual lands "the kernel refines the cache to
-// Q_full". Both are streaming decodes of the planes: per element one nibble
+// section 4: the anchor planes alone give the draft cache that decoding starts
+// from; once the residual planes are in, the cache is refined to the full
+// quantization. Both are streaming decodes of the planes: per element one nibble
 // (pair) lookup and one fused multiply-add,
 //   x = a + b * Ls(code),  a = mn + rng * mu,  b = rng * s  (per chunk, channel).
 // Refinement rewrites the dense cache written by the anchor pass with the full

@@ -21,28 +21,25 @@ constexpr int kQMax = 63;      // codes -63..63 (127 levels)
 constexpr int kBias = 7;       // +7 before the 4-bit cut
 constexpr double kAlpha = 255.0;
 
-// Stage-3 bucket table. The fp32 value |w| in [2^-13, 2) falls in bucket
-// ((bits >> 19) - kBucketBase): 16 buckets per octave, each narrower than the
-// gap between two consecutive thresholds, so at most one threshold lies inside
-// a bucket. Entry = {bits of that threshold (0xFFFFFFFF if none), number of
-// thresholds at or below the bucket's lower edge}. Entry kNBucket catches
-// |w| < 2^-13 (below the first threshold) and non-finite values.
-constexpr uint32_t kBucketBase = (127u - 13u) << 4;
-constexpr int kNBucket = 14 * 16;
+// Stage-3 bucket table. The code of w depends only on |w| through the count
+// q = #{k : |w| >= T_k}, and the table finds q with one lookup and one
+// compare: the bucket of |w| is bits(fp32(|w| + 2^-13)) >> 19, a monotone
+// function of |w| with 16 buckets per octave of |w| + 2^-13, each narrower
+// than the gap between two consecutive thresholds, so at most one threshold
+// T* lies in a bucket (the builder checks this). |w| in [0, 2) gives buckets
+// kBucketBase .. kBucketBase + kNBucket - 1 with no clamp. Each entry holds
+// the bits of the float just below T* (+inf when the bucket holds none), so
+// that |w| >= T* exactly when pred(T*) - |w| is negative, and the four
+// possible stored bytes (c + 7) & 0xFF, selected by 2*sign(w) + (|w| >= T*):
+//   byte 0: w >= 0 below T*   byte 1: w >= 0 at or above T*
+//   byte 2: w < 0 below T*    byte 3: w < 0 at or above T*
+// (sign(w) is the sign bit: the encoder turns -0 into +0 first).
+constexpr uint32_t kBucketBase = (127u - 13u) << 4;   // bucket of 2^-13
+constexpr int kNBucket = 15 * 16;                      // |w| + 2^-13 in [2^-13, 4)
+constexpr uint32_t kBucketOffsetBits = (127u - 13u) << 23;   // 2^-13
 
-struct MapTable {
-    uint2 e[kNBucket + 1];
-};
-
-// The same buckets as the encoder uses them: entry 0 catches |w| below the
-// first bucket (and NaN), entry 1 + i is bucket i. Each entry holds the bits
-// of the threshold inside the bucket (an all-ones NaN pattern when there is
-// none, so the compare fails) and the four possible stored bytes
-// (c + 7) & 0xFF, selected by 2*(w < 0) + (|w| >= threshold):
-//   byte 0: w >= 0 below the threshold   byte 1: w >= 0 at or above it
-//   byte 2: w < 0 below the threshold    byte 3: w < 0 at or above it
 struct CodeTable {
-    uint2 e[kNBucket + 1];
+    uint2 e[kNBucket];
 };
 
 // Signed level values used by the decoders:
@@ -56,7 +53,6 @@ struct LevelTable {
 struct HostTables {
     float thr[64];
     uint16_t lv[65];
-    MapTable map;
     CodeTable code;
     LevelTable lev;
     bool ok;

@@ -1,9 +1,9 @@
 // lynx_tables.cu -- host-built tables of the Lynx quantizer, and device queries.
 //
 // Thresholds and level values come from section 3 of the aigenapps reading of
-// Lynx ("an alpha-law logarithmic map onto 2^7 - 1 = 127 levels"; "reconstructed
-// magnitude scales as (1+alpha)^q"), evaluated in double on the host and rounded
-// once: thresholds to fp32, levels to fp16.
+// Lynx (a logarithmic alpha-law map of |w| onto 127 levels, whose reconstructed
+// magnitude grows geometrically as (1+alpha)^q), evaluated in double on the
+// host and rounded once: thresholds to fp32, levels to fp16.
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -50,38 +50,33 @@ void build(HostTables &t)
         lvf[k] = __half2float(h);
     }
 
-    // stage-3 buckets
+    // stage-3 buckets: bucket of each threshold under the encoder's index
+    // function, evaluated in fp32 exactly as on the device
+    int tb[kQMax + 1];
+    for (int k = 1; k <= kQMax; ++k) {
+        volatile float sum = t.thr[k] + f32_from_bits(kBucketOffsetBits);
+        tb[k] = (int)(f32_bits(sum) >> 19) - (int)kBucketBase;
+        if (tb[k] < 0 || tb[k] >= kNBucket || !(t.thr[k] > 0.0f) || (k > 1 && !(t.thr[k] > t.thr[k - 1])))
+            t.ok = false;
+    }
+    auto byte_of = [](int c) { return (uint32_t)(c + kBias) & 0xFFu; };
     for (int i = 0; i < kNBucket; ++i) {
-        uint32_t lo = (kBucketBase + (uint32_t)i) << 19;
-        uint32_t hi = lo + (1u << 19);
-        int q0 = 0, inside = 0, next = -1;
+        int q0 = 0, inside = 0, kin = 0;
         for (int k = 1; k <= kQMax; ++k) {
-            uint32_t tb = f32_bits(t.thr[k]);
-            if (tb <= lo)
+            if (tb[k] < i)
                 ++q0;
-            else if (tb < hi) {
+            else if (tb[k] == i) {
                 ++inside;
-                next = k;
+                kin = k;
             }
         }
         if (inside > 1)
             t.ok = false;   // would break the one-compare lookup
-        t.map.e[i] = make_uint2(next > 0 ? f32_bits(t.thr[next]) : 0xFFFFFFFFu, (uint32_t)q0);
-    }
-    // everything below 2^-13 is below the first threshold
-    if (f32_bits(t.thr[1]) < (kBucketBase << 19))
-        t.ok = false;
-    t.map.e[kNBucket] = make_uint2(0xFFFFFFFFu, 0u);
-    (void)f32_from_bits;
-
-    // biased code bytes for the encoder's table (sentinel first)
-    auto byte_of = [](int c) { return (uint32_t)(c + kBias) & 0xFFu; };
-    for (int i = 0; i <= kNBucket; ++i) {
-        const uint2 m = i == 0 ? t.map.e[kNBucket] : t.map.e[i - 1];
-        const int q0 = (int)m.y, q1 = q0 + 1 > kQMax ? kQMax : q0 + 1;
+        const int q1 = q0 + 1 > kQMax ? kQMax : q0 + 1;
         const int n0 = -(q0 > 1 ? q0 : 1), n1 = -(q1 > 1 ? q1 : 1);
         const uint32_t bytes = byte_of(q0) | (byte_of(q1) << 8) | (byte_of(n0) << 16) | (byte_of(n1) << 24);
-        t.code.e[i] = make_uint2(m.x, bytes);
+        const uint32_t below = inside ? f32_bits(t.thr[kin]) - 1u : 0x7F800000u;
+        t.code.e[i] = make_uint2(below, bytes);
     }
 
     // decoder levels

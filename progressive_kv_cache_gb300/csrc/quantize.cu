@@ -18,6 +18,15 @@
 // compare and one byte permute. The packed planes are staged in shared memory
 // and leave with two 16 KiB bulk stores; the metadata goes out with direct
 // 4/8-byte stores.
+//
+// The kernel is bound by instruction issue, so the per-element work is kept
+// short: the bucket index needs no clamp (|w| + 2^-13 always lands in the
+// table), the threshold test is the sign of pred(T*) - |w|, and the chunk's
+// max |v| comes from its two extremes instead of a max over all elements (v
+// is a monotone function of x, so the extremes of x give the extremes of v).
+// Codes are computed for a group of tokens before the group's stores: a table
+// load may not move above an earlier store to shared memory, so interleaving
+// them would serialise the tokens.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -32,7 +41,11 @@ constexpr int kCopies = 16;                            // table replicas (one pe
 constexpr uint32_t kPageBytes = kPage * kD * 2;       // 64 KiB of bf16
 constexpr uint32_t kPlaneBytes = kPage * kD / 2;      // 16 KiB per plane and page
 constexpr uint32_t kWaitLimit = 1u << 22;
-constexpr uint32_t kClampLoBits = (kBucketBase << 19) - 1u;   // largest float below 2^-13
+constexpr uint32_t kQNaN = 0x7FC00000u;
+constexpr int kGroup = 16;                           // tokens whose codes are computed before their stores
+static_assert(kGroup > 0 && kChunk % kGroup == 0, "groups must tile the chunk");
+constexpr float kF32Max = 3.40282347e38f;
+
 
 struct Smem {
     uint16_t x[2][kPage * kD];         // double-buffered input page
@@ -40,7 +53,7 @@ struct Smem {
     uint8_t res[kPage * kD / 2];       // staged residual plane of the page
     uint32_t pmin[kNChunk][kD / 2];    // bf16x2 chunk minima of channel pairs
     uint32_t pmax[kNChunk][kD / 2];
-    uint2 tab[(kNBucket + 1) * kCopies];
+    uint2 tab[kNBucket * kCopies];
     alignas(8) uint64_t bar[2];
 };
 
@@ -61,29 +74,40 @@ __device__ __forceinline__ uint2 lds_u2(uint32_t addr)
     return v;
 }
 
-// Stage 3 + the +7 bias for one value: the stored byte (c + 7) & 0xFF, whose
-// high nibble is the anchor and low nibble the residual. `tab_base` is the
-// shared address of this lane's table replica, offset so that the bucket
-// number (float bits >> 19) indexes it directly.
+// Stage 3 + the +7 bias for one value w (|w| < 2, never -0): the stored byte
+// (c + 7) & 0xFF (bits 8-31 zero), whose high nibble is the anchor and low
+// nibble the residual.
+// `tab_base` is the shared address of this lane's table replica, offset so
+// that the bucket number indexes it directly.
 __device__ __forceinline__ uint32_t code_byte(float w, uint32_t tab_base)
 {
     const float a = fabsf(w);
-    const float cl = fmaxf(a, __uint_as_float(kClampLoBits));
-    const uint2 e = lds_u2(tab_base + (__float_as_uint(cl) >> 19) * (kCopies * 8));
-    const uint32_t sel = (a >= __uint_as_float(e.x) ? 1u : 0u) | (w < 0.0f ? 2u : 0u);
-    return __byte_perm(e.y, 0u, sel);
+    const uint32_t bucket = __float_as_uint(__fadd_rn(a, __uint_as_float(kBucketOffsetBits))) >> 19;
+    const uint2 e = lds_u2(bucket * (kCopies * 8) + tab_base);
+    // |w| >= T* exactly when pred(T*) - |w| < 0 (its sign bit); 2 * sign(w)
+    // is bits 31-30 of w (bit 30 is 0 for |w| < 2); 0x4440 makes the permute
+    // fill bytes 1-3 of the result with zeros
+    const uint32_t d = __float_as_uint(__fsub_rn(__uint_as_float(e.x), a));
+    return __byte_perm(e.y, 0u, (d >> 31) + (__float_as_uint(w) >> 30) + 0x4440u);
 }
 
+// bf16x2 min / max that propagate NaN (a NaN value marks its channel)
 __device__ __forceinline__ uint32_t bf2_min(uint32_t a, uint32_t b)
 {
-    __nv_bfloat162 r = __hmin2(*reinterpret_cast<__nv_bfloat162 *>(&a), *reinterpret_cast<__nv_bfloat162 *>(&b));
+    __nv_bfloat162 r = __hmin2_nan(*reinterpret_cast<__nv_bfloat162 *>(&a), *reinterpret_cast<__nv_bfloat162 *>(&b));
     return *reinterpret_cast<uint32_t *>(&r);
 }
 
 __device__ __forceinline__ uint32_t bf2_max(uint32_t a, uint32_t b)
 {
-    __nv_bfloat162 r = __hmax2(*reinterpret_cast<__nv_bfloat162 *>(&a), *reinterpret_cast<__nv_bfloat162 *>(&b));
+    __nv_bfloat162 r = __hmax2_nan(*reinterpret_cast<__nv_bfloat162 *>(&a), *reinterpret_cast<__nv_bfloat162 *>(&b));
     return *reinterpret_cast<uint32_t *>(&r);
+}
+
+// A bf16x2 word as float2 (x = low half).
+__device__ __forceinline__ float2 bf2_to_f2(uint32_t x)
+{
+    return make_float2(__uint_as_float(x << 16), __uint_as_float(x & 0xFFFF0000u));
 }
 
 // Stages 2-4 for this thread's two channels of one chunk, held as float2
@@ -91,11 +115,13 @@ __device__ __forceinline__ uint32_t bf2_max(uint32_t a, uint32_t b)
 // instruction performs the contract's operation for both channels (every lane
 // of __fadd2_rn / __fmul2_rn is one IEEE round-to-nearest operation, and
 // x - y is computed as x + (-y), which is the same operation). `full` chunks
-// have 32 valid tokens, others nc. Writes the staged plane bytes and returns
-// the chunk metadata (mean, scale) of both channels as fp16x2 words.
+// have 32 valid tokens, others nc; ulo / uhi are u at the chunk's smallest and
+// largest valid x. Writes the staged plane bytes and returns the chunk
+// metadata (mean, scale) of both channels as fp16x2 words.
 template <bool FULL>
-__device__ __forceinline__ void encode_chunk(float2 (&u)[kChunk], int nc, uint32_t tab_base, uint8_t *anc_row0,
-                                             uint8_t *res_row0, uint32_t &mu2, uint32_t &s2)
+__device__ __forceinline__ void encode_chunk(const float2 (&u)[kChunk], int nc, float2 ulo, float2 uhi,
+                                             uint32_t tab_base, uint8_t *anc_row0, uint8_t *res_row0,
+                                             uint32_t &mu2, uint32_t &s2)
 {
     // chunk mean: stride-halving pairwise tree over 32 slots, absent slots +0
     const float2 zero = make_float2(0.0f, 0.0f);
@@ -119,31 +145,40 @@ __device__ __forceinline__ void encode_chunk(float2 (&u)[kChunk], int nc, uint32
     const __half mh1 = __float2half_rn(mean.y);
     const float2 negmu = make_float2(-__half2float(mh0), -__half2float(mh1));
 
-    float s0 = 0.0f, s1 = 0.0f;
-#pragma unroll
-    for (int i = 0; i < kChunk; ++i) {
-        u[i] = __fadd2_rn(u[i], negmu);   // u becomes v = u - mu
-        if (FULL || i < nc) {
-            s0 = fmaxf(s0, fabsf(u[i].x));
-            s1 = fmaxf(s1, fabsf(u[i].y));
-        }
-    }
+    // max |v| over the chunk: v = u - mu is non-decreasing in u, so it is
+    // reached at the chunk's extremes
+    const float2 vlo = __fadd2_rn(ulo, negmu), vhi = __fadd2_rn(uhi, negmu);
+    const float s0 = fmaxf(fabsf(vlo.x), fabsf(vhi.x)), s1 = fmaxf(fabsf(vlo.y), fabsf(vhi.y));
     const __half sh0 = __float2half_ru(s0), sh1 = __float2half_ru(s1);
     const float sf0 = __half2float(sh0), sf1 = __half2float(sh1);
     const float2 inv_s = make_float2(sf0 > 0.0f ? __frcp_rn(sf0) : 0.0f, sf1 > 0.0f ? __frcp_rn(sf1) : 0.0f);
 
+    // groups of kGroup tokens: all lookups of a group, then its stores (a
+    // table load may not move above an earlier store to shared memory, so
+    // interleaving them would serialise the tokens)
 #pragma unroll
-    for (int i = 0; i < kChunk; ++i) {
-        uint32_t ab = 0x00u, rb = 0x77u;                 // code 0: anchor 0, residual 7
-        if (FULL || i < nc) {
-            const float2 w = __fmul2_rn(u[i], inv_s);
-            const uint32_t b0 = code_byte(w.x, tab_base);
-            const uint32_t b1 = code_byte(w.y, tab_base);
-            ab = ((b0 >> 4) & 0x0Fu) | (b1 & 0xF0u);
-            rb = (b0 & 0x0Fu) | ((b1 << 4) & 0xF0u);
+    for (int g0 = 0; g0 < kChunk; g0 += kGroup) {
+        uint32_t ab[kGroup], rb[kGroup];
+#pragma unroll
+        for (int k = 0; k < kGroup; ++k) {
+            const int i = g0 + k;
+            ab[k] = 0x00u;                               // code 0: anchor 0, residual 7
+            rb[k] = 0x77u;
+            if (FULL || i < nc) {
+                // w = v * inv_s, as one rounding of the product plus +0, which
+                // turns a -0 product into +0 (both code 0) and changes nothing else
+                const float2 w = __ffma2_rn(__fadd2_rn(u[i], negmu), inv_s, zero);
+                const uint32_t b0 = code_byte(w.x, tab_base);
+                const uint32_t b1 = code_byte(w.y, tab_base);
+                ab[k] = (b0 >> 4) | (b1 & 0xF0u);
+                rb[k] = (b0 & 0x0Fu) | ((b1 << 4) & 0xF0u);
+            }
         }
-        anc_row0[i * (kD / 2)] = (uint8_t)ab;
-        res_row0[i * (kD / 2)] = (uint8_t)rb;
+#pragma unroll
+        for (int k = 0; k < kGroup; ++k) {
+            anc_row0[(g0 + k) * (kD / 2)] = (uint8_t)ab[k];
+            res_row0[(g0 + k) * (kD / 2)] = (uint8_t)rb[k];
+        }
     }
     mu2 = (uint32_t)__half_as_ushort(mh0) | ((uint32_t)__half_as_ushort(mh1) << 16);
     s2 = (uint32_t)__half_as_ushort(sh0) | ((uint32_t)__half_as_ushort(sh1) << 16);
@@ -158,7 +193,7 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_kernel(Params p, CodeTab
     const int j = warp >> 1;                       // chunk of this warp
     const int pi = (warp & 1) * 32 + lane;         // channel pair: channels 2pi, 2pi+1
 
-    for (int i = tid; i < (kNBucket + 1) * kCopies; i += kThreads)
+    for (int i = tid; i < kNBucket * kCopies; i += kThreads)
         sm.tab[i] = table.e[i / kCopies];
     if (tid == 0) {
         mbar_init(&sm.bar[0], 1);
@@ -166,7 +201,7 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_kernel(Params p, CodeTab
         fence_mbar_init();
     }
     __syncthreads();
-    const uint32_t tab_base = smem_u32(&sm.tab[lane & (kCopies - 1)]) - (kBucketBase - 1u) * (kCopies * 8);
+    const uint32_t tab_base = smem_u32(&sm.tab[lane & (kCopies - 1)]) - kBucketBase * (kCopies * 8);
 
     const int64_t first = blockIdx.x, stride = gridDim.x;
     if (tid == 0 && first < p.pages) {
@@ -203,17 +238,15 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_kernel(Params p, CodeTab
 #pragma unroll
         for (int i = 0; i < kChunk; ++i)
             xw[i] = *reinterpret_cast<const uint32_t *>(xs + i * kD);
-        {
-            uint32_t mn2 = 0x7F807F80u, mx2 = 0xFF80FF80u;   // +inf, -inf pairs
+        uint32_t cmn2 = 0x7F807F80u, cmx2 = 0xFF80FF80u;   // +inf, -inf pairs
 #pragma unroll
-            for (int i = 0; i < kChunk; ++i)
-                if (i < nc) {
-                    mn2 = bf2_min(mn2, xw[i]);
-                    mx2 = bf2_max(mx2, xw[i]);
-                }
-            sm.pmin[j][pi] = mn2;
-            sm.pmax[j][pi] = mx2;
-        }
+        for (int i = 0; i < kChunk; ++i)
+            if (i < nc) {
+                cmn2 = bf2_min(cmn2, xw[i]);
+                cmx2 = bf2_max(cmx2, xw[i]);
+            }
+        sm.pmin[j][pi] = cmn2;
+        sm.pmax[j][pi] = cmx2;
         if (tid == 0)
             bulk_wait_read_all();   // the previous page's planes have left the staging tile
         __syncthreads();
@@ -232,16 +265,45 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_kernel(Params p, CodeTab
         mn1 = __fadd_rn(mn1, 0.0f);
         mx0 = __fadd_rn(mx0, 0.0f);
         mx1 = __fadd_rn(mx1, 0.0f);
-        const float rg0 = __fsub_rn(mx0, mn0), rg1 = __fsub_rn(mx1, mn1);
-        const float ir0 = rg0 > 0.0f ? __frcp_rn(rg0) : 0.0f;
-        const float ir1 = rg1 > 0.0f ? __frcp_rn(rg1) : 0.0f;
-
-        float2 u[kChunk];
-        {
-            const float2 negmn = make_float2(-mn0, -mn1), ir = make_float2(ir0, ir1);
+        float rg0 = __fsub_rn(mx0, mn0), rg1 = __fsub_rn(mx1, mn1);
+        // a NaN value (min and max NaN) stores min and range as the quiet NaN;
+        // so does any NaN range
+        if (mn0 != mn0)
+            mn0 = __uint_as_float(kQNaN);
+        if (mn1 != mn1)
+            mn1 = __uint_as_float(kQNaN);
+        if (rg0 != rg0)
+            rg0 = __uint_as_float(kQNaN);
+        if (rg1 != rg1)
+            rg1 = __uint_as_float(kQNaN);
+        float ir0 = rg0 > 0.0f ? __frcp_rn(rg0) : 0.0f;
+        float ir1 = rg1 > 0.0f ? __frcp_rn(rg1) : 0.0f;
+        // statistics fp32 cannot carry (range or reciprocal not finite): the
+        // channel is coded as constant, every u = 0 (x and min taken as 0)
+        const bool bad0 = !(rg0 <= kF32Max) || !(ir0 <= kF32Max);
+        const bool bad1 = !(rg1 <= kF32Max) || !(ir1 <= kF32Max);
+        float2 negmn = make_float2(-mn0, -mn1);
+        if (bad0 | bad1) {
+            const uint32_t keep = (bad0 ? 0xFFFF0000u : 0xFFFFFFFFu) & (bad1 ? 0x0000FFFFu : 0xFFFFFFFFu);
 #pragma unroll
             for (int i = 0; i < kChunk; ++i)
-                u[i] = __fmul2_rn(__fadd2_rn(make_float2(bf16_lo(xw[i]), bf16_hi(xw[i])), negmn), ir);
+                xw[i] &= keep;
+            cmn2 &= keep;
+            cmx2 &= keep;
+            if (bad0)
+                negmn.x = ir0 = 0.0f;
+            if (bad1)
+                negmn.y = ir1 = 0.0f;
+        }
+
+        float2 u[kChunk], ulo, uhi;
+        {
+            const float2 ir = make_float2(ir0, ir1);
+#pragma unroll
+            for (int i = 0; i < kChunk; ++i)
+                u[i] = __fmul2_rn(__fadd2_rn(bf2_to_f2(xw[i]), negmn), ir);
+            ulo = __fmul2_rn(__fadd2_rn(bf2_to_f2(cmn2), negmn), ir);
+            uhi = __fmul2_rn(__fadd2_rn(bf2_to_f2(cmx2), negmn), ir);
         }
 
         // (c) stages 2-4
@@ -249,9 +311,9 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_kernel(Params p, CodeTab
         uint8_t *res_row0 = sm.res + j * kChunk * (kD / 2) + pi;
         uint32_t mu2 = 0, s2 = 0;
         if (nc == kChunk) {
-            encode_chunk<true>(u, nc, tab_base, anc_row0, res_row0, mu2, s2);
+            encode_chunk<true>(u, nc, ulo, uhi, tab_base, anc_row0, res_row0, mu2, s2);
         } else if (nc > 0) {
-            encode_chunk<false>(u, nc, tab_base, anc_row0, res_row0, mu2, s2);
+            encode_chunk<false>(u, nc, ulo, uhi, tab_base, anc_row0, res_row0, mu2, s2);
         } else {
 #pragma unroll
             for (int i = 0; i < kChunk; ++i) {
@@ -284,20 +346,21 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_kernel(Params p, CodeTab
 }
 
 // The encoder's stage-3 path on arbitrary values (a diagnostic): the same
-// table and code_byte(), with |w| clamped below 2 first so that any input
-// stays inside the table (the encoder itself never sees |w| > 1 + 2^-23).
+// table and code_byte(), with |w| clamped below 2, -0 turned into +0 and NaN
+// into 0 first, so that any input stays inside the table (the encoder itself
+// sees only finite w with |w| <= 1 + 2^-23, never -0).
 __global__ void level_codes_kernel(const float *__restrict__ w, int64_t n, int8_t *__restrict__ codes,
                                    CodeTable table)
 {
-    __shared__ uint2 tab[(kNBucket + 1) * kCopies];
-    for (int i = threadIdx.x; i < (kNBucket + 1) * kCopies; i += blockDim.x)
+    __shared__ uint2 tab[kNBucket * kCopies];
+    for (int i = threadIdx.x; i < kNBucket * kCopies; i += blockDim.x)
         tab[i] = table.e[i / kCopies];
     __syncthreads();
-    const uint32_t tab_base = smem_u32(&tab[threadIdx.x & (kCopies - 1)]) - (kBucketBase - 1u) * (kCopies * 8);
+    const uint32_t tab_base = smem_u32(&tab[threadIdx.x & (kCopies - 1)]) - kBucketBase * (kCopies * 8);
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
         const float v = w[i];
-        const float c = copysignf(fminf(fabsf(v), 1.99999988f), v);
-        codes[i] = (int8_t)((int)(int8_t)code_byte(v == v ? c : v, tab_base) - kBias);
+        const float c = v == v ? __fadd_rn(copysignf(fminf(fabsf(v), 1.99999988f), v), 0.0f) : 0.0f;
+        codes[i] = (int8_t)((int)(int8_t)code_byte(c, tab_base) - kBias);
     }
 }
 

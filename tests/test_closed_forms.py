@@ -20,8 +20,8 @@ def test_worked_example_cache_size_is_23_5_gib():
     assert size / 2 ** 30 == f["stated_size_gb"]           # the page's "GB" is GiB
     t100 = size * 8 / 100e9
     t400 = size * 8 / 400e9
-    assert abs(t100 - f["stated_transfer_s_at_100gbps"]) < 0.05    # "about 2 seconds"
-    assert t400 > f["stated_lower_bound_s_at_400gbps"]             # "over 0.5 second"
+    assert abs(t100 - f["stated_transfer_s_at_100gbps"]) < 0.05    # roughly two seconds
+    assert t400 > f["stated_lower_bound_s_at_400gbps"]             # more than half a second
 
 
 def test_effective_bins_of_a_linear_grid_under_an_outlier(orc):

@@ -85,6 +85,27 @@ def test_special_values(lx, orc):
     assert_planes_equal(_encode(lx, xb), orc.quantize(xb))
 
 
+def test_unrepresentable_statistics(lx, orc):
+    """NaN, infinite, overflowing-range and subnormal-range channels (coded as
+    constant, NaN statistics stored as the quiet NaN) next to ordinary ones, in
+    every chunk position; bit-exact, metadata included."""
+    w = S.Workload("t", 79, L=1, H=2, T=512, n_outliers_fixed=3)
+    xf = S.bf16_bits_to_f32(S.laplace_bf16(w.key(S.S_K), w.scales(S.S_K), 1, 2, 512)).copy()
+    xf[0, 0, 9, 4] = np.inf
+    xf[0, 1, 300, 4] = -np.inf
+    xf[0, 0, :, 5] = 1.0
+    xf[0, 0, 3, 5], xf[0, 0, 200, 5] = -3.0e38, 3.0e38
+    xf[0, 1, :256, 6] = 0.0
+    xf[0, 1, 17, 6] = 2.0 ** -130
+    xf[0, 1, 256:, 8] = 0.0
+    xf[0, 1, 296, 8] = 2.0 ** -126
+    xb = S.f32_to_bf16_bits(xf)
+    xb[0, 0, 5, 3] = 0x7FC1
+    xb[0, 1, 511, 7] = 0xFF80           # -inf in the last token
+    xb[0, 1, 260, 9] = 0xFFC0           # negative NaN
+    assert_planes_equal(_encode(lx, xb), orc.quantize(xb))
+
+
 def test_qwen3_235b_like_layer_every_page(lx, orc):
     """4 KV heads x 32K tokens, K and V: every page bit-exact."""
     w = S.WORKLOADS[2]

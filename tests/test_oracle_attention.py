@@ -2,8 +2,8 @@
 
 Decode attention over the reconstructed cache is the textbook
 softmax(sm_scale * q K^T) V ("KV-cache quantization" explainer, aicassindra,
-"Middle row": quantized keys and values are dequantized on read and feed Q.K^T,
-softmax and the weighted sum over V). Pins: numpy's matmul/softmax over the
+"Middle row": the stored keys and values are expanded back to real numbers as
+they are read, then go through Q.K^T, the softmax and the weighted sum over V). Pins: numpy's matmul/softmax over the
 oracle's own dense reconstruction (through a permuted page table), single-token
 and uniform-score special cases, the anchor/full identity when every residual is
 centred, GQA head grouping, empty contexts and the scores output.

@@ -1,10 +1,11 @@
 """Pins of stage 3 (alpha-law map, sign-aware mapping) and stage 4 (bias, cut).
 
-Lynx reading, section 3: "an alpha-law logarithmic map onto 2^7 - 1 = 127
-levels"; "a round-half-down bias of +7 applied before the shift makes the
-residual a centred signed correction"; "a sign-aware mapping sends negative
-zero to distinct negative integers, preserving the sign of small-magnitude
-values"; "4 bits anchor plus 4 bits residual".
+Lynx reading, section 3: |w| goes through a logarithmic alpha-law map onto
+127 levels; small negative values keep their sign through a sign-aware rule
+(a negative w whose level rounds to 0 is coded -1); adding 7 before the 4-bit
+shift rounds the anchor half down, so the residual is a signed correction
+centred on the anchor; each code is cut into a 4-bit anchor and a 4-bit
+residual.
 """
 import numpy as np
 
