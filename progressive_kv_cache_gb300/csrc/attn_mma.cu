@@ -15,22 +15,28 @@
 // so the tensor-core operands on the cache side are the level values
 // themselves (no rounding), and the dense operand (q b, or p) is split into an
 // fp16 hi/lo pair to keep fp32-level accuracy (mma.sync m16n8k16, fp32
-// accumulation). The MMA rows are 8 query heads' hi parts over the same heads'
-// lo parts, so one MMA carries both halves of the split.
+// accumulation).
 //
-// Work: a CTA per (page range, KV head, request) with 8 warps per group of 8
-// query heads; warp w owns chunk w % 8 for head group w / 8. A page's K planes
-// and V planes arrive by bulk copy into their own buffers. Per page:
-//   K phase: the warps of chunk j turn its 32 x 128 K codes into fp16 levels
-//            in a swizzled shared-memory tile (one table lookup per code byte),
-//            then each warp runs Q.K^T on it (B fragments by ldmatrix) and the
-//            online softmax of its 8 heads;
-//   V phase: the same warps overwrite the tile with the chunk's V levels and
-//            run P.V (B fragments by ldmatrix.trans).
-// Each code is decoded once per CTA; a K or V buffer is refilled with a later
-// page as soon as its codes are decoded. The chunks' running (max, sum, output)
-// are merged in shared memory into one partial per query head; a second
-// kernel merges the partials of the ranges.
+// Register-direct operands. A code byte holds two channels of one token, and
+// the MMA's B fragment wants two adjacent k-indices of one column in one
+// register. Q.K^T contracts over channels, so the channel order inside the
+// contraction is free: lane (g, q) of the warp reads 16 code bytes of token g
+// of an 8-token tile (channels 32q .. 32q + 31) and every byte, through one
+// table lookup, is a finished B register; the A fragments (q b) follow the
+// same channel order. P.V contracts over tokens: the nibbles of one channel of
+// two tokens are merged into one byte (two logic operations per four bytes),
+// whose lookup is again a finished B register. No decoded value touches shared
+// memory. The lookup table is replicated per lane (conflict-free) with entries
+// 256 bytes apart, so that one byte permute forms the whole address.
+//
+// Work: a CTA per (page range, KV head, request): one producer warp streams
+// the pages' K and V planes and metadata by bulk copy into a ring of slots
+// (one tensor's page per slot); consumer warp j owns chunk j of every page and
+// all query heads of the group: with up to 8 heads the MMA rows are the heads'
+// hi parts over their lo parts; with up to 16 the rows are the heads and hi and
+// lo go through two MMAs into the same accumulators. The chunks' running (max,
+// sum, output) are merged in shared memory into one partial per query head; a
+// second kernel merges the partials of the ranges.
 #include <cuda_fp16.h>
 
 #include "lynx_internal.cuh"
@@ -41,43 +47,41 @@ namespace {
 
 constexpr uint32_t kPlane = kPage * kD / 2;   // 16 KiB: one page of one plane
 constexpr int kRow = kD / 2;                  // code bytes per token
-constexpr int kTileRow = kD * 2;              // bytes per token of an fp16 tile
 constexpr int kPart = kD + 2;
+constexpr int kCons = kNChunk;                // consumer warps, one per chunk
+constexpr int kThreads = (kCons + 1) * 32;    // + one producer warp
+constexpr int kAff = kD + 16;                 // channel c stored at c + 4 (c / 32): no bank conflicts
 constexpr uint32_t kWaitLimit = 1u << 22;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
 // One tensor's page as it arrives.
 template <bool FULL>
-struct Raw {
+struct Slot {
     uint8_t a[kPlane];
     uint8_t r[FULL ? kPlane : 16];
     float pm[2 * kD];
     uint16_t cm[kNChunk * 2 * kD];
 };
 
-template <bool FULL, int NB>
+template <bool FULL, int NS>
 struct Smem {
-    Raw<FULL> rk[NB], rv[NB];
-    // fp16 levels of chunk j ([32 tokens][128 channels], K then V); the
-    // 16-byte slot s of token t sits at slot s ^ (t & 7) so that 8 rows of one
-    // slot column (an ldmatrix 8x8 matrix) fall in distinct banks
-    uint16_t dec[kNChunk][kChunk * kD];
-    // chunk affines of channel pairs: (a_2i, a_2i+1, b_2i, b_2i+1)
-    float4 kab[kNChunk][kD / 2];
-    float4 vab[kNChunk][kD / 2];
-    float qs[16][kD + 8];                     // the group's queries times sm_scale log2(e); unused rows 0
-    // level table, one copy per lane (conflict-free lookups): anchor mode maps a
-    // byte of two anchors to the half2 of their levels, full mode a code byte
-    // (A << 4 | r) to the fp16 level
-    uint32_t lut[FULL ? 256 * 32 / 2 : 256 * 32];
-    float rmaxw[16];                          // per warp: max |b| of K in its chunk
+    // level table: entry e (a code byte) at byte 256 e; anchor mode: word
+    // `lane` = half2 of the levels of the two anchor nibbles of e; full mode:
+    // word `lane` = fp16 level of the code byte e (A << 4 | r) in its low half
+    uint32_t lut[256 * 64];
+    // the group's queries times sm_scale log2(e), as this lane's A-fragment
+    // channels: qf[s][r][lane] = q[row g + 8 r][32 q + 4 s .. + 3]
+    float4 qf[8][2][32];
+    Slot<FULL> slot[NS];
+    // per consumer warp and tensor (K, V): chunk affines a and b
+    float aff[kCons][2][2][kAff];
     float qmax;
-    alignas(8) uint64_t bar_k[NB];
-    uint64_t bar_v[NB];
+    alignas(8) uint64_t full_bar[NS];
+    uint64_t empty_bar[NS];
 };
 
-struct Merge {                                // overlays the raw buffers after the page loop
+struct Merge {                                // overlays the table and queries after the page loop
     float m[kNChunk][16];                     // per chunk and query head
     float l[kNChunk][16];
     float o[kNChunk][16][kD];
@@ -91,161 +95,148 @@ __device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], 
                  : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4])
-{
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(addr));
-}
-
-__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4])
-{
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(addr));
-}
-
 // (x0, x1) -> fp16 pairs hi and lo with hi + lo = (x0, x1) to ~22 bits.
 __device__ __forceinline__ void split2(float2 x, uint32_t &hi, uint32_t &lo)
 {
     const __half2 h = __floats2half2_rn(x.x, x.y);
-    const float2 hf = __half22float2(h);
-    const __half2 l = __floats2half2_rn(x.x - hf.x, x.y - hf.y);
+    const float2 r = __ffma2_rn(__half22float2(h), make_float2(-1.0f, -1.0f), x);
+    const __half2 l = __floats2half2_rn(r.x, r.y);
     hi = *reinterpret_cast<const uint32_t *>(&h);
     lo = *reinterpret_cast<const uint32_t *>(&l);
 }
 
-// Byte offset of 16-byte slot `slot` of token `t` in a chunk tile.
-__device__ __forceinline__ uint32_t tile_off(int t, int slot)
-{
-    return (uint32_t)(t * kTileRow + ((slot ^ (t & 7)) << 4));
-}
-
 __device__ __forceinline__ float neg_inf() { return -__int_as_float(0x7F800000); }
 
-// Barrier of the HG warps that share a chunk.
-template <int HG>
-__device__ __forceinline__ void chunk_sync(int j)
+// Byte offset of the table word of code byte `i` of w for this lane:
+// (byte << 8) | (lane << 2) in one permute (lane4 = lane << 2).
+template <int I>
+__device__ __forceinline__ uint32_t lut_addr(uint32_t w, uint32_t lane4)
 {
-    if (HG == 1)
-        __syncwarp();
-    else
-        asm volatile("bar.sync %0, %1;" ::"r"(1 + j), "r"(HG * 32) : "memory");
+    return __byte_perm(w, lane4, 0x5504u | (I << 4));
 }
 
-// Codes of one chunk (32 token rows of 64 bytes per plane) -> fp16 levels in
-// the chunk tile. Unit u = (token u / 16, channels 8 (u % 16) .. + 7): one
-// 4-byte read per plane, four table lookups, one 16-byte store.
-template <bool FULL, int PT>
-__device__ __forceinline__ void decode_chunk(const uint8_t *pa, const uint8_t *pr, uint8_t *tile, int pt,
-                                             const uint32_t *lut_lane, const uint16_t *lut16_lane)
+template <int I>
+__device__ __forceinline__ uint32_t lut_anchor(const unsigned char *lut, uint32_t w, uint32_t lane4)
 {
-#pragma unroll 4
-    for (int u = pt; u < kChunk * 16; u += PT) {
-        const int t = u >> 4, c8 = u & 15;
-        const uint32_t aw = *reinterpret_cast<const uint32_t *>(pa + t * kRow + c8 * 4);
-        uint4 v;
-        if (FULL) {
-            const uint32_t rw = *reinterpret_cast<const uint32_t *>(pr + t * kRow + c8 * 4);
-            // byte i of ev / od: code (A << 4 | r) of channel 8 c8 + 2i / 2i + 1
-            const uint32_t ev = ((aw << 4) & 0xF0F0F0F0u) | (rw & 0x0F0F0F0Fu);
-            const uint32_t od = (aw & 0xF0F0F0F0u) | ((rw >> 4) & 0x0F0F0F0Fu);
-            uint32_t w[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const uint32_t le = lut16_lane[__byte_perm(ev, 0u, 0x4440u | i) * 32];
-                const uint32_t lo = lut16_lane[__byte_perm(od, 0u, 0x4440u | i) * 32];
-                w[i] = __byte_perm(le, lo, 0x5410u);
-            }
-            v = make_uint4(w[0], w[1], w[2], w[3]);
-        } else {
-            v = make_uint4(lut_lane[__byte_perm(aw, 0u, 0x4440u) * 32], lut_lane[__byte_perm(aw, 0u, 0x4441u) * 32],
-                           lut_lane[__byte_perm(aw, 0u, 0x4442u) * 32], lut_lane[__byte_perm(aw, 0u, 0x4443u) * 32]);
-        }
-        *reinterpret_cast<uint4 *>(tile + tile_off(t, c8)) = v;
-    }
+    return *reinterpret_cast<const uint32_t *>(lut + lut_addr<I>(w, lane4));
 }
 
-// Chunk affine (a, b) of channel pair c from one tensor's page metadata.
-__device__ __forceinline__ float4 chunk_affine(const float *pm, const uint16_t *cm, int j, int c)
+template <int I>
+__device__ __forceinline__ uint32_t lut_full(const unsigned char *lut, uint32_t w, uint32_t lane4)
 {
-    const int d = 2 * c;
-    const float2 mn = *reinterpret_cast<const float2 *>(pm + d);
-    const float2 rg = *reinterpret_cast<const float2 *>(pm + kD + d);
-    const float2 mu = __half22float2(*reinterpret_cast<const __half2 *>(cm + (j * 2) * kD + d));
-    const float2 sc = __half22float2(*reinterpret_cast<const __half2 *>(cm + (j * 2 + 1) * kD + d));
-    const float2 b = __fmul2_rn(rg, sc), a = __ffma2_rn(rg, mu, mn);
-    return make_float4(a.x, a.y, b.x, b.y);
+    return *reinterpret_cast<const uint32_t *>(lut + 128 + lut_addr<I>(w, lane4));
 }
 
-template <int HG, bool FULL, int NB>
-__global__ void __launch_bounds__(HG * 256, 1) attn_mma_kernel(AttnArgs a, LevelTable lev)
+// Low halves of x and y as one half2 (x's in the low half).
+__device__ __forceinline__ uint32_t pack_lo(uint32_t x, uint32_t y) { return __byte_perm(x, y, 0x5410u); }
+
+// Full-mode code bytes (A << 4 | r) of the even / odd channels of a word of
+// anchor nibbles aw and residual nibbles rw.
+__device__ __forceinline__ uint32_t codes_even(uint32_t aw, uint32_t rw)
 {
-    constexpr int NW = 8 * HG;
-    constexpr int NT = NW * 32;
-    constexpr int PT = HG * 32;             // threads per chunk
+    return ((aw << 4) & 0xF0F0F0F0u) | (rw & 0x0F0F0F0Fu);
+}
+__device__ __forceinline__ uint32_t codes_odd(uint32_t aw, uint32_t rw)
+{
+    return (aw & 0xF0F0F0F0u) | ((rw >> 4) & 0x0F0F0F0Fu);
+}
+
+// Byte i of the result holds nibble 2i of x (low) and nibble 2i of y (high),
+// resp. nibble 2i + 1: one channel of two tokens.
+__device__ __forceinline__ uint32_t nib_even(uint32_t x, uint32_t y)
+{
+    return (x & 0x0F0F0F0Fu) | ((y << 4) & 0xF0F0F0F0u);
+}
+__device__ __forceinline__ uint32_t nib_odd(uint32_t x, uint32_t y)
+{
+    return ((x >> 4) & 0x0F0F0F0Fu) | (y & 0xF0F0F0F0u);
+}
+
+// Chunk affines a = mn + rng mu and b = rng s of channels 4l .. 4l + 3 of one
+// tensor's page into the warp's buffers; returns max |b| of those channels.
+__device__ __forceinline__ float chunk_affines(const float *pm, const uint16_t *cm, int j, int lane, float *fa,
+                                               float *fb)
+{
+    const int d = 4 * lane;
+    const float4 mn = *reinterpret_cast<const float4 *>(pm + d);
+    const float4 rg = *reinterpret_cast<const float4 *>(pm + kD + d);
+    const uint2 mu2 = *reinterpret_cast<const uint2 *>(cm + (2 * j) * kD + d);
+    const uint2 sc2 = *reinterpret_cast<const uint2 *>(cm + (2 * j + 1) * kD + d);
+    const float2 mu01 = __half22float2(*reinterpret_cast<const __half2 *>(&mu2.x));
+    const float2 mu23 = __half22float2(*reinterpret_cast<const __half2 *>(&mu2.y));
+    const float2 s01 = __half22float2(*reinterpret_cast<const __half2 *>(&sc2.x));
+    const float2 s23 = __half22float2(*reinterpret_cast<const __half2 *>(&sc2.y));
+    const float2 a01 = __ffma2_rn(make_float2(rg.x, rg.y), mu01, make_float2(mn.x, mn.y));
+    const float2 a23 = __ffma2_rn(make_float2(rg.z, rg.w), mu23, make_float2(mn.z, mn.w));
+    const float2 b01 = __fmul2_rn(make_float2(rg.x, rg.y), s01);
+    const float2 b23 = __fmul2_rn(make_float2(rg.z, rg.w), s23);
+    const int p = d + 4 * (d >> 5);
+    *reinterpret_cast<float4 *>(fa + p) = make_float4(a01.x, a01.y, a23.x, a23.y);
+    *reinterpret_cast<float4 *>(fb + p) = make_float4(b01.x, b01.y, b23.x, b23.y);
+    return fmaxf(fmaxf(fabsf(b01.x), fabsf(b01.y)), fmaxf(fabsf(b23.x), fabsf(b23.y)));
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+template <bool G16, bool FULL, int NS>
+__global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(AttnArgs a, LevelTable lev)
+{
+    constexpr int R = G16 ? 2 : 1;          // query-head rows per lane: g (and g + 8)
     extern __shared__ __align__(128) unsigned char smem_raw[];
-    Smem<FULL, NB> &sm = *reinterpret_cast<Smem<FULL, NB> *>(smem_raw);
+    Smem<FULL, NS> &sm = *reinterpret_cast<Smem<FULL, NS> *>(smem_raw);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int n = lane >> 2, q = lane & 3;
-    const int j = warp & 7;                 // chunk of this warp
-    const int hg = warp >> 3;               // head group: query heads 8 hg .. 8 hg + 7 of the KV head's group
-    const int pt = hg * 32 + lane;          // index among the chunk's threads
-    const int hrow = hg * 8 + n;            // this lane's query head (MMA rows n and n + 8)
-    const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+    const int g = lane >> 2, q = lane & 3;
+    const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
     const int G = a.G;
     const int64_t T = (int64_t)a.pool_pages * kPage;
 
     // ---- per-CTA set-up ------------------------------------------------
-    if (FULL) {
-        uint16_t *lut16 = reinterpret_cast<uint16_t *>(sm.lut);
-        for (int i = tid; i < 256 * 32; i += NT)
-            lut16[i] = __half_as_ushort(__float2half_rn(lev.full[i >> 5]));
-    } else {
-        for (int i = tid; i < 256 * 32; i += NT) {
-            const int e = i >> 5;
+    for (int i = tid; i < 256 * 32; i += kThreads) {
+        const int e = i >> 5, l = i & 31;
+        uint32_t v;
+        if (FULL) {
+            v = (uint32_t)__half_as_ushort(__float2half_rn(lev.full[e]));
+        } else {
             const __half2 h = __floats2half2_rn(lev.anchor[e & 15], lev.anchor[e >> 4]);
-            sm.lut[i] = *reinterpret_cast<const uint32_t *>(&h);
+            v = *reinterpret_cast<const uint32_t *>(&h);
         }
+        sm.lut[e * 64 + (FULL ? 32 : 0) + l] = v;
     }
     const float qscale = a.sm_scale * kLog2e;
+    const int64_t qrow0 = (int64_t)b * a.Hq + (int64_t)kvh * G;
     float lq = 0.0f;
-    for (int i = tid; i < 16 * kD; i += NT) {
-        const int h = i / kD, d = i % kD;
+    for (int i = tid; i < 8 * 2 * 32 * 4; i += kThreads) {
+        // element c of qf[s][r][l]
+        const int c = i & 3, l = (i >> 2) & 31, r = (i >> 7) & 1, s = i >> 8;
+        const int row = (l >> 2) + 8 * r;
+        const int d = 32 * (l & 3) + 4 * s + c;
         float v = 0.0f;
-        if (h < G)
-            v = __uint_as_float((uint32_t)a.q[((int64_t)b * a.Hq + g * G + h) * kD + d] << 16) * qscale;
-        sm.qs[h][d] = v;
+        if (row < G && (G16 || r == 0))
+            v = __uint_as_float((uint32_t)a.q[(qrow0 + row) * kD + d] << 16) * qscale;
+        reinterpret_cast<float *>(&sm.qf[s][r][l])[c] = v;
         lq = fmaxf(lq, fabsf(v));
     }
     if (tid == 0) {
         sm.qmax = 0.0f;
-        for (int s = 0; s < NB; ++s) {
-            mbar_init(&sm.bar_k[s], 1);
-            mbar_init(&sm.bar_v[s], 1);
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(&sm.full_bar[s], 1);
+            mbar_init(&sm.empty_bar[s], kCons);
         }
         fence_mbar_init();
     }
     __syncthreads();
-    atomicMax(reinterpret_cast<int *>(&sm.qmax), __float_as_int(lq));
+    atomicMax(reinterpret_cast<int *>(&sm.qmax), __float_as_int(lq));   // non-negative floats order as ints
 
     int ctx = a.ctx[b];
     if (ctx < 0 || ctx > a.max_pages * kPage) {
-        if (a.dev_err && split == 0 && g == 0 && tid == 0)
+        if (a.dev_err && split == 0 && kvh == 0 && tid == 0)
             atomicOr(a.dev_err, LYNX_DEVERR_CTX);
         ctx = min(max(ctx, 0), a.max_pages * kPage);
     }
-    const uint8_t *ka = a.ka + (int64_t)g * T * kRow;
-    const uint8_t *va = a.va + (int64_t)g * T * kRow;
-    const uint8_t *kr = FULL ? a.kr + (int64_t)g * T * kRow : nullptr;
-    const uint8_t *vr = FULL ? a.vr + (int64_t)g * T * kRow : nullptr;
-    const float *kpm = a.kpm + (int64_t)g * a.pool_pages * (2 * kD);
-    const float *vpm = a.vpm + (int64_t)g * a.pool_pages * (2 * kD);
-    const uint16_t *kcm = a.kcm + (int64_t)g * a.pool_pages * (kNChunk * 2 * kD);
-    const uint16_t *vcm = a.vcm + (int64_t)g * a.pool_pages * (kNChunk * 2 * kD);
     const int64_t score_stride = (int64_t)a.max_pages * kPage;
-    const int64_t qrow0 = (int64_t)b * a.Hq + g * G;
-
     const int p_begin = split * a.pages_per_split;
     const int p_end = min(p_begin + a.pages_per_split, a.max_pages);
     const int p_live = min(p_end, (ctx + kPage - 1) / kPage);   // pages holding context
@@ -256,289 +247,423 @@ __global__ void __launch_bounds__(HG * 256, 1) attn_mma_kernel(AttnArgs a, Level
         const int p = a.page_table[(int64_t)b * a.max_pages + p_begin + i];
         return (p >= 0 && p < a.pool_pages) ? p : -1;
     };
-    // copies of page i into buffer s; `pend` (thread 0) marks buffers with a copy in flight
-    uint32_t pend = 0;
-    auto issue = [&](int i, int s, bool is_v) {
-        const int p = phys_of(i);
-        if (p < 0)
-            return;
-        Raw<FULL> &r = is_v ? sm.rv[s] : sm.rk[s];
-        uint64_t *bar = is_v ? &sm.bar_v[s] : &sm.bar_k[s];
-        const uint8_t *pa = is_v ? va : ka;
-        const uint8_t *pr = is_v ? vr : kr;
-        const float *pm = is_v ? vpm : kpm;
-        const uint16_t *cm = is_v ? vcm : kcm;
-        mbar_arrive_expect_tx(bar, (FULL ? 2u : 1u) * kPlane + 2 * kD * 4 + kNChunk * 2 * kD * 2);
-        bulk_g2s(r.a, pa + (int64_t)p * kPlane, kPlane, bar);
-        if (FULL)
-            bulk_g2s(r.r, pr + (int64_t)p * kPlane, kPlane, bar);
-        bulk_g2s(r.pm, pm + (int64_t)p * (2 * kD), 2 * kD * 4, bar);
-        bulk_g2s(r.cm, cm + (int64_t)p * (kNChunk * 2 * kD), kNChunk * 2 * kD * 2, bar);
-        pend |= 1u << (is_v ? NB + s : s);
-    };
-    if (tid == 0)
-        for (int i = 0; i < NB && i < np; ++i) {
-            issue(i, i, false);
-            issue(i, i, true);
-        }
 
     // pages of the range past the context: scores -inf
     if (a.scores) {
         for (int lp = max(p_live, p_begin); lp < p_end; ++lp)
-            for (int i = tid; i < G * kPage; i += NT)
+            for (int i = tid; i < G * kPage; i += kThreads)
                 a.scores[(qrow0 + i / kPage) * score_stride + (int64_t)lp * kPage + i % kPage] = neg_inf();
     }
+    __syncthreads();   // qmax complete
 
-    float m_run = neg_inf(), l_run = 0.0f;
-    float2 O[16];                           // head hrow, channels 8 nt + 2q, + 1
+    float m_run[R], l_run[R];                // per row: running max (base 2) and this lane's sum
+    float2 Olo[R][8], Ohi[R][8];             // per row: channels 32q + 2m, + 1 and 32q + 16 + 2m, + 1
 #pragma unroll
-    for (int nt = 0; nt < 16; ++nt)
-        O[nt] = make_float2(0.0f, 0.0f);
-    const uint32_t *lut_lane = sm.lut + lane;
-    const uint16_t *lut16_lane = reinterpret_cast<const uint16_t *>(sm.lut) + lane;
-    uint8_t *tile = reinterpret_cast<uint8_t *>(sm.dec[j]);
-    const uint32_t tile_s = smem_u32(tile);
-    // ldmatrix: this lane gives the address of row lane % 8 of matrix lane / 8
-    const int lm = lane >> 3, lr = lane & 7;
-
-    uint32_t phk[NB], phv[NB];
+    for (int r = 0; r < R; ++r) {
+        m_run[r] = neg_inf();
+        l_run[r] = 0.0f;
 #pragma unroll
-    for (int s = 0; s < NB; ++s)
-        phk[s] = phv[s] = 0u;
-    bool timed_out = false;
-    for (int i = 0; i < np; ++i) {
-        const int s = i % NB;
-        const int lp = p_begin + i;
-        const int nvalid = min(kPage, ctx - lp * kPage);
-        if (phys_of(i) < 0) {
-            if (a.dev_err && tid == 0)
-                atomicOr(a.dev_err, LYNX_DEVERR_PAGE);
-            if (a.scores)
-                for (int e = tid; e < G * kPage; e += NT)
-                    a.scores[(qrow0 + e / kPage) * score_stride + (int64_t)lp * kPage + e % kPage] = neg_inf();
-            __syncthreads();
-            if (tid == 0 && i + NB < np) {
-                issue(i + NB, s, false);
-                issue(i + NB, s, true);
-            }
-            continue;
-        }
-        const int nv = min(max(nvalid - j * kChunk, 0), kChunk);   // valid tokens of chunk j
+        for (int m = 0; m < 8; ++m)
+            Olo[r][m] = Ohi[r][m] = make_float2(0.0f, 0.0f);
+    }
 
-        // ---- K phase: decode chunk j's K, Q.K^T and softmax ----------------
-        bool ok = mbar_wait_bounded(&sm.bar_k[s], phk[s], kWaitLimit);
-        if (ok && nv > 0) {
-            const Raw<FULL> &rk = sm.rk[s];
-            float rmax = 0.0f;
-            for (int c = pt; c < kD / 2; c += PT) {
-                const float4 ab = chunk_affine(rk.pm, rk.cm, j, c);
-                sm.kab[j][c] = ab;
-                rmax = fmaxf(rmax, fmaxf(fabsf(ab.z), fabsf(ab.w)));
+    if (warp == kCons) {
+        // ---- producer: page i's K into item 2i, V into item 2i + 1 of the ring
+        if (lane == 0) {
+            int last[NS];
+            for (int s = 0; s < NS; ++s)
+                last[s] = -1;
+            bool ok = true;
+            for (int x = 0; x < 2 * np; ++x) {
+                const int s = x % NS;
+                if (x >= NS) {
+                    ok = mbar_wait_bounded(&sm.empty_bar[s], (uint32_t)((x / NS - 1) & 1), kWaitLimit);
+                    if (!ok)
+                        break;
+                    fence_proxy_async_smem();
+                }
+                const int t = x & 1;
+                const int p = phys_of(x >> 1);
+                Slot<FULL> &sl = sm.slot[s];
+                uint64_t *bar = &sm.full_bar[s];
+                last[s] = x;
+                if (p < 0) {
+                    mbar_arrive(bar);   // completes the phase with no data: consumers skip the page
+                    continue;
+                }
+                const int64_t off = (int64_t)kvh * T * kRow + (int64_t)p * kPlane;
+                const int64_t pmo = ((int64_t)kvh * a.pool_pages + p) * (2 * kD);
+                const int64_t cmo = ((int64_t)kvh * a.pool_pages + p) * (kNChunk * 2 * kD);
+                mbar_arrive_expect_tx(bar, (FULL ? 2u : 1u) * kPlane + 2 * kD * 4 + kNChunk * 2 * kD * 2);
+                bulk_g2s(sl.a, (t ? a.va : a.ka) + off, kPlane, bar);
+                if (FULL)
+                    bulk_g2s(sl.r, (t ? a.vr : a.kr) + off, kPlane, bar);
+                bulk_g2s(sl.pm, (t ? a.vpm : a.kpm) + pmo, 2 * kD * 4, bar);
+                bulk_g2s(sl.cm, (t ? a.vcm : a.kcm) + cmo, kNChunk * 2 * kD * 2, bar);
             }
+            // let every copy issued land before the CTA can end (bounded)
+            for (int s = 0; s < NS; ++s)
+                if (last[s] >= 0 && !mbar_wait_bounded(&sm.full_bar[s], (uint32_t)((last[s] / NS) & 1), kWaitLimit))
+                    ok = false;
+            if (!ok && a.dev_err)
+                atomicOr(a.dev_err, LYNX_DEVERR_TIMEOUT);
+        }
+    } else {
+        // ---- consumer warp j: chunk j of every page --------------------------
+        const int j = warp;
+        const uint32_t lane4 = (uint32_t)lane << 2;
+        const unsigned char *lut = reinterpret_cast<const unsigned char *>(sm.lut);
+        float *kaf = sm.aff[j][0][0], *kbf = sm.aff[j][0][1];
+        float *vaf = sm.aff[j][1][0], *vbf = sm.aff[j][1][1];
+        const float qmax = sm.qmax;
+        bool timed_out = false;
+
+        for (int i = 0; i < np; ++i) {
+            const int xk = 2 * i, sK = xk % NS, sV = (xk + 1) % NS;
+            const uint32_t parK = (uint32_t)((xk / NS) & 1), parV = (uint32_t)(((xk + 1) / NS) & 1);
+            const int lp = p_begin + i;
+            const bool valid = phys_of(i) >= 0;
+            const int nv = min(max(ctx - lp * kPage - j * kChunk, 0), kChunk);   // valid tokens of chunk j
+            if (!mbar_wait_bounded(&sm.full_bar[sK], parK, kWaitLimit)) {
+                timed_out = true;
+                break;
+            }
+            if (!valid || nv == 0) {
+                if (!valid && a.dev_err && j == 0 && lane == 0)
+                    atomicOr(a.dev_err, LYNX_DEVERR_PAGE);
+                if (a.scores)
+                    for (int e = lane; e < G * kChunk; e += 32)
+                        a.scores[(qrow0 + e / kChunk) * score_stride + (int64_t)lp * kPage + j * kChunk + e % kChunk] =
+                            neg_inf();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&sm.empty_bar[sK]);
+                if (!mbar_wait_bounded(&sm.full_bar[sV], parV, kWaitLimit)) {
+                    timed_out = true;
+                    break;
+                }
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&sm.empty_bar[sV]);
+                continue;
+            }
+
+            // ---- K: affines and codes of chunk j, then release the slot -------
+            float gscale, gdown;
+            uint4 kc[4], kr4[4];
+            {
+                const Slot<FULL> &sl = sm.slot[sK];
+                float bm = chunk_affines(sl.pm, sl.cm, j, lane, kaf, kbf);
+                const uint8_t *ca = sl.a + (j * kChunk + g) * kRow + 16 * q;
 #pragma unroll
-            for (int o = 16; o >= 1; o >>= 1)
-                rmax = fmaxf(rmax, __shfl_xor_sync(0xFFFFFFFFu, rmax, o));
-            if (lane == 0)
-                sm.rmaxw[warp] = rmax;
-            decode_chunk<FULL, PT>(rk.a + j * kChunk * kRow, FULL ? rk.r + j * kChunk * kRow : nullptr, tile, pt,
-                                   lut_lane, lut16_lane);
-        }
-        if (__syncthreads_or(!ok)) {
-            timed_out = true;
-            break;
-        }
-        phk[s] ^= 1u;
-        if (tid == 0) {
-            pend &= ~(1u << s);
-            if (i + NB < np) {
-                fence_proxy_async_smem();
-                issue(i + NB, s, false);
+                for (int nt = 0; nt < 4; ++nt)
+                    kc[nt] = *reinterpret_cast<const uint4 *>(ca + nt * 8 * kRow);
+                if (FULL) {
+                    const uint8_t *cr = sl.r + (j * kChunk + g) * kRow + 16 * q;
+#pragma unroll
+                    for (int nt = 0; nt < 4; ++nt)
+                        kr4[nt] = *reinterpret_cast<const uint4 *>(cr + nt * 8 * kRow);
+                }
+#pragma unroll
+                for (int o = 16; o >= 1; o >>= 1)
+                    bm = fmaxf(bm, __shfl_xor_sync(0xFFFFFFFFu, bm, o));
+                // q b must stay a finite fp16 pair: past 2^14 it is scaled by
+                // 2^-e and the scores back by 2^e
+                int ge = 0;
+                if (bm * qmax >= 16384.0f) {
+                    frexpf(bm * qmax, &ge);
+                    ge -= 14;
+                }
+                gdown = exp2f((float)-ge);
+                gscale = exp2f((float)ge);
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&sm.empty_bar[sK]);
             }
-        }
 
-        uint32_t Phi[2][4];
-        float psum = 0.0f;
-        if (nv > 0) {
-            // q b must stay a finite fp16 pair: if qmax * max|b| reaches 2^14 in
-            // this chunk, q b is scaled by 2^-e and the scores back by 2^e
-            float rm = sm.rmaxw[j];
-            if (HG == 2)
-                rm = fmaxf(rm, sm.rmaxw[j + 8]);
-            int ge = 0;
-            if (rm * sm.qmax >= 16384.0f) {
-                frexpf(rm * sm.qmax, &ge);
-                ge -= 14;
-            }
-            const float gdown = exp2f((float)-ge), gscale = exp2f((float)ge);
-
-            // Q.K^T: rows = 8 heads' hi parts over their lo parts
+            // ---- Q.K^T ------------------------------------------------------------
             float S[4][4];
 #pragma unroll
             for (int nt = 0; nt < 4; ++nt)
                 S[nt][0] = S[nt][1] = S[nt][2] = S[nt][3] = 0.0f;
-            float2 beta2 = make_float2(0.0f, 0.0f);
+            float2 beta2[R];
 #pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-                const int c0 = ks * 16 + 2 * q;
-                const float4 k01 = sm.kab[j][c0 >> 1];          // channels c0, c0 + 1
-                const float4 k89 = sm.kab[j][(c0 >> 1) + 4];    // channels c0 + 8, c0 + 9
-                const float2 q01 = *reinterpret_cast<const float2 *>(&sm.qs[hrow][c0]);
-                const float2 q89 = *reinterpret_cast<const float2 *>(&sm.qs[hrow][c0 + 8]);
-                beta2 = __ffma2_rn(q01, make_float2(k01.x, k01.y), beta2);
-                beta2 = __ffma2_rn(q89, make_float2(k89.x, k89.y), beta2);
-                float2 x0 = __fmul2_rn(q01, make_float2(k01.z, k01.w));
-                float2 x1 = __fmul2_rn(q89, make_float2(k89.z, k89.w));
-                if (ge) {
-                    x0 = __fmul2_rn(x0, make_float2(gdown, gdown));
-                    x1 = __fmul2_rn(x1, make_float2(gdown, gdown));
+            for (int r = 0; r < R; ++r)
+                beta2[r] = make_float2(0.0f, 0.0f);
+#pragma unroll
+            for (int s = 0; s < 8; ++s) {
+                const int cp = 36 * q + 4 * s;   // channels 32q + 4s .. + 3 (padded index)
+                const float4 bb = *reinterpret_cast<const float4 *>(kbf + cp);
+                const float4 aa = *reinterpret_cast<const float4 *>(kaf + cp);
+                uint32_t A0[4], A1[4];           // G16: hi and lo fragments; else A0 = hi rows over lo rows
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    const float4 qv = sm.qf[s][r][lane];
+                    beta2[r] = __ffma2_rn(make_float2(qv.x, qv.y), make_float2(aa.x, aa.y), beta2[r]);
+                    beta2[r] = __ffma2_rn(make_float2(qv.z, qv.w), make_float2(aa.z, aa.w), beta2[r]);
+                    float2 x01 = __fmul2_rn(make_float2(qv.x, qv.y), make_float2(bb.x, bb.y));
+                    float2 x23 = __fmul2_rn(make_float2(qv.z, qv.w), make_float2(bb.z, bb.w));
+                    x01 = __fmul2_rn(x01, make_float2(gdown, gdown));
+                    x23 = __fmul2_rn(x23, make_float2(gdown, gdown));
+                    if (G16) {
+                        split2(x01, A0[r], A1[r]);
+                        split2(x23, A0[2 + r], A1[2 + r]);
+                    } else {
+                        split2(x01, A0[0], A0[1]);
+                        split2(x23, A0[2], A0[3]);
+                    }
                 }
-                uint32_t A[4];
-                split2(x0, A[0], A[1]);
-                split2(x1, A[2], A[3]);
+                const int wi = s >> 1;
 #pragma unroll
-                for (int p = 0; p < 2; ++p) {
-                    // n-tiles 2p, 2p + 1: matrices (n-tile 2p + m / 2, slot 2ks + m % 2)
-                    uint32_t bb[4];
-                    const int t = 8 * (2 * p + (lm >> 1)) + lr;
-                    ldsm_x4(tile_s + tile_off(t, 2 * ks + (lm & 1)), bb);
-                    mma16816(S[2 * p], A, bb[0], bb[1]);
-                    mma16816(S[2 * p + 1], A, bb[2], bb[3]);
+                for (int nt = 0; nt < 4; ++nt) {
+                    const uint32_t aw = wi == 0 ? kc[nt].x : wi == 1 ? kc[nt].y : wi == 2 ? kc[nt].z : kc[nt].w;
+                    uint32_t b0, b1;
+                    if (FULL) {
+                        const uint32_t rw = wi == 0 ? kr4[nt].x : wi == 1 ? kr4[nt].y : wi == 2 ? kr4[nt].z : kr4[nt].w;
+                        const uint32_t ev = codes_even(aw, rw), od = codes_odd(aw, rw);
+                        if (s & 1) {
+                            b0 = pack_lo(lut_full<2>(lut, ev, lane4), lut_full<2>(lut, od, lane4));
+                            b1 = pack_lo(lut_full<3>(lut, ev, lane4), lut_full<3>(lut, od, lane4));
+                        } else {
+                            b0 = pack_lo(lut_full<0>(lut, ev, lane4), lut_full<0>(lut, od, lane4));
+                            b1 = pack_lo(lut_full<1>(lut, ev, lane4), lut_full<1>(lut, od, lane4));
+                        }
+                    } else {
+                        if (s & 1) {
+                            b0 = lut_anchor<2>(lut, aw, lane4);
+                            b1 = lut_anchor<3>(lut, aw, lane4);
+                        } else {
+                            b0 = lut_anchor<0>(lut, aw, lane4);
+                            b1 = lut_anchor<1>(lut, aw, lane4);
+                        }
+                    }
+                    mma16816(S[nt], A0, b0, b1);
+                    if (G16)
+                        mma16816(S[nt], A1, b0, b1);
                 }
             }
-            float beta = beta2.x + beta2.y;
-            beta += __shfl_xor_sync(0xFFFFFFFFu, beta, 1);
-            beta += __shfl_xor_sync(0xFFFFFFFFu, beta, 2);
 
-            // scores of head hrow (base-2 log domain), masking, online softmax
-            float P[4][2];
-            float mx = neg_inf();
+            // ---- scores (base-2 log domain), masking, online softmax ---------------
+            float beta[R];
 #pragma unroll
-            for (int nt = 0; nt < 4; ++nt)
+            for (int r = 0; r < R; ++r) {
+                float bt = beta2[r].x + beta2[r].y;
+                bt += __shfl_xor_sync(0xFFFFFFFFu, bt, 1);
+                bt += __shfl_xor_sync(0xFFFFFFFFu, bt, 2);
+                beta[r] = bt;
+            }
+            float P[R][4][2];                    // row r, n-tile nt: tokens 8 nt + 2q, + 1
+            float psum[R];
+            bool rescale = false;
+            float alpha[R];
 #pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int tt = nt * 8 + 2 * q + e;
-                    const float v = tt < nv ? fmaf(S[nt][e] + S[nt][e + 2], gscale, beta) : neg_inf();
-                    P[nt][e] = v;
-                    mx = fmaxf(mx, v);
-                }
-            if (a.scores && hrow < G) {
-                float *srow = a.scores + (qrow0 + hrow) * score_stride + (int64_t)lp * kPage + j * kChunk;
+            for (int r = 0; r < R; ++r) {
+                float mx = neg_inf();
 #pragma unroll
                 for (int nt = 0; nt < 4; ++nt)
-                    *reinterpret_cast<float2 *>(srow + nt * 8 + 2 * q) = make_float2(P[nt][0] * kLn2, P[nt][1] * kLn2);
-            }
-            mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
-            mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));
-            const float m_new = fmaxf(m_run, mx);
-            const float alpha = exp2f(m_run - m_new);
-            m_run = m_new;
 #pragma unroll
-            for (int nt = 0; nt < 4; ++nt)
+                    for (int e = 0; e < 2; ++e) {
+                        const float acc = G16 ? S[nt][2 * r + e] : S[nt][e] + S[nt][2 + e];
+                        float v = fmaf(acc, gscale, beta[r]);
+                        if (nv < kChunk && 8 * nt + 2 * q + e >= nv)
+                            v = neg_inf();
+                        P[r][nt][e] = v;
+                        mx = fmaxf(mx, v);
+                    }
+                const int h = g + 8 * r;
+                if (a.scores && h < G) {
+                    float *srow = a.scores + (qrow0 + h) * score_stride + (int64_t)lp * kPage + j * kChunk;
 #pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const float pv = exp2f(P[nt][e] - m_new);
-                    P[nt][e] = pv;
-                    psum += pv;
+                    for (int nt = 0; nt < 4; ++nt)
+                        *reinterpret_cast<float2 *>(srow + nt * 8 + 2 * q) =
+                            make_float2(P[r][nt][0] * kLn2, P[r][nt][1] * kLn2);
                 }
-            l_run = fmaf(l_run, alpha, psum);
-            psum += __shfl_xor_sync(0xFFFFFFFFu, psum, 1);
-            psum += __shfl_xor_sync(0xFFFFFFFFu, psum, 2);
-            if (alpha != 1.0f) {
-                const float2 al = make_float2(alpha, alpha);
+                mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
+                mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));
+                const float m_new = fmaxf(m_run[r], mx);
+                alpha[r] = exp2f(m_run[r] - m_new);
+                rescale |= alpha[r] != 1.0f;
+                m_run[r] = m_new;
+                float ps = 0.0f;
 #pragma unroll
-                for (int nt = 0; nt < 16; ++nt)
-                    O[nt] = __fmul2_rn(O[nt], al);
-            }
-            // P as A fragments: k = tokens of n-tiles 2ks, 2ks + 1; rows hi over lo
+                for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
-            for (int ks = 0; ks < 2; ++ks) {
-                split2(make_float2(P[2 * ks][0], P[2 * ks][1]), Phi[ks][0], Phi[ks][1]);
-                split2(make_float2(P[2 * ks + 1][0], P[2 * ks + 1][1]), Phi[ks][2], Phi[ks][3]);
+                    for (int e = 0; e < 2; ++e) {
+                        const float pv = exp2f(P[r][nt][e] - m_new);
+                        P[r][nt][e] = pv;
+                        ps += pv;
+                    }
+                l_run[r] = fmaf(l_run[r], alpha[r], ps);
+                ps += __shfl_xor_sync(0xFFFFFFFFu, ps, 1);
+                ps += __shfl_xor_sync(0xFFFFFFFFu, ps, 2);
+                psum[r] = ps;
             }
-        } else if (a.scores && hrow < G) {
-            for (int e = q; e < kChunk; e += 4)
-                a.scores[(qrow0 + hrow) * score_stride + (int64_t)lp * kPage + j * kChunk + e] = neg_inf();
-        }
-        chunk_sync<HG>(j);   // the chunk's warps are done with its K tile
+            if (__any_sync(0xFFFFFFFFu, rescale)) {
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    const float2 al = make_float2(alpha[r], alpha[r]);
+#pragma unroll
+                    for (int m = 0; m < 8; ++m) {
+                        Olo[r][m] = __fmul2_rn(Olo[r][m], al);
+                        Ohi[r][m] = __fmul2_rn(Ohi[r][m], al);
+                    }
+                }
+            }
+            // P as A fragments; k-step kk = tokens 16 kk .. 16 kk + 15
+            uint32_t PA0[2][4], PA1[2][4];       // G16: hi, lo; else PA0 = hi rows over lo rows
+#pragma unroll
+            for (int kk = 0; kk < 2; ++kk) {
+                if (G16) {
+#pragma unroll
+                    for (int r = 0; r < R; ++r) {
+                        split2(make_float2(P[r][2 * kk][0], P[r][2 * kk][1]), PA0[kk][r], PA1[kk][r]);
+                        split2(make_float2(P[r][2 * kk + 1][0], P[r][2 * kk + 1][1]), PA0[kk][2 + r], PA1[kk][2 + r]);
+                    }
+                } else {
+                    split2(make_float2(P[0][2 * kk][0], P[0][2 * kk][1]), PA0[kk][0], PA0[kk][1]);
+                    split2(make_float2(P[0][2 * kk + 1][0], P[0][2 * kk + 1][1]), PA0[kk][2], PA0[kk][3]);
+                }
+            }
 
-        // ---- V phase: decode chunk j's V, P.V --------------------------------
-        ok = mbar_wait_bounded(&sm.bar_v[s], phv[s], kWaitLimit);
-        if (ok && nv > 0) {
-            const Raw<FULL> &rv = sm.rv[s];
-            for (int c = pt; c < kD / 2; c += PT)
-                sm.vab[j][c] = chunk_affine(rv.pm, rv.cm, j, c);
-            decode_chunk<FULL, PT>(rv.a + j * kChunk * kRow, FULL ? rv.r + j * kChunk * kRow : nullptr, tile, pt,
-                                   lut_lane, lut16_lane);
-        }
-        if (__syncthreads_or(!ok)) {
-            timed_out = true;
-            break;
-        }
-        phv[s] ^= 1u;
-        if (tid == 0) {
-            pend &= ~(1u << (NB + s));
-            if (i + NB < np) {
-                fence_proxy_async_smem();
-                issue(i + NB, s, true);
+            // ---- V: affines and codes of chunk j, then release the slot -------
+            if (!mbar_wait_bounded(&sm.full_bar[sV], parV, kWaitLimit)) {
+                timed_out = true;
+                break;
             }
-        }
-        if (nv > 0) {
-            const float2 ps2 = make_float2(psum, psum);
+            uint2 vc[2][4], vr4[2][4];           // [k-step][tokens 2q, 2q + 1, 2q + 8, 2q + 9], bytes 8g .. 8g + 7
+            {
+                const Slot<FULL> &sl = sm.slot[sV];
+                chunk_affines(sl.pm, sl.cm, j, lane, vaf, vbf);
+                const uint8_t *ca = sl.a + (j * kChunk + 2 * q) * kRow + 8 * g;
 #pragma unroll
-            for (int p = 0; p < 8; ++p) {
-                // n-tiles 2p, 2p + 1 (channels 16p ..); k-steps = tokens 0..15, 16..31:
-                // matrices (tokens 16 ks + 8 (m % 2) .., slot 2p + m / 2), transposed
-                float accA[4] = {0.0f, 0.0f, 0.0f, 0.0f}, accB[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                for (int kk = 0; kk < 2; ++kk)
 #pragma unroll
-                for (int ks = 0; ks < 2; ++ks) {
-                    uint32_t bb[4];
-                    const int t = 16 * ks + 8 * (lm & 1) + lr;
-                    ldsm_x4_trans(tile_s + tile_off(t, 2 * p + (lm >> 1)), bb);
-                    mma16816(accA, Phi[ks], bb[0], bb[1]);
-                    mma16816(accB, Phi[ks], bb[2], bb[3]);
+                    for (int u = 0; u < 4; ++u)
+                        vc[kk][u] = *reinterpret_cast<const uint2 *>(ca + (16 * kk + (u & 1) + 8 * (u >> 1)) * kRow);
+                if (FULL) {
+                    const uint8_t *cr = sl.r + (j * kChunk + 2 * q) * kRow + 8 * g;
+#pragma unroll
+                    for (int kk = 0; kk < 2; ++kk)
+#pragma unroll
+                        for (int u = 0; u < 4; ++u)
+                            vr4[kk][u] = *reinterpret_cast<const uint2 *>(cr + (16 * kk + (u & 1) + 8 * (u >> 1)) * kRow);
                 }
-                // o += b (P.L) + a sum(P), channels 8 nt + 2q, + 1
-                const float4 vA = sm.vab[j][(2 * p) * 4 + q];
-                const float4 vB = sm.vab[j][(2 * p + 1) * 4 + q];
-                O[2 * p] = __ffma2_rn(make_float2(vA.z, vA.w), make_float2(accA[0] + accA[2], accA[1] + accA[3]),
-                                      __ffma2_rn(ps2, make_float2(vA.x, vA.y), O[2 * p]));
-                O[2 * p + 1] = __ffma2_rn(make_float2(vB.z, vB.w), make_float2(accB[0] + accB[2], accB[1] + accB[3]),
-                                          __ffma2_rn(ps2, make_float2(vB.x, vB.y), O[2 * p + 1]));
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&sm.empty_bar[sV]);
+            }
+
+            // ---- P.V: n-tile 2m + e holds channel 16 n + 2m + e of column n ------
+#pragma unroll
+            for (int m = 0; m < 8; ++m) {
+                const int wi = m >> 2;
+                float C[2][4];
+#pragma unroll
+                for (int e = 0; e < 2; ++e)
+                    C[e][0] = C[e][1] = C[e][2] = C[e][3] = 0.0f;
+#pragma unroll
+                for (int kk = 0; kk < 2; ++kk) {
+                    uint32_t bl0, bl1, bo0, bo1;   // (b0, b1) of n-tiles 2m and 2m + 1
+                    const uint32_t x0 = wi ? vc[kk][0].y : vc[kk][0].x, x1 = wi ? vc[kk][1].y : vc[kk][1].x;
+                    const uint32_t x2 = wi ? vc[kk][2].y : vc[kk][2].x, x3 = wi ? vc[kk][3].y : vc[kk][3].x;
+                    if (FULL) {
+                        const uint32_t r0 = wi ? vr4[kk][0].y : vr4[kk][0].x, r1 = wi ? vr4[kk][1].y : vr4[kk][1].x;
+                        const uint32_t r2 = wi ? vr4[kk][2].y : vr4[kk][2].x, r3 = wi ? vr4[kk][3].y : vr4[kk][3].x;
+                        const uint32_t e0 = codes_even(x0, r0), e1 = codes_even(x1, r1);
+                        const uint32_t e2 = codes_even(x2, r2), e3 = codes_even(x3, r3);
+                        const uint32_t o0 = codes_odd(x0, r0), o1 = codes_odd(x1, r1);
+                        const uint32_t o2 = codes_odd(x2, r2), o3 = codes_odd(x3, r3);
+                        switch (m & 3) {
+#define LYNX_V_FULL(I)                                                                                                 \
+    case I:                                                                                                            \
+        bl0 = pack_lo(lut_full<I>(lut, e0, lane4), lut_full<I>(lut, e1, lane4));                                      \
+        bl1 = pack_lo(lut_full<I>(lut, e2, lane4), lut_full<I>(lut, e3, lane4));                                      \
+        bo0 = pack_lo(lut_full<I>(lut, o0, lane4), lut_full<I>(lut, o1, lane4));                                      \
+        bo1 = pack_lo(lut_full<I>(lut, o2, lane4), lut_full<I>(lut, o3, lane4));                                      \
+        break;
+                            LYNX_V_FULL(0)
+                            LYNX_V_FULL(1)
+                            LYNX_V_FULL(2)
+                            default:
+                            LYNX_V_FULL(3)
+#undef LYNX_V_FULL
+                        }
+                    } else {
+                        const uint32_t e01 = nib_even(x0, x1), e23 = nib_even(x2, x3);
+                        const uint32_t o01 = nib_odd(x0, x1), o23 = nib_odd(x2, x3);
+                        switch (m & 3) {
+#define LYNX_V_ANCHOR(I)                                                                                               \
+    case I:                                                                                                            \
+        bl0 = lut_anchor<I>(lut, e01, lane4);                                                                          \
+        bl1 = lut_anchor<I>(lut, e23, lane4);                                                                          \
+        bo0 = lut_anchor<I>(lut, o01, lane4);                                                                          \
+        bo1 = lut_anchor<I>(lut, o23, lane4);                                                                          \
+        break;
+                            LYNX_V_ANCHOR(0)
+                            LYNX_V_ANCHOR(1)
+                            LYNX_V_ANCHOR(2)
+                            default:
+                            LYNX_V_ANCHOR(3)
+#undef LYNX_V_ANCHOR
+                        }
+                    }
+                    mma16816(C[0], PA0[kk], bl0, bl1);
+                    mma16816(C[1], PA0[kk], bo0, bo1);
+                    if (G16) {
+                        mma16816(C[0], PA1[kk], bl0, bl1);
+                        mma16816(C[1], PA1[kk], bo0, bo1);
+                    }
+                }
+                // o += b (P.L) + a sum(P): column 2q -> channels 32q + 2m, + 1;
+                // column 2q + 1 -> channels 32q + 16 + 2m, + 1
+                const float2 bl = *reinterpret_cast<const float2 *>(vbf + 36 * q + 2 * m);
+                const float2 bh = *reinterpret_cast<const float2 *>(vbf + 36 * q + 16 + 2 * m);
+                const float2 al = *reinterpret_cast<const float2 *>(vaf + 36 * q + 2 * m);
+                const float2 ah = *reinterpret_cast<const float2 *>(vaf + 36 * q + 16 + 2 * m);
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    float2 cl, ch;
+                    if (G16) {
+                        cl = make_float2(C[0][2 * r], C[1][2 * r]);
+                        ch = make_float2(C[0][2 * r + 1], C[1][2 * r + 1]);
+                    } else {
+                        cl = make_float2(C[0][0] + C[0][2], C[1][0] + C[1][2]);
+                        ch = make_float2(C[0][1] + C[0][3], C[1][1] + C[1][3]);
+                    }
+                    const float2 ps2 = make_float2(psum[r], psum[r]);
+                    Olo[r][m] = __ffma2_rn(bl, cl, __ffma2_rn(al, ps2, Olo[r][m]));
+                    Ohi[r][m] = __ffma2_rn(bh, ch, __ffma2_rn(ah, ps2, Ohi[r][m]));
+                }
             }
         }
-        chunk_sync<HG>(j);   // the chunk's warps are done with its V tile
-    }
-    if (timed_out) {
-        // a copy never completed: let the ones in flight land (bounded), then stop
-        if (tid == 0) {
-            for (int s = 0; s < NB; ++s) {
-                if (pend & (1u << s))
-                    mbar_wait_bounded(&sm.bar_k[s], phk[s], kWaitLimit);
-                if (pend & (1u << (NB + s)))
-                    mbar_wait_bounded(&sm.bar_v[s], phv[s], kWaitLimit);
-            }
-            if (a.dev_err)
-                atomicOr(a.dev_err, LYNX_DEVERR_TIMEOUT);
-        }
+        if (timed_out && a.dev_err && lane == 0)
+            atomicOr(a.dev_err, LYNX_DEVERR_TIMEOUT);
     }
 
     // ---- merge the chunks' states, write this range's partial ------------
-    __syncthreads();
+    __syncthreads();   // every table and query read is done; the merge area overlays them
     Merge &mg = *reinterpret_cast<Merge *>(smem_raw);
-    {
-        float l = l_run;
-        l += __shfl_xor_sync(0xFFFFFFFFu, l, 1);
-        l += __shfl_xor_sync(0xFFFFFFFFu, l, 2);
-        if (q == 0) {
-            mg.m[j][hrow] = m_run;
-            mg.l[j][hrow] = l;
+    if (warp < kCons) {
+        const int j = warp;
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const int h = g + 8 * r;
+            float l = l_run[r];
+            l += __shfl_xor_sync(0xFFFFFFFFu, l, 1);
+            l += __shfl_xor_sync(0xFFFFFFFFu, l, 2);
+            if (q == 0) {
+                mg.m[j][h] = m_run[r];
+                mg.l[j][h] = l;
+            }
+#pragma unroll
+            for (int m = 0; m < 8; ++m) {
+                *reinterpret_cast<float2 *>(&mg.o[j][h][32 * q + 2 * m]) = Olo[r][m];
+                *reinterpret_cast<float2 *>(&mg.o[j][h][32 * q + 16 + 2 * m]) = Ohi[r][m];
+            }
         }
     }
-#pragma unroll
-    for (int nt = 0; nt < 16; ++nt)
-        *reinterpret_cast<float2 *>(&mg.o[j][hrow][nt * 8 + 2 * q]) = O[nt];
     __syncthreads();
-    for (int e = tid; e < G * kD; e += NT) {
+    for (int e = tid; e < G * kD; e += kThreads) {
         const int h = e / kD, d = e % kD;
         float M = neg_inf();
 #pragma unroll
@@ -562,18 +687,19 @@ __global__ void __launch_bounds__(HG * 256, 1) attn_mma_kernel(AttnArgs a, Level
     }
 }
 
-template <int HG, bool FULL, int NB>
+template <bool G16, bool FULL, int NS>
 cudaError_t run(const AttnArgs &a, cudaStream_t s)
 {
-    static_assert(sizeof(Merge) <= sizeof(Raw<FULL>) * 2 * NB, "merge area overlays the raw buffers");
-    static_assert(sizeof(Smem<FULL, NB>) <= 227 * 1024, "shared memory per CTA");
-    const size_t smem = sizeof(Smem<FULL, NB>);
-    cudaError_t e = cudaFuncSetAttribute(attn_mma_kernel<HG, FULL, NB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    static_assert(sizeof(Merge) <= sizeof(uint32_t) * 256 * 64 + sizeof(float4) * 8 * 2 * 32,
+                  "merge area overlays the table and the queries");
+    static_assert(sizeof(Smem<FULL, NS>) <= 227 * 1024, "shared memory per CTA");
+    const size_t smem = sizeof(Smem<FULL, NS>);
+    cudaError_t e = cudaFuncSetAttribute(attn_mma_kernel<G16, FULL, NS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess)
         return e;
     dim3 grid((unsigned)a.n_splits, (unsigned)a.H, (unsigned)a.B);
-    attn_mma_kernel<HG, FULL, NB><<<grid, HG * 256, smem, s>>>(a, host_tables().lev);
+    attn_mma_kernel<G16, FULL, NS><<<grid, kThreads, smem, s>>>(a, host_tables().lev);
     return cudaGetLastError();
 }
 
@@ -581,10 +707,10 @@ cudaError_t run(const AttnArgs &a, cudaStream_t s)
 
 cudaError_t launch_attn_mma(const AttnArgs &a, cudaStream_t s)
 {
-    // anchor pages are small enough for two buffers per tensor; full pages get one
+    // slots hold one tensor's page: 21 KiB in anchor mode, 37 KiB in full mode
     if (a.G <= 8)
-        return a.full ? run<1, true, 1>(a, s) : run<1, false, 2>(a, s);
-    return a.full ? run<2, true, 1>(a, s) : run<2, false, 2>(a, s);
+        return a.full ? run<false, true, 3>(a, s) : run<false, false, 6>(a, s);
+    return a.full ? run<true, true, 3>(a, s) : run<true, false, 6>(a, s);
 }
 
 } // namespace lynx
