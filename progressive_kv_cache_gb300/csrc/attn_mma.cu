@@ -29,11 +29,12 @@
 // memory. The lookup table is replicated per lane (conflict-free) with entries
 // 256 bytes apart, so that one byte permute forms the whole address.
 //
-// Work: a CTA per (page range, KV head, request): one producer warp streams
-// the pages' K and V planes and metadata by bulk copy into a ring of slots
-// (one tensor's page per slot); consumer warp j owns chunk j of every page and
-// all query heads of the group: with up to 8 heads the MMA rows are the heads'
-// hi parts over their lo parts; with up to 16 the rows are the heads and hi and
+// Work: a CTA per (page range, KV head, request) of 12 warps. The pages' K
+// and V planes and metadata arrive by bulk copy in a ring of slots (one
+// tensor's page per slot); the warp that releases the last chunk of a slot
+// refills it. Warp w takes chunks w, w + 12, ... of the range, each for all
+// query heads of the group: with up to 8 heads the MMA rows are the heads' hi
+// parts over their lo parts; with up to 16 the rows are the heads and hi and
 // lo go through two MMAs into the same accumulators. The chunks' running (max,
 // sum, output) are merged in shared memory into one partial per query head; a
 // second kernel merges the partials of the ranges.
@@ -48,8 +49,8 @@ namespace {
 constexpr uint32_t kPlane = kPage * kD / 2;   // 16 KiB: one page of one plane
 constexpr int kRow = kD / 2;                  // code bytes per token
 constexpr int kPart = kD + 2;
-constexpr int kCons = kNChunk;                // consumer warps, one per chunk
-constexpr int kThreads = (kCons + 1) * 32;    // + one producer warp
+constexpr int kWarps = 12;                    // three per scheduler
+constexpr int kThreads = kWarps * 32;
 constexpr int kAff = kD + 16;                 // channel c stored at c + 4 (c / 32): no bank conflicts
 constexpr uint32_t kWaitLimit = 1u << 22;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -75,16 +76,17 @@ struct Smem {
     float4 qf[8][2][32];
     Slot<FULL> slot[NS];
     // per consumer warp and tensor (K, V): chunk affines a and b
-    float aff[kCons][2][2][kAff];
+    float aff[kWarps][2][2][kAff];
     float qmax;
+    int rel[NS];                              // releases of the slot's current item
+    int last[NS];                             // last item issued into each slot (its tag)
     alignas(8) uint64_t full_bar[NS];
-    uint64_t empty_bar[NS];
 };
 
-struct Merge {                                // overlays the table and queries after the page loop
-    float m[kNChunk][16];                     // per chunk and query head
-    float l[kNChunk][16];
-    float o[kNChunk][16][kD];
+struct Merge {                                // overlays the slots after the page loop
+    float m[kWarps][16];                      // per warp and query head
+    float l[kWarps][16];
+    float o[kWarps][16][kD];
 };
 
 __device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
@@ -93,6 +95,15 @@ __device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], 
                  "{%0,%1,%2,%3};"
                  : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
                  : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// The same with a zero accumulator in.
+__device__ __forceinline__ void mma16816_z(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
+{
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+                 "{%10,%10,%10,%10};"
+                 : "=f"(c[0]), "=f"(c[1]), "=f"(c[2]), "=f"(c[3])
+                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(0.0f));
 }
 
 // (x0, x1) -> fp16 pairs hi and lo with hi + lo = (x0, x1) to ~22 bits.
@@ -106,6 +117,15 @@ __device__ __forceinline__ void split2(float2 x, uint32_t &hi, uint32_t &lo)
 }
 
 __device__ __forceinline__ float neg_inf() { return -__int_as_float(0x7F800000); }
+
+// 2^x for the softmax weights (x <= 0): the hardware approximation, results
+// below 2^-126 flushed to zero.
+__device__ __forceinline__ float exp2_sm(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 
 // Byte offset of the table word of code byte `i` of w for this lane:
 // (byte << 8) | (lane << 2) in one permute (lane4 = lane << 2).
@@ -176,6 +196,7 @@ __device__ __forceinline__ float chunk_affines(const float *pm, const uint16_t *
     return fmaxf(fmaxf(fabsf(b01.x), fabsf(b01.y)), fmaxf(fabsf(b23.x), fabsf(b23.y)));
 }
 
+
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar)
 {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
@@ -223,7 +244,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(AttnArgs a, Level
         sm.qmax = 0.0f;
         for (int s = 0; s < NS; ++s) {
             mbar_init(&sm.full_bar[s], 1);
-            mbar_init(&sm.empty_bar[s], kCons);
+            sm.rel[s] = 0;
+            sm.last[s] = -1;
         }
         fence_mbar_init();
     }
@@ -267,383 +289,416 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(AttnArgs a, Level
             Olo[r][m] = Ohi[r][m] = make_float2(0.0f, 0.0f);
     }
 
-    if (warp == kCons) {
-        // ---- producer: page i's K into item 2i, V into item 2i + 1 of the ring
-        if (lane == 0) {
-            int last[NS];
-            for (int s = 0; s < NS; ++s)
-                last[s] = -1;
-            bool ok = true;
-            for (int x = 0; x < 2 * np; ++x) {
-                const int s = x % NS;
-                if (x >= NS) {
-                    ok = mbar_wait_bounded(&sm.empty_bar[s], (uint32_t)((x / NS - 1) & 1), kWaitLimit);
-                    if (!ok)
-                        break;
-                    fence_proxy_async_smem();
-                }
-                const int t = x & 1;
-                const int p = phys_of(x >> 1);
-                Slot<FULL> &sl = sm.slot[s];
-                uint64_t *bar = &sm.full_bar[s];
-                last[s] = x;
-                if (p < 0) {
-                    mbar_arrive(bar);   // completes the phase with no data: consumers skip the page
-                    continue;
-                }
-                const int64_t off = (int64_t)kvh * T * kRow + (int64_t)p * kPlane;
-                const int64_t pmo = ((int64_t)kvh * a.pool_pages + p) * (2 * kD);
-                const int64_t cmo = ((int64_t)kvh * a.pool_pages + p) * (kNChunk * 2 * kD);
-                mbar_arrive_expect_tx(bar, (FULL ? 2u : 1u) * kPlane + 2 * kD * 4 + kNChunk * 2 * kD * 2);
-                bulk_g2s(sl.a, (t ? a.va : a.ka) + off, kPlane, bar);
-                if (FULL)
-                    bulk_g2s(sl.r, (t ? a.vr : a.kr) + off, kPlane, bar);
-                bulk_g2s(sl.pm, (t ? a.vpm : a.kpm) + pmo, 2 * kD * 4, bar);
-                bulk_g2s(sl.cm, (t ? a.vcm : a.kcm) + cmo, kNChunk * 2 * kD * 2, bar);
-            }
-            // let every copy issued land before the CTA can end (bounded)
-            for (int s = 0; s < NS; ++s)
-                if (last[s] >= 0 && !mbar_wait_bounded(&sm.full_bar[s], (uint32_t)((last[s] / NS) & 1), kWaitLimit))
-                    ok = false;
-            if (!ok && a.dev_err)
-                atomicOr(a.dev_err, LYNX_DEVERR_TIMEOUT);
+    // ---- the ring: page i's K is item 2i, its V item 2i + 1; item x goes
+    // to slot x % NS. Each of the 8 chunks of an item releases it once its
+    // codes and metadata are in registers; the warp giving the 8th release
+    // refills the slot with item x + NS at once.
+    auto issue = [&](int x) {
+        const int s = x % NS;
+        const int t = x & 1;
+        const int p = phys_of(x >> 1);
+        Slot<FULL> &sl = sm.slot[s];
+        uint64_t *bar = &sm.full_bar[s];
+        *reinterpret_cast<volatile int *>(&sm.last[s]) = x;
+        if (p < 0) {
+            mbar_arrive(bar);   // completes the phase with no data: consumers skip the page
+            return;
         }
-    } else {
-        // ---- consumer warp j: chunk j of every page --------------------------
-        const int j = warp;
-        const uint32_t lane4 = (uint32_t)lane << 2;
-        const unsigned char *lut = reinterpret_cast<const unsigned char *>(sm.lut);
-        float *kaf = sm.aff[j][0][0], *kbf = sm.aff[j][0][1];
-        float *vaf = sm.aff[j][1][0], *vbf = sm.aff[j][1][1];
-        const float qmax = sm.qmax;
-        bool timed_out = false;
+        const int64_t off = (int64_t)kvh * T * kRow + (int64_t)p * kPlane;
+        const int64_t pmo = ((int64_t)kvh * a.pool_pages + p) * (2 * kD);
+        const int64_t cmo = ((int64_t)kvh * a.pool_pages + p) * (kNChunk * 2 * kD);
+        mbar_arrive_expect_tx(bar, (FULL ? 2u : 1u) * kPlane + 2 * kD * 4 + kNChunk * 2 * kD * 2);
+        bulk_g2s(sl.a, (t ? a.va : a.ka) + off, kPlane, bar);
+        if (FULL)
+            bulk_g2s(sl.r, (t ? a.vr : a.kr) + off, kPlane, bar);
+        bulk_g2s(sl.pm, (t ? a.vpm : a.kpm) + pmo, 2 * kD * 4, bar);
+        bulk_g2s(sl.cm, (t ? a.vcm : a.kcm) + cmo, kNChunk * 2 * kD * 2, bar);
+    };
+    // lane 0, after the warp's last read of item x's slot
+    auto release = [&](int x) {
+        const int s = x % NS;
+        __threadfence_block();
+        if (atomicAdd(&sm.rel[s], 1) == kNChunk - 1) {
+            sm.rel[s] = 0;
+            __threadfence_block();
+            if (x + NS < 2 * np) {
+                fence_proxy_async_smem();
+                issue(x + NS);
+            }
+        }
+    };
+    // A warp skips the pages other warps take, so a slot's barrier may still
+    // be in the phase of an item this warp never saw, whose parity equals
+    // that of the one it waits for; the slot's tag (the item last issued into
+    // it) tells the two apart: once it reads x, the phase of x is current or
+    // complete.
+    auto wait_item = [&](int x) -> bool {
+        const int s = x % NS;
+        const volatile int *tag = &sm.last[s];
+        uint32_t it = 0;
+        while (*tag != x) {
+            if (++it == kWaitLimit)
+                return false;
+            __nanosleep(32);
+        }
+        return mbar_wait_bounded(&sm.full_bar[s], (uint32_t)((x / NS) & 1), kWaitLimit);
+    };
+    if (tid == 0)
+        for (int x = 0; x < NS && x < 2 * np; ++x)
+            issue(x);
 
-        for (int i = 0; i < np; ++i) {
-            const int xk = 2 * i, sK = xk % NS, sV = (xk + 1) % NS;
-            const uint32_t parK = (uint32_t)((xk / NS) & 1), parV = (uint32_t)(((xk + 1) / NS) & 1);
-            const int lp = p_begin + i;
-            const bool valid = phys_of(i) >= 0;
-            const int nv = min(max(ctx - lp * kPage - j * kChunk, 0), kChunk);   // valid tokens of chunk j
-            if (!mbar_wait_bounded(&sm.full_bar[sK], parK, kWaitLimit)) {
+    // ---- warp w: chunks w, w + kWarps, ... of the range (chunk c = chunk
+    // c % 8 of page c / 8) ------------------------------------------------
+    const uint32_t lane4 = (uint32_t)lane << 2;
+    const unsigned char *lut = reinterpret_cast<const unsigned char *>(sm.lut);
+    float *kaf = sm.aff[warp][0][0], *kbf = sm.aff[warp][0][1];
+    float *vaf = sm.aff[warp][1][0], *vbf = sm.aff[warp][1][1];
+    const float qmax = sm.qmax;
+    bool timed_out = false;
+    for (int c = warp; c < kNChunk * np; c += kWarps) {
+        const int i = c >> 3, j = c & 7;
+        const int xk = 2 * i, sK = xk % NS, sV = (xk + 1) % NS;
+        const int lp = p_begin + i;
+        const bool valid = phys_of(i) >= 0;
+        const int nv = min(max(ctx - lp * kPage - j * kChunk, 0), kChunk);   // valid tokens of chunk j
+        if (!wait_item(xk)) {
+            timed_out = true;
+            break;
+        }
+        if (!valid || nv == 0) {
+            if (!valid && a.dev_err && j == 0 && lane == 0)
+                atomicOr(a.dev_err, LYNX_DEVERR_PAGE);
+            if (a.scores)
+                for (int e = lane; e < G * kChunk; e += 32)
+                    a.scores[(qrow0 + e / kChunk) * score_stride + (int64_t)lp * kPage + j * kChunk + e % kChunk] =
+                        neg_inf();
+            __syncwarp();
+            if (lane == 0)
+                release(xk);
+            if (!wait_item(xk + 1)) {
                 timed_out = true;
                 break;
             }
-            if (!valid || nv == 0) {
-                if (!valid && a.dev_err && j == 0 && lane == 0)
-                    atomicOr(a.dev_err, LYNX_DEVERR_PAGE);
-                if (a.scores)
-                    for (int e = lane; e < G * kChunk; e += 32)
-                        a.scores[(qrow0 + e / kChunk) * score_stride + (int64_t)lp * kPage + j * kChunk + e % kChunk] =
-                            neg_inf();
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(&sm.empty_bar[sK]);
-                if (!mbar_wait_bounded(&sm.full_bar[sV], parV, kWaitLimit)) {
-                    timed_out = true;
-                    break;
-                }
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(&sm.empty_bar[sV]);
-                continue;
-            }
+            __syncwarp();
+            if (lane == 0)
+                release(xk + 1);
+            continue;
+        }
 
-            // ---- K: affines and codes of chunk j, then release the slot -------
-            float gscale, gdown;
-            uint4 kc[4], kr4[4];
-            {
-                const Slot<FULL> &sl = sm.slot[sK];
-                float bm = chunk_affines(sl.pm, sl.cm, j, lane, kaf, kbf);
-                const uint8_t *ca = sl.a + (j * kChunk + g) * kRow + 16 * q;
-#pragma unroll
-                for (int nt = 0; nt < 4; ++nt)
-                    kc[nt] = *reinterpret_cast<const uint4 *>(ca + nt * 8 * kRow);
-                if (FULL) {
-                    const uint8_t *cr = sl.r + (j * kChunk + g) * kRow + 16 * q;
-#pragma unroll
-                    for (int nt = 0; nt < 4; ++nt)
-                        kr4[nt] = *reinterpret_cast<const uint4 *>(cr + nt * 8 * kRow);
-                }
-#pragma unroll
-                for (int o = 16; o >= 1; o >>= 1)
-                    bm = fmaxf(bm, __shfl_xor_sync(0xFFFFFFFFu, bm, o));
-                // q b must stay a finite fp16 pair: past 2^14 it is scaled by
-                // 2^-e and the scores back by 2^e
-                int ge = 0;
-                if (bm * qmax >= 16384.0f) {
-                    frexpf(bm * qmax, &ge);
-                    ge -= 14;
-                }
-                gdown = exp2f((float)-ge);
-                gscale = exp2f((float)ge);
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(&sm.empty_bar[sK]);
-            }
-
-            // ---- Q.K^T ------------------------------------------------------------
-            float S[4][4];
+        // ---- K: affines and codes of chunk j, then release the slot -------
+        float gscale, gdown;
+        int ge = 0;
+        uint4 kc[4], kr4[4];
+        {
+            const Slot<FULL> &sl = sm.slot[sK];
+            float bm = chunk_affines(sl.pm, sl.cm, j, lane, kaf, kbf);
+            const uint8_t *ca = sl.a + (j * kChunk + g) * kRow + 16 * q;
 #pragma unroll
             for (int nt = 0; nt < 4; ++nt)
-                S[nt][0] = S[nt][1] = S[nt][2] = S[nt][3] = 0.0f;
-            float2 beta2[R];
+                kc[nt] = *reinterpret_cast<const uint4 *>(ca + nt * 8 * kRow);
+            if (FULL) {
+                const uint8_t *cr = sl.r + (j * kChunk + g) * kRow + 16 * q;
 #pragma unroll
-            for (int r = 0; r < R; ++r)
-                beta2[r] = make_float2(0.0f, 0.0f);
+                for (int nt = 0; nt < 4; ++nt)
+                    kr4[nt] = *reinterpret_cast<const uint4 *>(cr + nt * 8 * kRow);
+            }
 #pragma unroll
-            for (int s = 0; s < 8; ++s) {
-                const int cp = 36 * q + 4 * s;   // channels 32q + 4s .. + 3 (padded index)
-                const float4 bb = *reinterpret_cast<const float4 *>(kbf + cp);
-                const float4 aa = *reinterpret_cast<const float4 *>(kaf + cp);
-                uint32_t A0[4], A1[4];           // G16: hi and lo fragments; else A0 = hi rows over lo rows
+            for (int o = 16; o >= 1; o >>= 1)
+                bm = fmaxf(bm, __shfl_xor_sync(0xFFFFFFFFu, bm, o));
+            // q b must stay a finite fp16 pair: past 2^14 it is scaled by
+            // 2^-e and the scores back by 2^e
+            if (bm * qmax >= 16384.0f) {
+                frexpf(bm * qmax, &ge);
+                ge -= 14;
+            }
+            gdown = exp2f((float)-ge);
+            gscale = exp2f((float)ge);
+            __syncwarp();
+            if (lane == 0)
+                release(xk);
+        }
+
+        // ---- Q.K^T ------------------------------------------------------------
+        float S[4][4];
+        float2 beta2[R];
 #pragma unroll
-                for (int r = 0; r < R; ++r) {
-                    const float4 qv = sm.qf[s][r][lane];
-                    beta2[r] = __ffma2_rn(make_float2(qv.x, qv.y), make_float2(aa.x, aa.y), beta2[r]);
-                    beta2[r] = __ffma2_rn(make_float2(qv.z, qv.w), make_float2(aa.z, aa.w), beta2[r]);
-                    float2 x01 = __fmul2_rn(make_float2(qv.x, qv.y), make_float2(bb.x, bb.y));
-                    float2 x23 = __fmul2_rn(make_float2(qv.z, qv.w), make_float2(bb.z, bb.w));
+        for (int r = 0; r < R; ++r)
+            beta2[r] = make_float2(0.0f, 0.0f);
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
+            const int cp = 36 * q + 4 * s;   // channels 32q + 4s .. + 3 (padded index)
+            const float4 bb = *reinterpret_cast<const float4 *>(kbf + cp);
+            const float4 aa = *reinterpret_cast<const float4 *>(kaf + cp);
+            uint32_t A0[4], A1[4];           // G16: hi and lo fragments; else A0 = hi rows over lo rows
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const float4 qv = sm.qf[s][r][lane];
+                beta2[r] = __ffma2_rn(make_float2(qv.x, qv.y), make_float2(aa.x, aa.y), beta2[r]);
+                beta2[r] = __ffma2_rn(make_float2(qv.z, qv.w), make_float2(aa.z, aa.w), beta2[r]);
+                float2 x01 = __fmul2_rn(make_float2(qv.x, qv.y), make_float2(bb.x, bb.y));
+                float2 x23 = __fmul2_rn(make_float2(qv.z, qv.w), make_float2(bb.z, bb.w));
+                if (ge != 0) {
                     x01 = __fmul2_rn(x01, make_float2(gdown, gdown));
                     x23 = __fmul2_rn(x23, make_float2(gdown, gdown));
-                    if (G16) {
-                        split2(x01, A0[r], A1[r]);
-                        split2(x23, A0[2 + r], A1[2 + r]);
-                    } else {
-                        split2(x01, A0[0], A0[1]);
-                        split2(x23, A0[2], A0[3]);
-                    }
                 }
-                const int wi = s >> 1;
-#pragma unroll
-                for (int nt = 0; nt < 4; ++nt) {
-                    const uint32_t aw = wi == 0 ? kc[nt].x : wi == 1 ? kc[nt].y : wi == 2 ? kc[nt].z : kc[nt].w;
-                    uint32_t b0, b1;
-                    if (FULL) {
-                        const uint32_t rw = wi == 0 ? kr4[nt].x : wi == 1 ? kr4[nt].y : wi == 2 ? kr4[nt].z : kr4[nt].w;
-                        const uint32_t ev = codes_even(aw, rw), od = codes_odd(aw, rw);
-                        if (s & 1) {
-                            b0 = pack_lo(lut_full<2>(lut, ev, lane4), lut_full<2>(lut, od, lane4));
-                            b1 = pack_lo(lut_full<3>(lut, ev, lane4), lut_full<3>(lut, od, lane4));
-                        } else {
-                            b0 = pack_lo(lut_full<0>(lut, ev, lane4), lut_full<0>(lut, od, lane4));
-                            b1 = pack_lo(lut_full<1>(lut, ev, lane4), lut_full<1>(lut, od, lane4));
-                        }
-                    } else {
-                        if (s & 1) {
-                            b0 = lut_anchor<2>(lut, aw, lane4);
-                            b1 = lut_anchor<3>(lut, aw, lane4);
-                        } else {
-                            b0 = lut_anchor<0>(lut, aw, lane4);
-                            b1 = lut_anchor<1>(lut, aw, lane4);
-                        }
-                    }
-                    mma16816(S[nt], A0, b0, b1);
-                    if (G16)
-                        mma16816(S[nt], A1, b0, b1);
-                }
-            }
-
-            // ---- scores (base-2 log domain), masking, online softmax ---------------
-            float beta[R];
-#pragma unroll
-            for (int r = 0; r < R; ++r) {
-                float bt = beta2[r].x + beta2[r].y;
-                bt += __shfl_xor_sync(0xFFFFFFFFu, bt, 1);
-                bt += __shfl_xor_sync(0xFFFFFFFFu, bt, 2);
-                beta[r] = bt;
-            }
-            float P[R][4][2];                    // row r, n-tile nt: tokens 8 nt + 2q, + 1
-            float psum[R];
-            bool rescale = false;
-            float alpha[R];
-#pragma unroll
-            for (int r = 0; r < R; ++r) {
-                float mx = neg_inf();
-#pragma unroll
-                for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const float acc = G16 ? S[nt][2 * r + e] : S[nt][e] + S[nt][2 + e];
-                        float v = fmaf(acc, gscale, beta[r]);
-                        if (nv < kChunk && 8 * nt + 2 * q + e >= nv)
-                            v = neg_inf();
-                        P[r][nt][e] = v;
-                        mx = fmaxf(mx, v);
-                    }
-                const int h = g + 8 * r;
-                if (a.scores && h < G) {
-                    float *srow = a.scores + (qrow0 + h) * score_stride + (int64_t)lp * kPage + j * kChunk;
-#pragma unroll
-                    for (int nt = 0; nt < 4; ++nt)
-                        *reinterpret_cast<float2 *>(srow + nt * 8 + 2 * q) =
-                            make_float2(P[r][nt][0] * kLn2, P[r][nt][1] * kLn2);
-                }
-                mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
-                mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));
-                const float m_new = fmaxf(m_run[r], mx);
-                alpha[r] = exp2f(m_run[r] - m_new);
-                rescale |= alpha[r] != 1.0f;
-                m_run[r] = m_new;
-                float ps = 0.0f;
-#pragma unroll
-                for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const float pv = exp2f(P[r][nt][e] - m_new);
-                        P[r][nt][e] = pv;
-                        ps += pv;
-                    }
-                l_run[r] = fmaf(l_run[r], alpha[r], ps);
-                ps += __shfl_xor_sync(0xFFFFFFFFu, ps, 1);
-                ps += __shfl_xor_sync(0xFFFFFFFFu, ps, 2);
-                psum[r] = ps;
-            }
-            if (__any_sync(0xFFFFFFFFu, rescale)) {
-#pragma unroll
-                for (int r = 0; r < R; ++r) {
-                    const float2 al = make_float2(alpha[r], alpha[r]);
-#pragma unroll
-                    for (int m = 0; m < 8; ++m) {
-                        Olo[r][m] = __fmul2_rn(Olo[r][m], al);
-                        Ohi[r][m] = __fmul2_rn(Ohi[r][m], al);
-                    }
-                }
-            }
-            // P as A fragments; k-step kk = tokens 16 kk .. 16 kk + 15
-            uint32_t PA0[2][4], PA1[2][4];       // G16: hi, lo; else PA0 = hi rows over lo rows
-#pragma unroll
-            for (int kk = 0; kk < 2; ++kk) {
                 if (G16) {
+                    split2(x01, A0[r], A1[r]);
+                    split2(x23, A0[2 + r], A1[2 + r]);
+                } else {
+                    split2(x01, A0[0], A0[1]);
+                    split2(x23, A0[2], A0[3]);
+                }
+            }
+            const int wi = s >> 1;
 #pragma unroll
-                    for (int r = 0; r < R; ++r) {
-                        split2(make_float2(P[r][2 * kk][0], P[r][2 * kk][1]), PA0[kk][r], PA1[kk][r]);
-                        split2(make_float2(P[r][2 * kk + 1][0], P[r][2 * kk + 1][1]), PA0[kk][2 + r], PA1[kk][2 + r]);
+            for (int nt = 0; nt < 4; ++nt) {
+                const uint32_t aw = wi == 0 ? kc[nt].x : wi == 1 ? kc[nt].y : wi == 2 ? kc[nt].z : kc[nt].w;
+                uint32_t b0, b1;
+                if (FULL) {
+                    const uint32_t rw = wi == 0 ? kr4[nt].x : wi == 1 ? kr4[nt].y : wi == 2 ? kr4[nt].z : kr4[nt].w;
+                    const uint32_t ev = codes_even(aw, rw), od = codes_odd(aw, rw);
+                    if (s & 1) {
+                        b0 = pack_lo(lut_full<2>(lut, ev, lane4), lut_full<2>(lut, od, lane4));
+                        b1 = pack_lo(lut_full<3>(lut, ev, lane4), lut_full<3>(lut, od, lane4));
+                    } else {
+                        b0 = pack_lo(lut_full<0>(lut, ev, lane4), lut_full<0>(lut, od, lane4));
+                        b1 = pack_lo(lut_full<1>(lut, ev, lane4), lut_full<1>(lut, od, lane4));
                     }
                 } else {
-                    split2(make_float2(P[0][2 * kk][0], P[0][2 * kk][1]), PA0[kk][0], PA0[kk][1]);
-                    split2(make_float2(P[0][2 * kk + 1][0], P[0][2 * kk + 1][1]), PA0[kk][2], PA0[kk][3]);
+                    if (s & 1) {
+                        b0 = lut_anchor<2>(lut, aw, lane4);
+                        b1 = lut_anchor<3>(lut, aw, lane4);
+                    } else {
+                        b0 = lut_anchor<0>(lut, aw, lane4);
+                        b1 = lut_anchor<1>(lut, aw, lane4);
+                    }
+                }
+                if (s == 0)
+                    mma16816_z(S[nt], A0, b0, b1);
+                else
+                    mma16816(S[nt], A0, b0, b1);
+                if (G16)
+                    mma16816(S[nt], A1, b0, b1);
+            }
+        }
+
+        // ---- scores (base-2 log domain), masking, online softmax ---------------
+        float beta[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            float bt = beta2[r].x + beta2[r].y;
+            bt += __shfl_xor_sync(0xFFFFFFFFu, bt, 1);
+            bt += __shfl_xor_sync(0xFFFFFFFFu, bt, 2);
+            beta[r] = bt;
+        }
+        float P[R][4][2];                    // row r, n-tile nt: tokens 8 nt + 2q, + 1
+        float psum[R];
+        bool rescale = false;
+        float alpha[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            float mx = neg_inf();
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const float acc = G16 ? S[nt][2 * r + e] : S[nt][e] + S[nt][2 + e];
+                    float v = fmaf(acc, gscale, beta[r]);
+                    if (nv < kChunk && 8 * nt + 2 * q + e >= nv)
+                        v = neg_inf();
+                    P[r][nt][e] = v;
+                    mx = fmaxf(mx, v);
+                }
+            const int h = g + 8 * r;
+            if (a.scores && h < G) {
+                float *srow = a.scores + (qrow0 + h) * score_stride + (int64_t)lp * kPage + j * kChunk;
+#pragma unroll
+                for (int nt = 0; nt < 4; ++nt)
+                    *reinterpret_cast<float2 *>(srow + nt * 8 + 2 * q) =
+                        make_float2(P[r][nt][0] * kLn2, P[r][nt][1] * kLn2);
+            }
+            mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
+            mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));
+            // the reference max moves only when a score passes it by more than
+            // 2^8 (weights up to 2^8 are exact in fp32 and fine in fp16), so
+            // the running output is rarely rescaled
+            const bool up = mx > m_run[r] + 8.0f;
+            const float m_new = up ? mx : m_run[r];
+            alpha[r] = up ? exp2_sm(m_run[r] - m_new) : 1.0f;
+            rescale |= up;
+            m_run[r] = m_new;
+            float ps = 0.0f;
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const float pv = exp2_sm(P[r][nt][e] - m_new);
+                    P[r][nt][e] = pv;
+                    ps += pv;
+                }
+            l_run[r] = fmaf(l_run[r], alpha[r], ps);
+            ps += __shfl_xor_sync(0xFFFFFFFFu, ps, 1);
+            ps += __shfl_xor_sync(0xFFFFFFFFu, ps, 2);
+            psum[r] = ps;
+        }
+        if (__any_sync(0xFFFFFFFFu, rescale)) {
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const float2 al = make_float2(alpha[r], alpha[r]);
+#pragma unroll
+                for (int m = 0; m < 8; ++m) {
+                    Olo[r][m] = __fmul2_rn(Olo[r][m], al);
+                    Ohi[r][m] = __fmul2_rn(Ohi[r][m], al);
                 }
             }
-
-            // ---- V: affines and codes of chunk j, then release the slot -------
-            if (!mbar_wait_bounded(&sm.full_bar[sV], parV, kWaitLimit)) {
-                timed_out = true;
-                break;
+        }
+        // P as A fragments; k-step kk = tokens 16 kk .. 16 kk + 15
+        uint32_t PA0[2][4], PA1[2][4];       // G16: hi, lo; else PA0 = hi rows over lo rows
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk) {
+            if (G16) {
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    split2(make_float2(P[r][2 * kk][0], P[r][2 * kk][1]), PA0[kk][r], PA1[kk][r]);
+                    split2(make_float2(P[r][2 * kk + 1][0], P[r][2 * kk + 1][1]), PA0[kk][2 + r], PA1[kk][2 + r]);
+                }
+            } else {
+                split2(make_float2(P[0][2 * kk][0], P[0][2 * kk][1]), PA0[kk][0], PA0[kk][1]);
+                split2(make_float2(P[0][2 * kk + 1][0], P[0][2 * kk + 1][1]), PA0[kk][2], PA0[kk][3]);
             }
-            uint2 vc[2][4], vr4[2][4];           // [k-step][tokens 2q, 2q + 1, 2q + 8, 2q + 9], bytes 8g .. 8g + 7
-            {
-                const Slot<FULL> &sl = sm.slot[sV];
-                chunk_affines(sl.pm, sl.cm, j, lane, vaf, vbf);
-                const uint8_t *ca = sl.a + (j * kChunk + 2 * q) * kRow + 8 * g;
+        }
+
+        // ---- V: affines and codes of chunk j, then release the slot -------
+        if (!wait_item(xk + 1)) {
+            timed_out = true;
+            break;
+        }
+        uint2 vc[2][4], vr4[2][4];           // [k-step][tokens 2q, 2q + 1, 2q + 8, 2q + 9], bytes 8g .. 8g + 7
+        {
+            const Slot<FULL> &sl = sm.slot[sV];
+            chunk_affines(sl.pm, sl.cm, j, lane, vaf, vbf);
+            const uint8_t *ca = sl.a + (j * kChunk + 2 * q) * kRow + 8 * g;
+#pragma unroll
+            for (int kk = 0; kk < 2; ++kk)
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    vc[kk][u] = *reinterpret_cast<const uint2 *>(ca + (16 * kk + (u & 1) + 8 * (u >> 1)) * kRow);
+            if (FULL) {
+                const uint8_t *cr = sl.r + (j * kChunk + 2 * q) * kRow + 8 * g;
 #pragma unroll
                 for (int kk = 0; kk < 2; ++kk)
 #pragma unroll
                     for (int u = 0; u < 4; ++u)
-                        vc[kk][u] = *reinterpret_cast<const uint2 *>(ca + (16 * kk + (u & 1) + 8 * (u >> 1)) * kRow);
-                if (FULL) {
-                    const uint8_t *cr = sl.r + (j * kChunk + 2 * q) * kRow + 8 * g;
-#pragma unroll
-                    for (int kk = 0; kk < 2; ++kk)
-#pragma unroll
-                        for (int u = 0; u < 4; ++u)
-                            vr4[kk][u] = *reinterpret_cast<const uint2 *>(cr + (16 * kk + (u & 1) + 8 * (u >> 1)) * kRow);
-                }
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(&sm.empty_bar[sV]);
+                        vr4[kk][u] = *reinterpret_cast<const uint2 *>(cr + (16 * kk + (u & 1) + 8 * (u >> 1)) * kRow);
             }
+            __syncwarp();
+            if (lane == 0)
+                release(xk + 1);
+        }
 
-            // ---- P.V: n-tile 2m + e holds channel 16 n + 2m + e of column n ------
+        // ---- P.V: n-tile 2m + e holds channel 16 n + 2m + e of column n ------
 #pragma unroll
-            for (int m = 0; m < 8; ++m) {
-                const int wi = m >> 2;
-                float C[2][4];
+        for (int m = 0; m < 8; ++m) {
+            const int wi = m >> 2;
+            float C[2][4];
 #pragma unroll
-                for (int e = 0; e < 2; ++e)
-                    C[e][0] = C[e][1] = C[e][2] = C[e][3] = 0.0f;
-#pragma unroll
-                for (int kk = 0; kk < 2; ++kk) {
-                    uint32_t bl0, bl1, bo0, bo1;   // (b0, b1) of n-tiles 2m and 2m + 1
-                    const uint32_t x0 = wi ? vc[kk][0].y : vc[kk][0].x, x1 = wi ? vc[kk][1].y : vc[kk][1].x;
-                    const uint32_t x2 = wi ? vc[kk][2].y : vc[kk][2].x, x3 = wi ? vc[kk][3].y : vc[kk][3].x;
-                    if (FULL) {
-                        const uint32_t r0 = wi ? vr4[kk][0].y : vr4[kk][0].x, r1 = wi ? vr4[kk][1].y : vr4[kk][1].x;
-                        const uint32_t r2 = wi ? vr4[kk][2].y : vr4[kk][2].x, r3 = wi ? vr4[kk][3].y : vr4[kk][3].x;
-                        const uint32_t e0 = codes_even(x0, r0), e1 = codes_even(x1, r1);
-                        const uint32_t e2 = codes_even(x2, r2), e3 = codes_even(x3, r3);
-                        const uint32_t o0 = codes_odd(x0, r0), o1 = codes_odd(x1, r1);
-                        const uint32_t o2 = codes_odd(x2, r2), o3 = codes_odd(x3, r3);
-                        switch (m & 3) {
+            for (int kk = 0; kk < 2; ++kk) {
+                uint32_t bl0, bl1, bo0, bo1;   // (b0, b1) of n-tiles 2m and 2m + 1
+                const uint32_t x0 = wi ? vc[kk][0].y : vc[kk][0].x, x1 = wi ? vc[kk][1].y : vc[kk][1].x;
+                const uint32_t x2 = wi ? vc[kk][2].y : vc[kk][2].x, x3 = wi ? vc[kk][3].y : vc[kk][3].x;
+                if (FULL) {
+                    const uint32_t r0 = wi ? vr4[kk][0].y : vr4[kk][0].x, r1 = wi ? vr4[kk][1].y : vr4[kk][1].x;
+                    const uint32_t r2 = wi ? vr4[kk][2].y : vr4[kk][2].x, r3 = wi ? vr4[kk][3].y : vr4[kk][3].x;
+                    const uint32_t e0 = codes_even(x0, r0), e1 = codes_even(x1, r1);
+                    const uint32_t e2 = codes_even(x2, r2), e3 = codes_even(x3, r3);
+                    const uint32_t o0 = codes_odd(x0, r0), o1 = codes_odd(x1, r1);
+                    const uint32_t o2 = codes_odd(x2, r2), o3 = codes_odd(x3, r3);
+                    switch (m & 3) {
 #define LYNX_V_FULL(I)                                                                                                 \
-    case I:                                                                                                            \
-        bl0 = pack_lo(lut_full<I>(lut, e0, lane4), lut_full<I>(lut, e1, lane4));                                      \
-        bl1 = pack_lo(lut_full<I>(lut, e2, lane4), lut_full<I>(lut, e3, lane4));                                      \
-        bo0 = pack_lo(lut_full<I>(lut, o0, lane4), lut_full<I>(lut, o1, lane4));                                      \
-        bo1 = pack_lo(lut_full<I>(lut, o2, lane4), lut_full<I>(lut, o3, lane4));                                      \
-        break;
-                            LYNX_V_FULL(0)
-                            LYNX_V_FULL(1)
-                            LYNX_V_FULL(2)
-                            default:
-                            LYNX_V_FULL(3)
+case I:                                                                                                            \
+    bl0 = pack_lo(lut_full<I>(lut, e0, lane4), lut_full<I>(lut, e1, lane4));                                      \
+    bl1 = pack_lo(lut_full<I>(lut, e2, lane4), lut_full<I>(lut, e3, lane4));                                      \
+    bo0 = pack_lo(lut_full<I>(lut, o0, lane4), lut_full<I>(lut, o1, lane4));                                      \
+    bo1 = pack_lo(lut_full<I>(lut, o2, lane4), lut_full<I>(lut, o3, lane4));                                      \
+    break;
+                        LYNX_V_FULL(0)
+                        LYNX_V_FULL(1)
+                        LYNX_V_FULL(2)
+                        default:
+                        LYNX_V_FULL(3)
 #undef LYNX_V_FULL
-                        }
-                    } else {
-                        const uint32_t e01 = nib_even(x0, x1), e23 = nib_even(x2, x3);
-                        const uint32_t o01 = nib_odd(x0, x1), o23 = nib_odd(x2, x3);
-                        switch (m & 3) {
-#define LYNX_V_ANCHOR(I)                                                                                               \
-    case I:                                                                                                            \
-        bl0 = lut_anchor<I>(lut, e01, lane4);                                                                          \
-        bl1 = lut_anchor<I>(lut, e23, lane4);                                                                          \
-        bo0 = lut_anchor<I>(lut, o01, lane4);                                                                          \
-        bo1 = lut_anchor<I>(lut, o23, lane4);                                                                          \
-        break;
-                            LYNX_V_ANCHOR(0)
-                            LYNX_V_ANCHOR(1)
-                            LYNX_V_ANCHOR(2)
-                            default:
-                            LYNX_V_ANCHOR(3)
-#undef LYNX_V_ANCHOR
-                        }
                     }
+                } else {
+                    const uint32_t e01 = nib_even(x0, x1), e23 = nib_even(x2, x3);
+                    const uint32_t o01 = nib_odd(x0, x1), o23 = nib_odd(x2, x3);
+                    switch (m & 3) {
+#define LYNX_V_ANCHOR(I)                                                                                               \
+case I:                                                                                                            \
+    bl0 = lut_anchor<I>(lut, e01, lane4);                                                                          \
+    bl1 = lut_anchor<I>(lut, e23, lane4);                                                                          \
+    bo0 = lut_anchor<I>(lut, o01, lane4);                                                                          \
+    bo1 = lut_anchor<I>(lut, o23, lane4);                                                                          \
+    break;
+                        LYNX_V_ANCHOR(0)
+                        LYNX_V_ANCHOR(1)
+                        LYNX_V_ANCHOR(2)
+                        default:
+                        LYNX_V_ANCHOR(3)
+#undef LYNX_V_ANCHOR
+                    }
+                }
+                if (kk == 0) {
+                    mma16816_z(C[0], PA0[kk], bl0, bl1);
+                    mma16816_z(C[1], PA0[kk], bo0, bo1);
+                } else {
                     mma16816(C[0], PA0[kk], bl0, bl1);
                     mma16816(C[1], PA0[kk], bo0, bo1);
-                    if (G16) {
-                        mma16816(C[0], PA1[kk], bl0, bl1);
-                        mma16816(C[1], PA1[kk], bo0, bo1);
-                    }
                 }
-                // o += b (P.L) + a sum(P): column 2q -> channels 32q + 2m, + 1;
-                // column 2q + 1 -> channels 32q + 16 + 2m, + 1
-                const float2 bl = *reinterpret_cast<const float2 *>(vbf + 36 * q + 2 * m);
-                const float2 bh = *reinterpret_cast<const float2 *>(vbf + 36 * q + 16 + 2 * m);
-                const float2 al = *reinterpret_cast<const float2 *>(vaf + 36 * q + 2 * m);
-                const float2 ah = *reinterpret_cast<const float2 *>(vaf + 36 * q + 16 + 2 * m);
-#pragma unroll
-                for (int r = 0; r < R; ++r) {
-                    float2 cl, ch;
-                    if (G16) {
-                        cl = make_float2(C[0][2 * r], C[1][2 * r]);
-                        ch = make_float2(C[0][2 * r + 1], C[1][2 * r + 1]);
-                    } else {
-                        cl = make_float2(C[0][0] + C[0][2], C[1][0] + C[1][2]);
-                        ch = make_float2(C[0][1] + C[0][3], C[1][1] + C[1][3]);
-                    }
-                    const float2 ps2 = make_float2(psum[r], psum[r]);
-                    Olo[r][m] = __ffma2_rn(bl, cl, __ffma2_rn(al, ps2, Olo[r][m]));
-                    Ohi[r][m] = __ffma2_rn(bh, ch, __ffma2_rn(ah, ps2, Ohi[r][m]));
+                if (G16) {
+                    mma16816(C[0], PA1[kk], bl0, bl1);
+                    mma16816(C[1], PA1[kk], bo0, bo1);
                 }
             }
+            // o += b (P.L) + a sum(P): column 2q -> channels 32q + 2m, + 1;
+            // column 2q + 1 -> channels 32q + 16 + 2m, + 1
+            const float2 bl = *reinterpret_cast<const float2 *>(vbf + 36 * q + 2 * m);
+            const float2 bh = *reinterpret_cast<const float2 *>(vbf + 36 * q + 16 + 2 * m);
+            const float2 al = *reinterpret_cast<const float2 *>(vaf + 36 * q + 2 * m);
+            const float2 ah = *reinterpret_cast<const float2 *>(vaf + 36 * q + 16 + 2 * m);
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                float2 cl, ch;
+                if (G16) {
+                    cl = make_float2(C[0][2 * r], C[1][2 * r]);
+                    ch = make_float2(C[0][2 * r + 1], C[1][2 * r + 1]);
+                } else {
+                    cl = make_float2(C[0][0] + C[0][2], C[1][0] + C[1][2]);
+                    ch = make_float2(C[0][1] + C[0][3], C[1][1] + C[1][3]);
+                }
+                const float2 ps2 = make_float2(psum[r], psum[r]);
+                Olo[r][m] = __ffma2_rn(bl, cl, __ffma2_rn(al, ps2, Olo[r][m]));
+                Ohi[r][m] = __ffma2_rn(bh, ch, __ffma2_rn(ah, ps2, Ohi[r][m]));
+            }
         }
-        if (timed_out && a.dev_err && lane == 0)
+    }
+    if (timed_out && a.dev_err && lane == 0)
+        atomicOr(a.dev_err, LYNX_DEVERR_TIMEOUT);
+    __syncthreads();
+    if (tid == 0) {
+        // every copy issued must land before the merge reuses the slots
+        // (after a timeout some may still be in flight; bounded)
+        bool ok = true;
+        for (int s = 0; s < NS; ++s)
+            if (sm.last[s] >= 0 && !mbar_wait_bounded(&sm.full_bar[s], (uint32_t)((sm.last[s] / NS) & 1), kWaitLimit))
+                ok = false;
+        if (!ok && a.dev_err)
             atomicOr(a.dev_err, LYNX_DEVERR_TIMEOUT);
     }
 
     // ---- merge the chunks' states, write this range's partial ------------
-    __syncthreads();   // every table and query read is done; the merge area overlays them
-    Merge &mg = *reinterpret_cast<Merge *>(smem_raw);
-    if (warp < kCons) {
+    __syncthreads();   // every copy has landed and every slot read is done: the merge area overlays the slots
+    Merge &mg = *reinterpret_cast<Merge *>(sm.slot);
+    {
         const int j = warp;
 #pragma unroll
         for (int r = 0; r < R; ++r) {
@@ -667,12 +722,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(AttnArgs a, Level
         const int h = e / kD, d = e % kD;
         float M = neg_inf();
 #pragma unroll
-        for (int w = 0; w < kNChunk; ++w)
+        for (int w = 0; w < kWarps; ++w)
             M = fmaxf(M, mg.m[w][h]);
         float L = 0.0f, o = 0.0f;
         if (M > neg_inf()) {
 #pragma unroll
-            for (int w = 0; w < kNChunk; ++w) {
+            for (int w = 0; w < kWarps; ++w) {
                 const float sc = exp2f(mg.m[w][h] - M);
                 L = fmaf(mg.l[w][h], sc, L);
                 o = fmaf(mg.o[w][h][d], sc, o);
@@ -690,8 +745,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(AttnArgs a, Level
 template <bool G16, bool FULL, int NS>
 cudaError_t run(const AttnArgs &a, cudaStream_t s)
 {
-    static_assert(sizeof(Merge) <= sizeof(uint32_t) * 256 * 64 + sizeof(float4) * 8 * 2 * 32,
-                  "merge area overlays the table and the queries");
+    static_assert(sizeof(Merge) <= sizeof(Slot<FULL>) * NS, "merge area overlays the slots");
     static_assert(sizeof(Smem<FULL, NS>) <= 227 * 1024, "shared memory per CTA");
     const size_t smem = sizeof(Smem<FULL, NS>);
     cudaError_t e = cudaFuncSetAttribute(attn_mma_kernel<G16, FULL, NS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
