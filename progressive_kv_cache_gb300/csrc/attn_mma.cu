@@ -40,6 +40,8 @@
 // second kernel merges the partials of the ranges.
 #include <cuda_fp16.h>
 
+#include <mutex>
+
 #include "lynx_internal.cuh"
 #include "lynx_ptx.cuh"
 
@@ -56,34 +58,46 @@ constexpr uint32_t kWaitLimit = 1u << 22;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
-// One tensor's page as it arrives.
-template <bool FULL>
-struct Slot {
-    uint8_t a[kPlane];
-    uint8_t r[FULL ? kPlane : 16];
+// The system reserves shared memory ahead of a kernel's dynamic window (1 KiB
+// on this part family). With that base the level table below starts at shared
+// address 0x10000, and the shared address of a table word is one byte permute
+// of the code byte and a per-lane constant. The base is measured once per
+// device (table_aligned()); with any other base the kernel adds the table's
+// address to every lookup instead.
+constexpr uint32_t kDynBase = 1024;
+constexpr uint32_t kPre = 0x10000 - kDynBase;
+
+// One tensor's page metadata as it arrives.
+struct SlotMeta {
     float pm[2 * kD];
     uint16_t cm[kNChunk * 2 * kD];
 };
 
-template <bool FULL, int NS>
-struct Smem {
-    // level table: entry e (a code byte) at byte 256 e; anchor mode: word
-    // `lane` = half2 of the levels of the two anchor nibbles of e; full mode:
-    // word `lane` = fp16 level of the code byte e (A << 4 | r) in its low half
-    uint32_t lut[256 * 64];
+template <int NS>
+struct Head {
     // the group's queries times sm_scale log2(e), as this lane's A-fragment
     // channels: qf[s][r][lane] = q[row g + 8 r][32 q + 4 s .. + 3]
     float4 qf[8][2][32];
-    Slot<FULL> slot[NS];
-    // per consumer warp and tensor (K, V): chunk affines a and b
-    float aff[kWarps][2][2][kAff];
+    float aff[kWarps][2][kAff];               // per warp: chunk affines a, b (K, then V)
+    SlotMeta meta[NS];
     float qmax;
     int rel[NS];                              // releases of the slot's current item
     int last[NS];                             // last item issued into each slot (its tag)
     alignas(8) uint64_t full_bar[NS];
 };
 
-struct Merge {                                // overlays the slots after the page loop
+template <bool FULL, int NS>
+struct Smem {
+    Head<NS> h;
+    unsigned char pad[kPre - sizeof(Head<NS>)];
+    // level table: entry e (a code byte) at byte 256 e; anchor mode: word
+    // `lane` = half2 of the levels of the two anchor nibbles of e; full mode:
+    // word 32 + `lane` = fp16 level of the code byte e (A << 4 | r) in its low half
+    uint32_t lut[256 * 64];
+    uint8_t plane[NS][FULL ? 2 : 1][kPlane];  // per slot: anchor (and residual) codes
+};
+
+struct Merge {                                // overlays the table and the planes after the page loop
     float m[kWarps][16];                      // per warp and query head
     float l[kWarps][16];
     float o[kWarps][16][kD];
@@ -127,24 +141,17 @@ __device__ __forceinline__ float exp2_sm(float x)
     return y;
 }
 
-// Byte offset of the table word of code byte `i` of w for this lane:
-// (byte << 8) | (lane << 2) in one permute (lane4 = lane << 2).
-template <int I>
-__device__ __forceinline__ uint32_t lut_addr(uint32_t w, uint32_t lane4)
+// Table word of code byte I of w. AL: lanebase = table address | lane offset
+// and one permute forms the shared address; otherwise lanebase = lane offset
+// and the table's address is added.
+template <bool AL, int I>
+__device__ __forceinline__ uint32_t lut_ld(uint32_t w, uint32_t lanebase, uint32_t base)
 {
-    return __byte_perm(w, lane4, 0x5504u | (I << 4));
-}
-
-template <int I>
-__device__ __forceinline__ uint32_t lut_anchor(const unsigned char *lut, uint32_t w, uint32_t lane4)
-{
-    return *reinterpret_cast<const uint32_t *>(lut + lut_addr<I>(w, lane4));
-}
-
-template <int I>
-__device__ __forceinline__ uint32_t lut_full(const unsigned char *lut, uint32_t w, uint32_t lane4)
-{
-    return *reinterpret_cast<const uint32_t *>(lut + 128 + lut_addr<I>(w, lane4));
+    const uint32_t addr =
+        AL ? __byte_perm(w, lanebase, 0x7604u | (I << 4)) : __byte_perm(w, lanebase, 0x5504u | (I << 4)) + base;
+    uint32_t v;
+    asm("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
 }
 
 // Low halves of x and y as one half2 (x's in the low half).
@@ -202,7 +209,7 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar)
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
-template <bool G16, bool FULL, int NS>
+template <bool G16, bool FULL, int NS, bool AL>
 __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(AttnArgs a, LevelTable lev)
 {
     constexpr int R = G16 ? 2 : 1;          // query-head rows per lane: g (and g + 8)
@@ -237,20 +244,20 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(AttnArgs a, Level
         float v = 0.0f;
         if (row < G && (G16 || r == 0))
             v = __uint_as_float((uint32_t)a.q[(qrow0 + row) * kD + d] << 16) * qscale;
-        reinterpret_cast<float *>(&sm.qf[s][r][l])[c] = v;
+        reinterpret_cast<float *>(&sm.h.qf[s][r][l])[c] = v;
         lq = fmaxf(lq, fabsf(v));
     }
     if (tid == 0) {
-        sm.qmax = 0.0f;
+        sm.h.qmax = 0.0f;
         for (int s = 0; s < NS; ++s) {
-            mbar_init(&sm.full_bar[s], 1);
-            sm.rel[s] = 0;
-            sm.last[s] = -1;
+            mbar_init(&sm.h.full_bar[s], 1);
+            sm.h.rel[s] = 0;
+            sm.h.last[s] = -1;
         }
         fence_mbar_init();
     }
     __syncthreads();
-    atomicMax(reinterpret_cast<int *>(&sm.qmax), __float_as_int(lq));   // non-negative floats order as ints
+    atomicMax(reinterpret_cast<int *>(&sm.h.qmax), __float_as_int(lq));   // non-negative floats order as ints
 
     int ctx = a.ctx[b];
     if (ctx < 0 || ctx > a.max_pages * kPage) {
@@ -297,9 +304,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(AttnArgs a, Level
         const int s = x % NS;
         const int t = x & 1;
         const int p = phys_of(x >> 1);
-        Slot<FULL> &sl = sm.slot[s];
-        uint64_t *bar = &sm.full_bar[s];
-        *reinterpret_cast<volatile int *>(&sm.last[s]) = x;
+        SlotMeta &mt = sm.h.meta[s];
+        uint64_t *bar = &sm.h.full_bar[s];
+        *reinterpret_cast<volatile int *>(&sm.h.last[s]) = x;
         if (p < 0) {
             mbar_arrive(bar);   // completes the phase with no data: consumers skip the page
             return;
@@ -308,18 +315,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(AttnArgs a, Level
         const int64_t pmo = ((int64_t)kvh * a.pool_pages + p) * (2 * kD);
         const int64_t cmo = ((int64_t)kvh * a.pool_pages + p) * (kNChunk * 2 * kD);
         mbar_arrive_expect_tx(bar, (FULL ? 2u : 1u) * kPlane + 2 * kD * 4 + kNChunk * 2 * kD * 2);
-        bulk_g2s(sl.a, (t ? a.va : a.ka) + off, kPlane, bar);
+        bulk_g2s(sm.plane[s][0], (t ? a.va : a.ka) + off, kPlane, bar);
         if (FULL)
-            bulk_g2s(sl.r, (t ? a.vr : a.kr) + off, kPlane, bar);
-        bulk_g2s(sl.pm, (t ? a.vpm : a.kpm) + pmo, 2 * kD * 4, bar);
-        bulk_g2s(sl.cm, (t ? a.vcm : a.kcm) + cmo, kNChunk * 2 * kD * 2, bar);
+            bulk_g2s(sm.plane[s][FULL ? 1 : 0], (t ? a.vr : a.kr) + off, kPlane, bar);
+        bulk_g2s(mt.pm, (t ? a.vpm : a.kpm) + pmo, 2 * kD * 4, bar);
+        bulk_g2s(mt.cm, (t ? a.vcm : a.kcm) + cmo, kNChunk * 2 * kD * 2, bar);
     };
     // lane 0, after the warp's last read of item x's slot
     auto release = [&](int x) {
         const int s = x % NS;
         __threadfence_block();
-        if (atomicAdd(&sm.rel[s], 1) == kNChunk - 1) {
-            sm.rel[s] = 0;
+        if (atomicAdd(&sm.h.rel[s], 1) == kNChunk - 1) {
+            sm.h.rel[s] = 0;
             __threadfence_block();
             if (x + NS < 2 * np) {
                 fence_proxy_async_smem();
@@ -334,14 +341,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(AttnArgs a, Level
     // complete.
     auto wait_item = [&](int x) -> bool {
         const int s = x % NS;
-        const volatile int *tag = &sm.last[s];
+        const volatile int *tag = &sm.h.last[s];
         uint32_t it = 0;
         while (*tag != x) {
             if (++it == kWaitLimit)
                 return false;
             __nanosleep(32);
         }
-        return mbar_wait_bounded(&sm.full_bar[s], (uint32_t)((x / NS) & 1), kWaitLimit);
+        return mbar_wait_bounded(&sm.h.full_bar[s], (uint32_t)((x / NS) & 1), kWaitLimit);
     };
     if (tid == 0)
         for (int x = 0; x < NS && x < 2 * np; ++x)
@@ -350,10 +357,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(AttnArgs a, Level
     // ---- warp w: chunks w, w + kWarps, ... of the range (chunk c = chunk
     // c % 8 of page c / 8) ------------------------------------------------
     const uint32_t lane4 = (uint32_t)lane << 2;
-    const unsigned char *lut = reinterpret_cast<const unsigned char *>(sm.lut);
-    float *kaf = sm.aff[warp][0][0], *kbf = sm.aff[warp][0][1];
-    float *vaf = sm.aff[warp][1][0], *vbf = sm.aff[warp][1][1];
-    const float qmax = sm.qmax;
+    const uint32_t lut_s = smem_u32(sm.lut);
+    const uint32_t lb = (FULL ? 128u : 0u) + lane4 + (AL ? lut_s : 0u);   // this lane's table column
+    float *kaf = sm.h.aff[warp][0], *kbf = sm.h.aff[warp][1];             // K's, then V's
+    float *vaf = kaf, *vbf = kbf;
+    const float qmax = sm.h.qmax;
     bool timed_out = false;
     for (int c = warp; c < kNChunk * np; c += kWarps) {
         const int i = c >> 3, j = c & 7;
@@ -390,14 +398,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(AttnArgs a, Level
         int ge = 0;
         uint4 kc[4], kr4[4];
         {
-            const Slot<FULL> &sl = sm.slot[sK];
-            float bm = chunk_affines(sl.pm, sl.cm, j, lane, kaf, kbf);
-            const uint8_t *ca = sl.a + (j * kChunk + g) * kRow + 16 * q;
+            const SlotMeta &mt = sm.h.meta[sK];
+            float bm = chunk_affines(mt.pm, mt.cm, j, lane, kaf, kbf);
+            const uint8_t *ca = sm.plane[sK][0] + (j * kChunk + g) * kRow + 16 * q;
 #pragma unroll
             for (int nt = 0; nt < 4; ++nt)
                 kc[nt] = *reinterpret_cast<const uint4 *>(ca + nt * 8 * kRow);
             if (FULL) {
-                const uint8_t *cr = sl.r + (j * kChunk + g) * kRow + 16 * q;
+                const uint8_t *cr = sm.plane[sK][FULL ? 1 : 0] + (j * kChunk + g) * kRow + 16 * q;
 #pragma unroll
                 for (int nt = 0; nt < 4; ++nt)
                     kr4[nt] = *reinterpret_cast<const uint4 *>(cr + nt * 8 * kRow);
@@ -432,7 +440,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(AttnArgs a, Level
             uint32_t A0[4], A1[4];           // G16: hi and lo fragments; else A0 = hi rows over lo rows
 #pragma unroll
             for (int r = 0; r < R; ++r) {
-                const float4 qv = sm.qf[s][r][lane];
+                const float4 qv = sm.h.qf[s][r][lane];
                 beta2[r] = __ffma2_rn(make_float2(qv.x, qv.y), make_float2(aa.x, aa.y), beta2[r]);
                 beta2[r] = __ffma2_rn(make_float2(qv.z, qv.w), make_float2(aa.z, aa.w), beta2[r]);
                 float2 x01 = __fmul2_rn(make_float2(qv.x, qv.y), make_float2(bb.x, bb.y));
@@ -458,19 +466,19 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(AttnArgs a, Level
                     const uint32_t rw = wi == 0 ? kr4[nt].x : wi == 1 ? kr4[nt].y : wi == 2 ? kr4[nt].z : kr4[nt].w;
                     const uint32_t ev = codes_even(aw, rw), od = codes_odd(aw, rw);
                     if (s & 1) {
-                        b0 = pack_lo(lut_full<2>(lut, ev, lane4), lut_full<2>(lut, od, lane4));
-                        b1 = pack_lo(lut_full<3>(lut, ev, lane4), lut_full<3>(lut, od, lane4));
+                        b0 = pack_lo(lut_ld<AL, 2>(ev, lb, lut_s), lut_ld<AL, 2>(od, lb, lut_s));
+                        b1 = pack_lo(lut_ld<AL, 3>(ev, lb, lut_s), lut_ld<AL, 3>(od, lb, lut_s));
                     } else {
-                        b0 = pack_lo(lut_full<0>(lut, ev, lane4), lut_full<0>(lut, od, lane4));
-                        b1 = pack_lo(lut_full<1>(lut, ev, lane4), lut_full<1>(lut, od, lane4));
+                        b0 = pack_lo(lut_ld<AL, 0>(ev, lb, lut_s), lut_ld<AL, 0>(od, lb, lut_s));
+                        b1 = pack_lo(lut_ld<AL, 1>(ev, lb, lut_s), lut_ld<AL, 1>(od, lb, lut_s));
                     }
                 } else {
                     if (s & 1) {
-                        b0 = lut_anchor<2>(lut, aw, lane4);
-                        b1 = lut_anchor<3>(lut, aw, lane4);
+                        b0 = lut_ld<AL, 2>(aw, lb, lut_s);
+                        b1 = lut_ld<AL, 3>(aw, lb, lut_s);
                     } else {
-                        b0 = lut_anchor<0>(lut, aw, lane4);
-                        b1 = lut_anchor<1>(lut, aw, lane4);
+                        b0 = lut_ld<AL, 0>(aw, lb, lut_s);
+                        b1 = lut_ld<AL, 1>(aw, lb, lut_s);
                     }
                 }
                 if (s == 0)
@@ -482,75 +490,93 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(AttnArgs a, Level
             }
         }
 
-        // ---- scores (base-2 log domain), masking, online softmax ---------------
-        float beta[R];
+        // ---- scores (base-2 log domain) relative to the running reference
+        // m_run (0 before the first chunk), masking, online softmax --------
+        // The reference moves only when a score passes it by more than 2^8
+        // (weights up to 2^8 are exact in fp32 and fine in fp16), so the
+        // running output is rarely rescaled.
+        float P[R][4][2];                    // row r, n-tile nt: tokens 8 nt + 2q, + 1
+        float mref[R], mx[R], psum[R];
+        bool up = false;
 #pragma unroll
         for (int r = 0; r < R; ++r) {
             float bt = beta2[r].x + beta2[r].y;
             bt += __shfl_xor_sync(0xFFFFFFFFu, bt, 1);
             bt += __shfl_xor_sync(0xFFFFFFFFu, bt, 2);
-            beta[r] = bt;
-        }
-        float P[R][4][2];                    // row r, n-tile nt: tokens 8 nt + 2q, + 1
-        float psum[R];
-        bool rescale = false;
-        float alpha[R];
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-            float mx = neg_inf();
+            mref[r] = m_run[r] == neg_inf() ? 0.0f : m_run[r];
+            const float bm = bt - mref[r];
 #pragma unroll
             for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
                     const float acc = G16 ? S[nt][2 * r + e] : S[nt][e] + S[nt][2 + e];
-                    float v = fmaf(acc, gscale, beta[r]);
-                    if (nv < kChunk && 8 * nt + 2 * q + e >= nv)
-                        v = neg_inf();
-                    P[r][nt][e] = v;
-                    mx = fmaxf(mx, v);
+                    P[r][nt][e] = fmaf(acc, gscale, bm);
                 }
+        }
+        if (nv < kChunk) {                   // ragged chunk: tokens past the context
+#pragma unroll
+            for (int r = 0; r < R; ++r)
+#pragma unroll
+                for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e)
+                        if (8 * nt + 2 * q + e >= nv)
+                            P[r][nt][e] = neg_inf();
+        }
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            float m = fmaxf(fmaxf(fmaxf(P[r][0][0], P[r][0][1]), fmaxf(P[r][1][0], P[r][1][1])),
+                            fmaxf(fmaxf(P[r][2][0], P[r][2][1]), fmaxf(P[r][3][0], P[r][3][1])));
+            m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+            m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+            mx[r] = m;
+            up |= m_run[r] == neg_inf() || m > 8.0f;
             const int h = g + 8 * r;
             if (a.scores && h < G) {
                 float *srow = a.scores + (qrow0 + h) * score_stride + (int64_t)lp * kPage + j * kChunk;
 #pragma unroll
                 for (int nt = 0; nt < 4; ++nt)
                     *reinterpret_cast<float2 *>(srow + nt * 8 + 2 * q) =
-                        make_float2(P[r][nt][0] * kLn2, P[r][nt][1] * kLn2);
+                        make_float2((P[r][nt][0] + mref[r]) * kLn2, (P[r][nt][1] + mref[r]) * kLn2);
             }
-            mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
-            mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));
-            // the reference max moves only when a score passes it by more than
-            // 2^8 (weights up to 2^8 are exact in fp32 and fine in fp16), so
-            // the running output is rarely rescaled
-            const bool up = mx > m_run[r] + 8.0f;
-            const float m_new = up ? mx : m_run[r];
-            alpha[r] = up ? exp2_sm(m_run[r] - m_new) : 1.0f;
-            rescale |= up;
-            m_run[r] = m_new;
-            float ps = 0.0f;
-#pragma unroll
-            for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const float pv = exp2_sm(P[r][nt][e] - m_new);
-                    P[r][nt][e] = pv;
-                    ps += pv;
-                }
-            l_run[r] = fmaf(l_run[r], alpha[r], ps);
-            ps += __shfl_xor_sync(0xFFFFFFFFu, ps, 1);
-            ps += __shfl_xor_sync(0xFFFFFFFFu, ps, 2);
-            psum[r] = ps;
         }
-        if (__any_sync(0xFFFFFFFFu, rescale)) {
+        if (__any_sync(0xFFFFFFFFu, up)) {   // rare: move the reference to this chunk's maximum
 #pragma unroll
             for (int r = 0; r < R; ++r) {
-                const float2 al = make_float2(alpha[r], alpha[r]);
+                const bool first = m_run[r] == neg_inf();
+                const bool u = first || mx[r] > 8.0f;
+                const float shift = u ? mx[r] : 0.0f;
+                const float alpha = first ? 0.0f : exp2_sm(-shift);
+                m_run[r] = mref[r] + shift;
+                l_run[r] *= alpha;
+#pragma unroll
+                for (int nt = 0; nt < 4; ++nt) {
+                    P[r][nt][0] -= shift;
+                    P[r][nt][1] -= shift;
+                }
+                const float2 al = make_float2(alpha, alpha);
 #pragma unroll
                 for (int m = 0; m < 8; ++m) {
                     Olo[r][m] = __fmul2_rn(Olo[r][m], al);
                     Ohi[r][m] = __fmul2_rn(Ohi[r][m], al);
                 }
             }
+        }
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            float ps = 0.0f;
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const float pv = exp2_sm(P[r][nt][e]);
+                    P[r][nt][e] = pv;
+                    ps += pv;
+                }
+            l_run[r] += ps;
+            ps += __shfl_xor_sync(0xFFFFFFFFu, ps, 1);
+            ps += __shfl_xor_sync(0xFFFFFFFFu, ps, 2);
+            psum[r] = ps;
         }
         // P as A fragments; k-step kk = tokens 16 kk .. 16 kk + 15
         uint32_t PA0[2][4], PA1[2][4];       // G16: hi, lo; else PA0 = hi rows over lo rows
@@ -575,16 +601,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(AttnArgs a, Level
         }
         uint2 vc[2][4], vr4[2][4];           // [k-step][tokens 2q, 2q + 1, 2q + 8, 2q + 9], bytes 8g .. 8g + 7
         {
-            const Slot<FULL> &sl = sm.slot[sV];
-            chunk_affines(sl.pm, sl.cm, j, lane, vaf, vbf);
-            const uint8_t *ca = sl.a + (j * kChunk + 2 * q) * kRow + 8 * g;
+            const SlotMeta &mt = sm.h.meta[sV];
+            __syncwarp();                    // every lane is done with K's affines
+            chunk_affines(mt.pm, mt.cm, j, lane, vaf, vbf);
+            const uint8_t *ca = sm.plane[sV][0] + (j * kChunk + 2 * q) * kRow + 8 * g;
 #pragma unroll
             for (int kk = 0; kk < 2; ++kk)
 #pragma unroll
                 for (int u = 0; u < 4; ++u)
                     vc[kk][u] = *reinterpret_cast<const uint2 *>(ca + (16 * kk + (u & 1) + 8 * (u >> 1)) * kRow);
             if (FULL) {
-                const uint8_t *cr = sl.r + (j * kChunk + 2 * q) * kRow + 8 * g;
+                const uint8_t *cr = sm.plane[sV][FULL ? 1 : 0] + (j * kChunk + 2 * q) * kRow + 8 * g;
 #pragma unroll
                 for (int kk = 0; kk < 2; ++kk)
 #pragma unroll
@@ -597,6 +624,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(AttnArgs a, Level
         }
 
         // ---- P.V: n-tile 2m + e holds channel 16 n + 2m + e of column n ------
+        float4 vb4l, vb4h, va4l, va4h;       // affines of this lane's channels for m, m + 1
 #pragma unroll
         for (int m = 0; m < 8; ++m) {
             const int wi = m >> 2;
@@ -616,10 +644,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(AttnArgs a, Level
                     switch (m & 3) {
 #define LYNX_V_FULL(I)                                                                                                 \
 case I:                                                                                                            \
-    bl0 = pack_lo(lut_full<I>(lut, e0, lane4), lut_full<I>(lut, e1, lane4));                                      \
-    bl1 = pack_lo(lut_full<I>(lut, e2, lane4), lut_full<I>(lut, e3, lane4));                                      \
-    bo0 = pack_lo(lut_full<I>(lut, o0, lane4), lut_full<I>(lut, o1, lane4));                                      \
-    bo1 = pack_lo(lut_full<I>(lut, o2, lane4), lut_full<I>(lut, o3, lane4));                                      \
+    bl0 = pack_lo(lut_ld<AL, I>(e0, lb, lut_s), lut_ld<AL, I>(e1, lb, lut_s));                                      \
+    bl1 = pack_lo(lut_ld<AL, I>(e2, lb, lut_s), lut_ld<AL, I>(e3, lb, lut_s));                                      \
+    bo0 = pack_lo(lut_ld<AL, I>(o0, lb, lut_s), lut_ld<AL, I>(o1, lb, lut_s));                                      \
+    bo1 = pack_lo(lut_ld<AL, I>(o2, lb, lut_s), lut_ld<AL, I>(o3, lb, lut_s));                                      \
     break;
                         LYNX_V_FULL(0)
                         LYNX_V_FULL(1)
@@ -634,10 +662,10 @@ case I:                                                                         
                     switch (m & 3) {
 #define LYNX_V_ANCHOR(I)                                                                                               \
 case I:                                                                                                            \
-    bl0 = lut_anchor<I>(lut, e01, lane4);                                                                          \
-    bl1 = lut_anchor<I>(lut, e23, lane4);                                                                          \
-    bo0 = lut_anchor<I>(lut, o01, lane4);                                                                          \
-    bo1 = lut_anchor<I>(lut, o23, lane4);                                                                          \
+    bl0 = lut_ld<AL, I>(e01, lb, lut_s);                                                                          \
+    bl1 = lut_ld<AL, I>(e23, lb, lut_s);                                                                          \
+    bo0 = lut_ld<AL, I>(o01, lb, lut_s);                                                                          \
+    bo1 = lut_ld<AL, I>(o23, lb, lut_s);                                                                          \
     break;
                         LYNX_V_ANCHOR(0)
                         LYNX_V_ANCHOR(1)
@@ -661,10 +689,16 @@ case I:                                                                         
             }
             // o += b (P.L) + a sum(P): column 2q -> channels 32q + 2m, + 1;
             // column 2q + 1 -> channels 32q + 16 + 2m, + 1
-            const float2 bl = *reinterpret_cast<const float2 *>(vbf + 36 * q + 2 * m);
-            const float2 bh = *reinterpret_cast<const float2 *>(vbf + 36 * q + 16 + 2 * m);
-            const float2 al = *reinterpret_cast<const float2 *>(vaf + 36 * q + 2 * m);
-            const float2 ah = *reinterpret_cast<const float2 *>(vaf + 36 * q + 16 + 2 * m);
+            if ((m & 1) == 0) {
+                vb4l = *reinterpret_cast<const float4 *>(vbf + 36 * q + 2 * m);
+                vb4h = *reinterpret_cast<const float4 *>(vbf + 36 * q + 16 + 2 * m);
+                va4l = *reinterpret_cast<const float4 *>(vaf + 36 * q + 2 * m);
+                va4h = *reinterpret_cast<const float4 *>(vaf + 36 * q + 16 + 2 * m);
+            }
+            const float2 bl = (m & 1) ? make_float2(vb4l.z, vb4l.w) : make_float2(vb4l.x, vb4l.y);
+            const float2 bh = (m & 1) ? make_float2(vb4h.z, vb4h.w) : make_float2(vb4h.x, vb4h.y);
+            const float2 al = (m & 1) ? make_float2(va4l.z, va4l.w) : make_float2(va4l.x, va4l.y);
+            const float2 ah = (m & 1) ? make_float2(va4h.z, va4h.w) : make_float2(va4h.x, va4h.y);
 #pragma unroll
             for (int r = 0; r < R; ++r) {
                 float2 cl, ch;
@@ -689,15 +723,15 @@ case I:                                                                         
         // (after a timeout some may still be in flight; bounded)
         bool ok = true;
         for (int s = 0; s < NS; ++s)
-            if (sm.last[s] >= 0 && !mbar_wait_bounded(&sm.full_bar[s], (uint32_t)((sm.last[s] / NS) & 1), kWaitLimit))
+            if (sm.h.last[s] >= 0 && !mbar_wait_bounded(&sm.h.full_bar[s], (uint32_t)((sm.h.last[s] / NS) & 1), kWaitLimit))
                 ok = false;
         if (!ok && a.dev_err)
             atomicOr(a.dev_err, LYNX_DEVERR_TIMEOUT);
     }
 
     // ---- merge the chunks' states, write this range's partial ------------
-    __syncthreads();   // every copy has landed and every slot read is done: the merge area overlays the slots
-    Merge &mg = *reinterpret_cast<Merge *>(sm.slot);
+    __syncthreads();   // every copy has landed and every table and plane read is done: the merge area overlays them
+    Merge &mg = *reinterpret_cast<Merge *>(sm.lut);
     {
         const int j = warp;
 #pragma unroll
@@ -742,29 +776,68 @@ case I:                                                                         
     }
 }
 
-template <bool G16, bool FULL, int NS>
+template <bool G16, bool FULL, int NS, bool AL>
 cudaError_t run(const AttnArgs &a, cudaStream_t s)
 {
-    static_assert(sizeof(Merge) <= sizeof(Slot<FULL>) * NS, "merge area overlays the slots");
+    static_assert(sizeof(Head<NS>) <= kPre, "everything ahead of the table fits below 0x10000");
+    static_assert(sizeof(Merge) <= sizeof(uint32_t) * 256 * 64 + NS * (FULL ? 2 : 1) * kPlane,
+                  "merge area overlays the table and the planes");
     static_assert(sizeof(Smem<FULL, NS>) <= 227 * 1024, "shared memory per CTA");
     const size_t smem = sizeof(Smem<FULL, NS>);
-    cudaError_t e = cudaFuncSetAttribute(attn_mma_kernel<G16, FULL, NS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(attn_mma_kernel<G16, FULL, NS, AL>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess)
         return e;
     dim3 grid((unsigned)a.n_splits, (unsigned)a.H, (unsigned)a.B);
-    attn_mma_kernel<G16, FULL, NS><<<grid, kThreads, smem, s>>>(a, host_tables().lev);
+    attn_mma_kernel<G16, FULL, NS, AL><<<grid, kThreads, smem, s>>>(a, host_tables().lev);
     return cudaGetLastError();
+}
+
+template <bool G16, bool FULL, int NS>
+cudaError_t run_aligned_or_not(const AttnArgs &a, cudaStream_t s, bool al)
+{
+    return al ? run<G16, FULL, NS, true>(a, s) : run<G16, FULL, NS, false>(a, s);
+}
+
+__device__ uint32_t g_dyn_base;
+
+__global__ void dyn_base_probe()
+{
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    g_dyn_base = smem_u32(smem_raw);
+}
+
+// Whether the dynamic shared window of this device starts at kDynBase, so
+// that the attention kernel's level table sits at shared address 0x10000.
+// Measured by a one-thread kernel at the first call on each device (a
+// synchronous step: that first call must not be inside a stream capture).
+bool table_aligned()
+{
+    static std::mutex mu;
+    static int state[64] = {};   // 0 unknown, 1 aligned, 2 not
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return false;
+    std::lock_guard<std::mutex> lock(mu);
+    if (state[dev] == 0) {
+        uint32_t base = 0;
+        dyn_base_probe<<<1, 1, 16>>>();
+        const bool ok = cudaGetLastError() == cudaSuccess &&
+                        cudaMemcpyFromSymbol(&base, g_dyn_base, sizeof(base)) == cudaSuccess;
+        state[dev] = ok && base == kDynBase ? 1 : 2;
+    }
+    return state[dev] == 1;
 }
 
 } // namespace
 
 cudaError_t launch_attn_mma(const AttnArgs &a, cudaStream_t s)
 {
-    // slots hold one tensor's page: 21 KiB in anchor mode, 37 KiB in full mode
+    // slots hold one tensor's page: 16 KiB of codes in anchor mode, 32 KiB in full mode
+    const bool al = table_aligned();
     if (a.G <= 8)
-        return a.full ? run<false, true, 3>(a, s) : run<false, false, 6>(a, s);
-    return a.full ? run<true, true, 3>(a, s) : run<true, false, 6>(a, s);
+        return a.full ? run_aligned_or_not<false, true, 3>(a, s, al) : run_aligned_or_not<false, false, 6>(a, s, al);
+    return a.full ? run_aligned_or_not<true, true, 3>(a, s, al) : run_aligned_or_not<true, false, 6>(a, s, al);
 }
 
 } // namespace lynx
