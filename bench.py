@@ -404,6 +404,84 @@ def progressive_arrival(torch, lx, w=None, top=32, keep=False):
     return result
 
 
+def append_report(args):
+    """Quantize-on-append at the batched-decode workload's shape on the 94-layer
+    model: the growing last page of each of 32 requests (ragged contexts,
+    seeded physical pages) re-encoded for 94 layers x 8 KV heads per step
+    (24,064 pages), one lynx_quantize_append call per tensor. Algorithmic bytes
+    are the encoder's 3.15625 B per element. The oracle is timed on a sample of
+    the same tails beside it."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    import progressive_kv_cache_gb300 as lx
+
+    w = S.WORKLOADS[4]
+    L, H, n = W3.L, w.H, w.B
+    ctx, pool, table = S.batched_layout(w)
+    last = (ctx - 1) // 256
+    phys = torch.from_numpy(table[np.arange(n), last].astype(np.int32)).cuda()
+    valid = torch.from_numpy((ctx - 256 * last).astype(np.int32)).cuda()
+
+    cpu = None
+    if not args.no_cpu_baseline:
+        import oracle as orc
+        orc.build()
+        sc = S.channel_scales(w.seed, S.S_K, 1, H, n_outliers=w.n_outliers, factor_log10=w.factor_log10)
+        xs = S.laplace_bf16(w.key(S.S_K), sc, 1, H, 8 * 256)          # 64 sample tails
+        pv = np.resize(valid.cpu().numpy(), 8)
+        orc.quantize(xs, pv)
+        t0 = time.perf_counter()
+        reps = 0
+        while time.perf_counter() - t0 < 10.0:
+            orc.quantize(xs, pv)
+            reps += 1
+        dt = time.perf_counter() - t0
+        cpu = {"value": reps * xs.size * B_QUANT / dt / 1e9, "unit": "GB/s", "cores": orc.num_threads(),
+               "kind": "oracle", "sample": f"{H * 8} tail pages (8 KV heads x 8 tails), {reps} passes, {dt:.1f} s"}
+
+    dev = torch.device("cuda")
+    gen = S.DeviceGenerator()
+    tails, qkv = {}, {}
+    for s in (S.S_K, S.S_V):
+        x = torch.empty((n, L, H, 256, D), dtype=torch.bfloat16, device=dev)
+        sc = S.channel_scales(w.seed, s, n * L, H, n_outliers=w.n_outliers, factor_log10=w.factor_log10)
+        gen.fill(x.view(n * L, H, 256, D), w.key(s), sc)
+        tails[s] = x
+        qkv[s] = lx.QuantizedKV.empty(L, H, pool * 256, dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def step():
+        for s in (S.S_K, S.S_V):
+            lx.quantize_append(tails[s], phys, valid, qkv[s], dev_err=err)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(0) as clk:
+        e0.record()
+        for _ in range(args.steps):
+            step()
+        e1.record()
+        torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    if int(err.item()) != 0:
+        raise RuntimeError("lynx_quantize_append flagged a page")
+    nbytes = 2 * n * L * H * 256 * D * B_QUANT
+    hbm, peak_kind = peaks()
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    line = {"report": "append", "metric": "quantize-on-append HBM GB/s vs HBM roofline (1 GB300)", "value": gbs,
+            "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms,
+            "higher_is_better": True, "dtype": "bf16 in, 4+4-bit planes", "data": "synthetic",
+            "config": {"workload": f"{w.name} tails on the 94-layer model", "requests": n, "layers": L,
+                       "kv_heads": H, "pages_per_step": 2 * n * L * H, "l2": "inputs larger than L2, no flush"},
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
+                         "peak_kind": peak_kind, "traffic": None},
+            "cpu_baseline": cpu, "gpu_launches": 2 * args.steps, "clocks": clk.summary()}
+    print(json.dumps(line))
+
+
 def run_gpu(args):
     import torch
     import torch.distributed as dist
@@ -565,8 +643,9 @@ def main():
                                        "decode_attn_full"], default=None,
                     help="time one kernel group only (for profiler captures on smaller cases)")
     ap.add_argument("--layers", type=int, default=None, help="layers of the cache (default: all 94)")
-    ap.add_argument("--report", choices=["progressive"], default=None,
-                    help="progressive: residual layers arriving one by one (8 layers, 64K tokens)")
+    ap.add_argument("--report", choices=["progressive", "append"], default=None,
+                    help="progressive: residual layers arriving one by one (8 layers, 64K tokens); "
+                         "append: quantize-on-append of 32 requests' tail pages over 94 layers x 8 KV heads")
     ap.add_argument("--no-graph", action="store_true",
                     help="issue every library call from Python instead of replaying CUDA graphs of them")
     args = ap.parse_args()
@@ -580,6 +659,8 @@ def main():
         __graft_entry__.build()
         import progressive_kv_cache_gb300 as lx
         print(json.dumps(progressive_arrival(torch, lx)))
+    elif args.report == "append":
+        append_report(args)
     else:
         run_gpu(args)
 

@@ -67,7 +67,7 @@ typedef enum {
 typedef enum { LYNX_OUT_BF16 = 0, LYNX_OUT_F32 = 1 } lynx_out_dtype;
 typedef enum { LYNX_MODE_ANCHOR = 0, LYNX_MODE_FULL = 1 } lynx_mode;
 
-/* Device-error bits written (OR-ed) into *dev_err by lynx_decode_attn. */
+/* Device-error bits written (OR-ed) into *dev_err by lynx_decode_attn and lynx_quantize_append. */
 #define LYNX_DEVERR_PAGE 1u   /* a page-table entry outside [0, tokens/256) */
 #define LYNX_DEVERR_CTX 2u    /* a context length outside [0, max_pages*256] */
 #define LYNX_DEVERR_TIMEOUT 4u /* a bulk copy did not complete within the kernel's wait limit */
@@ -107,6 +107,27 @@ typedef struct {
  */
 lynx_status lynx_quantize_pages(const void *x_bf16, const int32_t *page_valid, const lynx_qkv *out,
                                 void *stream);
+
+/*
+ * Quantize-on-append for the decode tail. The explainer's "Top row" compresses
+ * each token's K and V as they are produced (quantize-on-write); the Lynx
+ * encoder works on whole 256-token pages (section 3), so a page that is still
+ * growing is re-encoded whole from its bf16 staging copy each time tokens are
+ * added. This call does that for n tails at once: tail i is encoded into
+ * physical page phys_page[i] of every layer and KV head of `out`, with
+ * valid[i] valid tokens (statistics over those tokens only; the others store
+ * code 0), exactly as lynx_quantize_pages encodes a page with that count.
+ *   tail_bf16  device, [n][layers][kv_heads][256][128] bf16
+ *   phys_page  device, [n] int32 destination pages in [0, tokens/256); an
+ *              entry outside is skipped and sets LYNX_DEVERR_PAGE in *dev_err
+ *   valid      device, [n] int32 valid-token counts (clamped to 0..256)
+ *   out        the pool: planes and metadata of every layer and KV head
+ *              (residual non-NULL); only the destination pages are written
+ *   dev_err    device or NULL, one uint32
+ * Tails naming the same physical page race on it: pass distinct pages.
+ */
+lynx_status lynx_quantize_append(const void *tail_bf16, const int32_t *phys_page, const int32_t *valid,
+                                 int32_t n, const lynx_qkv *out, uint32_t *dev_err, void *stream);
 
 /*
  * Anchor-only reconstruction, the draft cache of section 4 (decoding begins

@@ -60,6 +60,7 @@ def _lib():
             L.lynx_status_string.argtypes = [ctypes.c_int]
             L.lynx_status_string.restype = ctypes.c_char_p
             L.lynx_quantize_pages.argtypes = [vp, vp, ctypes.POINTER(LynxQKV), vp]
+            L.lynx_quantize_append.argtypes = [vp, vp, vp, i32, ctypes.POINTER(LynxQKV), vp, vp]
             L.lynx_dequant_anchor.argtypes = [ctypes.POINTER(LynxQKV), vp, ctypes.c_int, vp]
             L.lynx_refine_residual.argtypes = [ctypes.POINTER(LynxQKV), vp, ctypes.c_int, vp]
             L.lynx_decode_attn_workspace.argtypes = [i32, i32, i32]
@@ -74,7 +75,7 @@ def _lib():
             L.lynx_host_tables.argtypes = [vp, vp]
             L.lynx_host_tables.restype = None
             L.lynx_level_codes.argtypes = [vp, i64, vp, vp]
-            for f in ("lynx_quantize_pages", "lynx_dequant_anchor", "lynx_refine_residual",
+            for f in ("lynx_quantize_pages", "lynx_quantize_append", "lynx_dequant_anchor", "lynx_refine_residual",
                       "lynx_decode_attn", "lynx_level_codes"):
                 getattr(L, f).restype = ctypes.c_int
             _L = L
@@ -163,6 +164,24 @@ def quantize_pages(x, out: QuantizedKV, page_valid=None, stream=None):
     d = out.desc()
     _check(_lib().lynx_quantize_pages(_ptr(x), _ptr(page_valid), ctypes.byref(d), _stream(stream)),
            "lynx_quantize_pages")
+    return out
+
+
+def quantize_append(tail, phys_page, valid, out: QuantizedKV, dev_err=None, stream=None):
+    """lynx_quantize_append: re-encode bf16 tails [n, L, H, 256, 128] into
+    physical pages phys_page[n] of every layer and KV head of `out`."""
+    _dev(tail, torch.bfloat16, "tail")
+    _dev(phys_page, torch.int32, "phys_page")
+    _dev(valid, torch.int32, "valid")
+    if dev_err is not None:
+        _dev(dev_err, torch.int32, "dev_err")
+    n = phys_page.numel()
+    L, H, _ = out.shape
+    if valid.numel() != n or tuple(tail.shape) != (n, L, H, PAGE, HEAD_DIM):
+        raise ValueError("tail must be [n, L, H, 256, 128] with n = len(phys_page) = len(valid)")
+    d = out.desc()
+    _check(_lib().lynx_quantize_append(_ptr(tail), _ptr(phys_page), _ptr(valid), n, ctypes.byref(d),
+                                       _ptr(dev_err), _stream(stream)), "lynx_quantize_append")
     return out
 
 

@@ -1,6 +1,7 @@
 // lynx_abi.cu -- the extern "C" entry points declared in include/lynx.h:
 // argument checks on the host, then one launch sequence per call. Nothing is
 // allocated here; every buffer belongs to the caller.
+#include <cstdint>
 #include <cstring>
 
 #include "lynx_internal.cuh"
@@ -64,6 +65,24 @@ lynx_status lynx_quantize_pages(const void *x_bf16, const int32_t *page_valid, c
     if (!aligned(x_bf16, 16) || (page_valid && !aligned(page_valid, 4)))
         return LYNX_ERR_ALIGN;
     return from_cuda(launch_quantize(static_cast<const uint16_t *>(x_bf16), page_valid, *out, (cudaStream_t)stream));
+}
+
+lynx_status lynx_quantize_append(const void *tail_bf16, const int32_t *phys_page, const int32_t *valid,
+                                 int32_t n, const lynx_qkv *out, uint32_t *dev_err, void *stream)
+{
+    lynx_status st = check_qkv(out, true);
+    if (st != LYNX_OK)
+        return st;
+    if (n < 0 || (int64_t)out->layers * out->kv_heads > INT32_MAX)
+        return LYNX_ERR_SHAPE;
+    if (n == 0 || out->layers == 0 || out->kv_heads == 0)
+        return LYNX_OK;
+    if (!tail_bf16 || !phys_page || !valid)
+        return LYNX_ERR_NULL;
+    if (!aligned(tail_bf16, 16) || !aligned(phys_page, 4) || !aligned(valid, 4) || (dev_err && !aligned(dev_err, 4)))
+        return LYNX_ERR_ALIGN;
+    return from_cuda(launch_quantize_append(static_cast<const uint16_t *>(tail_bf16), phys_page, valid, n, *out,
+                                            dev_err, (cudaStream_t)stream));
 }
 
 lynx_status lynx_dequant_anchor(const lynx_qkv *in, void *out, lynx_out_dtype dt, void *stream)

@@ -65,6 +65,8 @@ int device_sm_count();             // SM count of the current device (cached per
 // ---- launchers (one per translation unit) -------------------------------
 cudaError_t launch_quantize(const uint16_t *x, const int32_t *page_valid, const lynx_qkv &o,
                             cudaStream_t s);
+cudaError_t launch_quantize_append(const uint16_t *tail, const int32_t *dst_page, const int32_t *valid, int n,
+                                   const lynx_qkv &o, uint32_t *dev_err, cudaStream_t s);
 cudaError_t launch_level_codes(const float *w, int64_t n, int8_t *codes, cudaStream_t s);
 cudaError_t launch_dequant(const lynx_qkv &in, void *out, bool full, bool f32, cudaStream_t s);
 

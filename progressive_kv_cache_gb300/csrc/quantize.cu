@@ -58,14 +58,37 @@ struct Smem {
 };
 
 struct Params {
-    const uint16_t *x;
+    const uint16_t *x;            // source pages, one after another
     const int32_t *page_valid;
     uint8_t *anc, *res;
     float *pm;
     uint16_t *cm;
-    int64_t pages;  // L * H * P
-    int P;          // pages per (layer, head)
+    int64_t pages;                // source pages: L * H * P, or n * L * H when appending
+    int P;                        // pages per (layer, head) of the destination
+    // appending: source page i = (tail i / LH, layer-head i % LH) is encoded
+    // into physical page dst_page[i / LH] of that layer-head, with
+    // tail_valid[i / LH] valid tokens; NULL for the whole-tensor encoder
+    const int32_t *dst_page;
+    const int32_t *tail_valid;
+    int LH;
+    uint32_t *dev_err;
 };
+
+// Destination page of source page i (-1: outside the pool, flagged).
+__device__ __forceinline__ int64_t dst_of(const Params &p, int64_t i)
+{
+    if (!p.dst_page)
+        return i;
+    const int d = p.dst_page[i / p.LH];
+    return (d >= 0 && d < p.P) ? (i % p.LH) * (int64_t)p.P + d : -1;
+}
+
+// Valid tokens of source page i (clamped to 0..256).
+__device__ __forceinline__ int valid_of(const Params &p, int64_t i)
+{
+    const int n = p.dst_page ? p.tail_valid[i / p.LH] : (p.page_valid ? p.page_valid[i % p.P] : kPage);
+    return min(max(n, 0), kPage);
+}
 
 __device__ __forceinline__ uint2 lds_u2(uint32_t addr)
 {
@@ -228,8 +251,10 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_kernel(Params p, CodeTab
             break;
         }
 
-        int n = p.page_valid ? p.page_valid[page % p.P] : kPage;
-        n = min(max(n, 0), kPage);
+        const int n = valid_of(p, page);
+        const int64_t dst = dst_of(p, page);
+        if (dst < 0 && p.dev_err && tid == 0)
+            atomicOr(p.dev_err, LYNX_DEVERR_PAGE);
         const int nc = min(max(n - j * kChunk, 0), kChunk);
 
         // (a) this thread's 32 tokens x 2 channels, and their chunk min/max
@@ -323,21 +348,21 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_kernel(Params p, CodeTab
         }
 
         // metadata: page (min, range) from chunk 0's warps; chunk (mean, scale) from every thread
-        if (j == 0) {
-            float *pm = p.pm + page * (int64_t)(2 * kD) + 2 * pi;
+        if (j == 0 && dst >= 0) {
+            float *pm = p.pm + dst * (int64_t)(2 * kD) + 2 * pi;
             *reinterpret_cast<float2 *>(pm) = make_float2(mn0, mn1);
             *reinterpret_cast<float2 *>(pm + kD) = make_float2(rg0, rg1);
         }
-        {
-            uint16_t *cm = p.cm + (page * kNChunk + j) * (int64_t)(2 * kD) + 2 * pi;
+        if (dst >= 0) {
+            uint16_t *cm = p.cm + (dst * kNChunk + j) * (int64_t)(2 * kD) + 2 * pi;
             *reinterpret_cast<uint32_t *>(cm) = mu2;
             *reinterpret_cast<uint32_t *>(cm + kD) = s2;
         }
         __syncthreads();
-        if (tid == 0) {
+        if (tid == 0 && dst >= 0) {
             fence_proxy_async_smem();
-            bulk_s2g(p.anc + page * (int64_t)kPlaneBytes, sm.anc, kPlaneBytes);
-            bulk_s2g(p.res + page * (int64_t)kPlaneBytes, sm.res, kPlaneBytes);
+            bulk_s2g(p.anc + dst * (int64_t)kPlaneBytes, sm.anc, kPlaneBytes);
+            bulk_s2g(p.res + dst * (int64_t)kPlaneBytes, sm.res, kPlaneBytes);
             bulk_commit();
         }
     }
@@ -364,13 +389,9 @@ __global__ void level_codes_kernel(const float *__restrict__ w, int64_t n, int8_
     }
 }
 
-} // namespace
-
-cudaError_t launch_quantize(const uint16_t *x, const int32_t *page_valid, const lynx_qkv &o, cudaStream_t s)
+cudaError_t run_quantize(const Params &p, cudaStream_t s)
 {
-    const int P = o.tokens / kPage;
-    const int64_t pages = (int64_t)o.layers * o.kv_heads * P;
-    if (pages == 0)
+    if (p.pages == 0)
         return cudaSuccess;
     const int sms = device_sm_count();
     if (sms <= 0)
@@ -379,10 +400,28 @@ cudaError_t launch_quantize(const uint16_t *x, const int32_t *page_valid, const 
     cudaError_t e = cudaFuncSetAttribute(quantize_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess)
         return e;
-    Params p{x, page_valid, o.anchor, o.residual, o.page_meta, o.chunk_meta, pages, P};
-    const int64_t grid = pages < sms ? pages : sms;
+    const int64_t grid = p.pages < sms ? p.pages : sms;
     quantize_kernel<<<(unsigned)grid, kThreads, smem, s>>>(p, host_tables().code);
     return cudaGetLastError();
+}
+
+} // namespace
+
+cudaError_t launch_quantize(const uint16_t *x, const int32_t *page_valid, const lynx_qkv &o, cudaStream_t s)
+{
+    const int P = o.tokens / kPage;
+    Params p{x, page_valid, o.anchor, o.residual, o.page_meta, o.chunk_meta,
+             (int64_t)o.layers * o.kv_heads * P, P, nullptr, nullptr, 1, nullptr};
+    return run_quantize(p, s);
+}
+
+cudaError_t launch_quantize_append(const uint16_t *tail, const int32_t *dst_page, const int32_t *valid, int n,
+                                   const lynx_qkv &o, uint32_t *dev_err, cudaStream_t s)
+{
+    const int LH = o.layers * o.kv_heads;
+    Params p{tail, nullptr, o.anchor, o.residual, o.page_meta, o.chunk_meta,
+             (int64_t)n * LH, o.tokens / kPage, dst_page, valid, LH > 0 ? LH : 1, dev_err};
+    return run_quantize(p, s);
 }
 
 cudaError_t launch_level_codes(const float *w, int64_t n, int8_t *codes, cudaStream_t s)

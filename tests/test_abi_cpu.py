@@ -127,3 +127,24 @@ def test_level_codes_rejects_bad_arguments(lx):
     assert lib.lynx_level_codes(None, 10, None, None) == lx.ERR_NULL
     assert lib.lynx_level_codes(None, -1, None, None) == lx.ERR_SHAPE
     assert lib.lynx_level_codes(None, 0, None, None) == lx.OK
+
+
+def test_quantize_append_rejects_bad_arguments(lx):
+    lib = lx.library()
+
+    def call(d, tail=0x400000, pp=0x500000, va=0x500100, n=2, err=None):
+        return lib.lynx_quantize_append(ctypes.c_void_p(tail) if tail else None,
+                                        ctypes.c_void_p(pp) if pp else None,
+                                        ctypes.c_void_p(va) if va else None, n, ctypes.byref(d),
+                                        ctypes.c_void_p(err) if err else None, None)
+
+    assert call(_qkv(lx), tail=0) == lx.ERR_NULL
+    assert call(_qkv(lx), pp=0) == lx.ERR_NULL
+    assert call(_qkv(lx), va=0) == lx.ERR_NULL
+    assert call(_qkv(lx, residual=False)) == lx.ERR_NULL
+    assert call(_qkv(lx), n=-1) == lx.ERR_SHAPE
+    assert call(_qkv(lx, T=300)) == lx.ERR_SHAPE
+    assert call(_qkv(lx), tail=0x400008) == lx.ERR_ALIGN
+    assert call(_qkv(lx), pp=0x500002) == lx.ERR_ALIGN
+    assert call(_qkv(lx), err=0x600001) == lx.ERR_ALIGN
+    assert call(_qkv(lx), n=0) == lx.OK                       # nothing to do, no launch
