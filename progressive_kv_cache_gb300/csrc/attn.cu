@@ -257,6 +257,10 @@ __global__ void __launch_bounds__(kD) attn_combine_kernel(const float *__restric
 {
     extern __shared__ float wgt[];   // [n_splits]
     __shared__ float red[kD / 32];
+    // launched as a programmatic dependent of the split kernel: everything
+    // above this point overlaps its tail; the partials are read only after it
+    // has completed and its writes are visible
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int64_t bh = blockIdx.x;
     const int d = threadIdx.x, lane = d & 31, warp = d >> 5;
     const float *pp = part + bh * n_splits * kPart;
@@ -363,9 +367,19 @@ size_t attn_workspace_bytes(int batch, int q_heads, int n_splits)
 
 cudaError_t launch_attn_combine(const AttnArgs &a, cudaStream_t s)
 {
-    attn_combine_kernel<<<(unsigned)(a.B * a.Hq), kD, (size_t)a.n_splits * sizeof(float), s>>>(a.part, a.n_splits,
-                                                                                               a.out);
-    return cudaGetLastError();
+    // programmatic dependent launch: the combine is scheduled while the split
+    // kernel's last CTAs finish and waits for their results on the device
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(a.B * a.Hq));
+    cfg.blockDim = dim3(kD);
+    cfg.dynamicSmemBytes = (size_t)a.n_splits * sizeof(float);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, attn_combine_kernel, (const float *)a.part, a.n_splits, a.out);
 }
 
 cudaError_t launch_decode_attn(const AttnArgs &a, cudaStream_t s)

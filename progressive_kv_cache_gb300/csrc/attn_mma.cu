@@ -729,6 +729,10 @@ case I:                                                                         
             atomicOr(a.dev_err, LYNX_DEVERR_TIMEOUT);
     }
 
+    // the combine kernel that follows may be scheduled now (it waits for
+    // this grid's completion before reading the partials)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
     // ---- merge the chunks' states, write this range's partial ------------
     __syncthreads();   // every copy has landed and every table and plane read is done: the merge area overlays them
     Merge &mg = *reinterpret_cast<Merge *>(sm.lut);
