@@ -482,6 +482,61 @@ def append_report(args):
     print(json.dumps(line))
 
 
+def split_stream_report(args):
+    """Split-stream arrival (Lynx section 4) emulated on one GPU at the
+    progressive-arrival workload's shape (8 layers x 8 KV heads x 64K tokens, 8
+    requests sharing the context, 64 query heads): anchors and metadata cross
+    an emulated link first (high-priority stream), residuals after
+    (low-priority stream); each layer is decoded in anchor mode as soon as its
+    anchors are in and in full mode once its residuals are in. Compared with
+    the sequential baseline (whole cache, then full decode), unpaced and with
+    the link paced to 400 and 100 Gb/s."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    import progressive_kv_cache_gb300 as lx
+    from progressive_kv_cache_gb300 import split_stream as ss
+
+    w = S.WORKLOADS[5]
+    L, H, T, B, Hq = w.L, w.H, w.T, w.B, w.Hq
+    dev = torch.device("cuda")
+    gen = S.DeviceGenerator()
+    src = {}
+    x = torch.empty((L, H, T, D), dtype=torch.bfloat16, device=dev)
+    for s in (S.S_K, S.S_V):
+        gen.fill(x, w.key(s), w.scales(s))
+        src[s] = lx.QuantizedKV.empty(L, H, T, dev)
+        lx.quantize_pages(x, src[s])
+    del x
+    host = {s: ss.pinned_copy(src[s]) for s in src}
+    dst = {s: lx.QuantizedKV.empty(L, H, T, dev) for s in src}
+    qt = torch.from_numpy(w.queries_bf16().view(np.int16)).to(dev).view(torch.bfloat16)
+    table = torch.arange(T // 256, dtype=torch.int32, device=dev)[None, :].repeat(B, 1).contiguous()
+    ctx = torch.full((B,), T, dtype=torch.int32, device=dev)
+    sm = D ** -0.5
+    lx.decode_attn(qt, src[S.S_K], src[S.S_V], 0, table, ctx, sm, lx.MODE_FULL)   # first call: set-up
+    torch.cuda.synchronize()
+    a_bytes = sum(t.numel() * t.element_size() for q in src.values() for t in (q.anchor, q.page_meta, q.chunk_meta))
+    r_bytes = sum(q.residual.numel() for q in src.values())
+    runs = []
+    for gbps in (None, 400.0, 100.0):
+        best = None
+        for _ in range(2 if gbps is not None else 4):
+            _, _, t = ss.split_stream_decode(host[S.S_K], host[S.S_V], dst[S.S_K], dst[S.S_V], qt, table, ctx, sm,
+                                             link_gbps=gbps, order=S.arrival_order(w))
+            _, seq_ms = ss.sequential_decode(host[S.S_K], host[S.S_V], dst[S.S_K], dst[S.S_V], qt, table, ctx, sm,
+                                             link_gbps=gbps)
+            if best is None or t["anchor_decode_done"] < best[0]["anchor_decode_done"]:
+                best = (t, seq_ms)
+        t, seq_ms = best
+        runs.append({"link_gbps": gbps, "ms": t, "sequential_ms": seq_ms,
+                     "first_decode_speedup": seq_ms / t["anchor_decode_done"],
+                     "full_decode_vs_sequential": t["full_decode_done"] / seq_ms})
+    print(json.dumps({"report": "split-stream", "workload": w.name, "layers": L, "kv_heads": H, "tokens": T,
+                      "batch": B, "q_heads": Hq, "anchor_bytes": a_bytes, "residual_bytes": r_bytes,
+                      "runs": runs}))
+
+
 def run_gpu(args):
     import torch
     import torch.distributed as dist
@@ -643,9 +698,10 @@ def main():
                                        "decode_attn_full"], default=None,
                     help="time one kernel group only (for profiler captures on smaller cases)")
     ap.add_argument("--layers", type=int, default=None, help="layers of the cache (default: all 94)")
-    ap.add_argument("--report", choices=["progressive", "append"], default=None,
+    ap.add_argument("--report", choices=["progressive", "append", "split-stream"], default=None,
                     help="progressive: residual layers arriving one by one (8 layers, 64K tokens); "
-                         "append: quantize-on-append of 32 requests' tail pages over 94 layers x 8 KV heads")
+                         "append: quantize-on-append of 32 requests' tail pages over 94 layers x 8 KV heads; "
+                         "split-stream: anchors then residuals over an emulated link, decode on anchors first")
     ap.add_argument("--no-graph", action="store_true",
                     help="issue every library call from Python instead of replaying CUDA graphs of them")
     args = ap.parse_args()
@@ -661,6 +717,8 @@ def main():
         print(json.dumps(progressive_arrival(torch, lx)))
     elif args.report == "append":
         append_report(args)
+    elif args.report == "split-stream":
+        split_stream_report(args)
     else:
         run_gpu(args)
 
