@@ -209,6 +209,36 @@ lynx_status lynx_decode_attn_noalloc(const void *q_bf16, const lynx_qkv *k, cons
                                      int32_t q_heads, int32_t max_pages, float sm_scale, lynx_mode mode,
                                      float *out, float *scores, uint32_t *dev_err, void *stream);
 
+/*
+ * Workspace bytes lynx_verify_attn needs for this shape on the current device
+ * (split-K partials of every draft position). Returns 0 for invalid sizes.
+ */
+size_t lynx_verify_attn_workspace(int32_t batch, int32_t draft, int32_t q_heads, int32_t max_pages);
+
+/*
+ * Multi-token verify attention over one layer of the quantized paged cache.
+ * Section 4 of the Lynx reading drafts tokens on the anchor-only cache and,
+ * once the residuals have refined it, verifies the drafted positions against
+ * the full cache; this is the attention of that verify pass: `draft` query
+ * positions per request (at most 64), the last `draft` tokens of each context
+ * being the drafted ones, causal within the block:
+ *   out[b][i][h] = sum_{t < n_bi} softmax_t(sm_scale * q[b][i][h] . K[t]) V[t],
+ *   n_bi = ctx_lens[b] - draft + i + 1  (rows with n_bi <= 0 give zeros),
+ * with K, V, the page table and GQA mapping as in lynx_decode_attn (FULL:
+ * the refined reconstruction; ANCHOR: the draft one). The cache is decoded on
+ * chip into fp16 hi/lo tiles and multiplied on the tensor cores with three
+ * products per pair, keeping fp32-level accuracy; reconstructed values must
+ * lie inside the fp16 range (|x| < 65504).
+ *   q_bf16      device, [batch][draft][q_heads][128] bf16
+ *   out         device, [batch][draft][q_heads][128] fp32
+ *   workspace   device, ws_bytes >= lynx_verify_attn_workspace(batch, draft, q_heads, max_pages)
+ *   dev_err     device or NULL, one uint32 (LYNX_DEVERR_* bits OR-ed in)
+ */
+lynx_status lynx_verify_attn(const void *q_bf16, const lynx_qkv *k, const lynx_qkv *v, int32_t layer,
+                             const int32_t *page_table, const int32_t *ctx_lens, int32_t batch, int32_t draft,
+                             int32_t q_heads, int32_t max_pages, float sm_scale, lynx_mode mode, float *out,
+                             void *workspace, size_t ws_bytes, uint32_t *dev_err, void *stream);
+
 /* Human-readable name of a status. Never NULL. */
 const char *lynx_status_string(lynx_status s);
 

@@ -192,6 +192,25 @@ def decode_attn(q_bf16, k: Quantized, v: Quantized, layer: int, page_table, ctx_
     return (out, sc) if want_scores else out
 
 
+def verify_attn(q_bf16, k: Quantized, v: Quantized, layer: int, page_table, ctx_lens, sm_scale: float,
+                full: bool):
+    """fp64 verify attention of one layer for a block of T_q draft positions
+    per request, causal within the block (the Lynx reading, section 4: the
+    drafted positions are checked against the refined cache). The last T_q
+    tokens of each context are the drafted ones, so position i of request b is
+    exactly one decode step over the first ctx_b - T_q + i + 1 tokens (none
+    when that count is not positive). Returns out [B, T_q, Hq, 128]."""
+    qb = np.ascontiguousarray(q_bf16, dtype=np.uint16)
+    B, Tq, Hq, d = qb.shape
+    assert d == D
+    cl = np.ascontiguousarray(ctx_lens, dtype=np.int32)
+    out = np.empty((B, Tq, Hq, D), np.float64)
+    for i in range(Tq):
+        n = np.maximum(cl - Tq + i + 1, 0).astype(np.int32)
+        out[:, i] = decode_attn(qb[:, i], k, v, layer, page_table, n, sm_scale, full)
+    return out
+
+
 def uniform(x_bf16, bits: int, axis=None):
     """The plain linear grid that the Lynx reading argues against ("Not all bits
     are equal"): min/max over `axis` (None = the whole array, -1 = per token),

@@ -72,11 +72,16 @@ def _lib():
                                                    vp, vp, i32, i32, i32, ctypes.c_float, ctypes.c_int, vp, vp,
                                                    vp, vp]
             L.lynx_decode_attn_noalloc.restype = ctypes.c_int
+            L.lynx_verify_attn_workspace.argtypes = [i32, i32, i32, i32]
+            L.lynx_verify_attn_workspace.restype = ctypes.c_size_t
+            L.lynx_verify_attn.argtypes = [vp, ctypes.POINTER(LynxQKV), ctypes.POINTER(LynxQKV), i32, vp, vp, i32,
+                                           i32, i32, i32, ctypes.c_float, ctypes.c_int, vp, vp, ctypes.c_size_t,
+                                           vp, vp]
             L.lynx_host_tables.argtypes = [vp, vp]
             L.lynx_host_tables.restype = None
             L.lynx_level_codes.argtypes = [vp, i64, vp, vp]
             for f in ("lynx_quantize_pages", "lynx_quantize_append", "lynx_dequant_anchor", "lynx_refine_residual",
-                      "lynx_decode_attn", "lynx_level_codes"):
+                      "lynx_decode_attn", "lynx_verify_attn", "lynx_level_codes"):
                 getattr(L, f).restype = ctypes.c_int
             _L = L
     return _L
@@ -239,6 +244,34 @@ def decode_attn(q, k: QuantizedKV, v: QuantizedKV, layer, page_table, ctx_lens, 
                                    _ptr(scores), _ptr(workspace), workspace.numel() * workspace.element_size(),
                                    _ptr(dev_err), _stream(stream)),
            "lynx_decode_attn")
+    return out
+
+
+def verify_attn_workspace(batch, draft, q_heads, max_pages):
+    return int(_lib().lynx_verify_attn_workspace(batch, draft, q_heads, max_pages))
+
+
+def verify_attn(q, k: QuantizedKV, v: QuantizedKV, layer, page_table, ctx_lens, sm_scale, mode, out=None,
+                workspace=None, dev_err=None, stream=None):
+    """lynx_verify_attn: attention of a block of draft positions per request,
+    causal within the block. q: bfloat16 [B, T_q, Hq, 128]; returns float32
+    [B, T_q, Hq, 128]."""
+    _dev(q, torch.bfloat16, "q")
+    _dev(page_table, torch.int32, "page_table")
+    _dev(ctx_lens, torch.int32, "ctx_lens")
+    B, Tq, Hq, _ = q.shape
+    max_pages = page_table.shape[1]
+    if out is None:
+        out = torch.empty((B, Tq, Hq, HEAD_DIM), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        nbytes = verify_attn_workspace(B, Tq, Hq, max_pages)
+        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
+    kd, vd = k.desc(), v.desc()
+    _check(_lib().lynx_verify_attn(_ptr(q), ctypes.byref(kd), ctypes.byref(vd), layer, _ptr(page_table),
+                                   _ptr(ctx_lens), B, Tq, Hq, max_pages, float(sm_scale), int(mode), _ptr(out),
+                                   _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(dev_err),
+                                   _stream(stream)),
+           "lynx_verify_attn")
     return out
 
 

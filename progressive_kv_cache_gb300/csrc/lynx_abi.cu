@@ -194,6 +194,102 @@ lynx_status lynx_decode_attn(const void *q_bf16, const lynx_qkv *k, const lynx_q
     return from_cuda(launch_decode_attn(a, (cudaStream_t)stream));
 }
 
+// Split plan of the verify pass: the (request, row block) pairs play the part
+// of the requests of the decode plan.
+static void verify_plan(int batch, int draft, int kv_heads, int G, int max_pages, int sms, int *rb, int *n_splits,
+                        int *pps)
+{
+    *rb = verify_row_blocks(draft, G);
+    attn_split_plan(batch * *rb, kv_heads, max_pages, sms, n_splits, pps);
+}
+
+size_t lynx_verify_attn_workspace(int32_t batch, int32_t draft, int32_t q_heads, int32_t max_pages)
+{
+    if (batch <= 0 || draft <= 0 || draft > 64 || q_heads <= 0 || max_pages <= 0)
+        return 0;
+    const int sms = device_sm_count() > 0 ? device_sm_count() : 1;
+    int best = 1;
+    for (int h = 1; h <= q_heads; ++h) {      // every kv_heads the call may pass
+        if (q_heads % h)
+            continue;
+        int rb = 1, n = 1, pps = 1;
+        verify_plan(batch, draft, h, q_heads / h, max_pages, sms, &rb, &n, &pps);
+        best = n > best ? n : best;
+    }
+    return attn_workspace_bytes(batch * draft, q_heads, best);
+}
+
+lynx_status lynx_verify_attn(const void *q_bf16, const lynx_qkv *k, const lynx_qkv *v, int32_t layer,
+                             const int32_t *page_table, const int32_t *ctx_lens, int32_t batch, int32_t draft,
+                             int32_t q_heads, int32_t max_pages, float sm_scale, lynx_mode mode, float *out,
+                             void *workspace, size_t ws_bytes, uint32_t *dev_err, void *stream)
+{
+    const bool full = mode == LYNX_MODE_FULL;
+    if (mode != LYNX_MODE_ANCHOR && mode != LYNX_MODE_FULL)
+        return LYNX_ERR_UNSUPPORTED;
+    lynx_status st = check_qkv(k, full);
+    if (st != LYNX_OK)
+        return st;
+    if ((st = check_qkv(v, full)) != LYNX_OK)
+        return st;
+    if (!q_bf16 || !page_table || !ctx_lens || !out)
+        return LYNX_ERR_NULL;
+    if (batch < 0 || draft < 1 || draft > 64 || q_heads < 0 || max_pages <= 0 || k->kv_heads <= 0)
+        return LYNX_ERR_SHAPE;
+    if (k->layers != v->layers || k->kv_heads != v->kv_heads || k->tokens != v->tokens)
+        return LYNX_ERR_SHAPE;
+    if (layer < 0 || layer >= k->layers || q_heads % k->kv_heads)
+        return LYNX_ERR_SHAPE;
+    if (!aligned(q_bf16, 16) || !aligned(out, 16) || !aligned(page_table, 4) || !aligned(ctx_lens, 4) ||
+        (dev_err && !aligned(dev_err, 4)) || (workspace && !aligned(workspace, 16)))
+        return LYNX_ERR_ALIGN;
+    if (batch == 0 || q_heads == 0)
+        return LYNX_OK;
+    const int sms = device_sm_count();
+    if (sms <= 0)
+        return LYNX_ERR_CUDA;
+    const int G = q_heads / k->kv_heads;
+    int rb = 1, n_splits = 1, pps = 1;
+    verify_plan(batch, draft, k->kv_heads, G, max_pages, sms, &rb, &n_splits, &pps);
+    if (!workspace)
+        return LYNX_ERR_NULL;
+    if (ws_bytes < attn_workspace_bytes(batch * draft, q_heads, n_splits))
+        return LYNX_ERR_WORKSPACE;
+
+    const int64_t H = k->kv_heads, T = k->tokens, P = T / kPage;
+    const int64_t plane_off = (int64_t)layer * H * T * (kD / 2);
+    const int64_t pm_off = (int64_t)layer * H * P * (2 * kD);
+    const int64_t cm_off = (int64_t)layer * H * P * (kNChunk * 2 * kD);
+    VerifyArgs a{};
+    a.q = static_cast<const uint16_t *>(q_bf16);
+    a.ka = k->anchor + plane_off;
+    a.kr = full ? k->residual + plane_off : nullptr;
+    a.va = v->anchor + plane_off;
+    a.vr = full ? v->residual + plane_off : nullptr;
+    a.kpm = k->page_meta + pm_off;
+    a.vpm = v->page_meta + pm_off;
+    a.kcm = k->chunk_meta + cm_off;
+    a.vcm = v->chunk_meta + cm_off;
+    a.page_table = page_table;
+    a.ctx = ctx_lens;
+    a.out = out;
+    a.part = static_cast<float *>(workspace);
+    a.dev_err = dev_err;
+    a.B = batch;
+    a.Tq = draft;
+    a.Hq = q_heads;
+    a.H = (int)H;
+    a.G = G;
+    a.RB = rb;
+    a.max_pages = max_pages;
+    a.pool_pages = (int)P;
+    a.n_splits = n_splits;
+    a.pages_per_split = pps;
+    a.sm_scale = sm_scale;
+    a.full = full;
+    return from_cuda(launch_verify(a, (cudaStream_t)stream));
+}
+
 lynx_status lynx_level_codes(const float *w, int64_t n, int8_t *codes, void *stream)
 {
     if (n < 0)

@@ -92,6 +92,21 @@ cudaError_t launch_decode_attn(const AttnArgs &a, cudaStream_t s);
 cudaError_t launch_attn_mma(const AttnArgs &a, cudaStream_t s);        // tensor-core path, G <= 16
 cudaError_t launch_attn_combine(const AttnArgs &a, cudaStream_t s);
 
+struct VerifyArgs {
+    const uint16_t *q;                        // [B][Tq][Hq][128] bf16
+    const uint8_t *ka, *kr, *va, *vr;         // planes of one layer (all KV heads)
+    const float *kpm, *vpm;
+    const uint16_t *kcm, *vcm;
+    const int32_t *page_table, *ctx;
+    float *out, *part;                        // out [B][Tq][Hq][128]; partials [B*Tq*Hq][n_splits][130]
+    uint32_t *dev_err;
+    int B, Tq, Hq, H, G, RB, max_pages, pool_pages, n_splits, pages_per_split;
+    float sm_scale;
+    bool full;
+};
+int verify_row_blocks(int draft, int G);      // CTAs across the T_q * G query rows of a KV head
+cudaError_t launch_verify(const VerifyArgs &a, cudaStream_t s);
+
 // ---- device helpers ------------------------------------------------------
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }

@@ -148,3 +148,29 @@ def test_quantize_append_rejects_bad_arguments(lx):
     assert call(_qkv(lx), pp=0x500002) == lx.ERR_ALIGN
     assert call(_qkv(lx), err=0x600001) == lx.ERR_ALIGN
     assert call(_qkv(lx), n=0) == lx.OK                       # nothing to do, no launch
+
+
+def test_verify_attn_rejects_bad_arguments(lx):
+    lib = lx.library()
+    k, v = _qkv(lx, H=2), _qkv(lx, H=2, base=0x20000000)
+
+    def call(k=k, v=v, layer=0, B=1, Tq=4, Hq=4, maxp=1, mode=1, q=0x600000, out=0x800000, ws=0x900000,
+             wsb=1 << 30):
+        return lib.lynx_verify_attn(ctypes.c_void_p(q) if q else None, ctypes.byref(k), ctypes.byref(v), layer,
+                                    ctypes.c_void_p(0x700000), ctypes.c_void_p(0x700100), B, Tq, Hq, maxp, 0.1,
+                                    mode, ctypes.c_void_p(out) if out else None,
+                                    ctypes.c_void_p(ws) if ws else None, wsb, None, None)
+
+    assert call(q=0) == lx.ERR_NULL
+    assert call(out=0) == lx.ERR_NULL
+    assert call(Tq=0) == lx.ERR_SHAPE
+    assert call(Tq=65) == lx.ERR_SHAPE
+    assert call(Hq=3) == lx.ERR_SHAPE
+    assert call(layer=2) == lx.ERR_SHAPE
+    assert call(out=0x800004) == lx.ERR_ALIGN
+    assert call(mode=7) == lx.ERR_UNSUPPORTED
+    assert call(k=_qkv(lx, H=2, residual=False)) == lx.ERR_NULL     # full mode needs residuals
+    assert call(B=0) == lx.OK
+    assert lib.lynx_verify_attn_workspace(1, 0, 64, 8) == 0
+    assert lib.lynx_verify_attn_workspace(1, 65, 64, 8) == 0
+    assert lib.lynx_verify_attn_workspace(2, 64, 64, 512) % 16 == 0
