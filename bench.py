@@ -537,6 +537,92 @@ def split_stream_report(args):
                       "runs": runs}))
 
 
+def verify_report(args):
+    """Multi-token verify attention at the Qwen3-235B-like layer shape (4 KV
+    heads x 32K tokens, 64 query heads, batch 1) with a block of 64 draft
+    positions: 4,096 query rows over the full cache, causal within the block.
+    The dense contraction is tensor-bound: achieved = algorithmic FLOPs (QK^T
+    and PV, 2 per multiply-add, causal counts) / kernel time, against the
+    measured bf16 tensor peak (f16 operands: the same nominal rate). The
+    acceptance proxy: per drafted position, the fraction of (head) outputs
+    whose argmax channel agrees between the anchor-only and the full pass."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    import progressive_kv_cache_gb300 as lx
+
+    w = S.WORKLOADS[2]
+    H, T, Hq, Tq = w.H, w.T, w.Hq, 64
+    dev = torch.device("cuda")
+    gen = S.DeviceGenerator()
+    x = torch.empty((1, H, T, D), dtype=torch.bfloat16, device=dev)
+    qkv = {}
+    for s in (S.S_K, S.S_V):
+        gen.fill(x, w.key(s), w.scales(s))
+        qkv[s] = lx.QuantizedKV.empty(1, H, T, dev)
+        lx.quantize_pages(x, qkv[s])
+    del x
+    qb = S.laplace_bf16(S.key(w.seed, S.S_Q * 1000 + 64), np.ones((1, Tq * Hq, D), np.float32), 1, Tq * Hq, 1)
+    qt = torch.from_numpy(qb.reshape(1, Tq, Hq, D).view(np.int16)).to(dev).view(torch.bfloat16)
+    table = torch.arange(T // 256, dtype=torch.int32, device=dev)[None].contiguous()
+    ctx = torch.full((1,), T, dtype=torch.int32, device=dev)
+    ws = torch.empty(lx.verify_attn_workspace(1, Tq, Hq, T // 256), dtype=torch.uint8, device=dev)
+    sm = D ** -0.5
+    outs = {}
+    for m in (lx.MODE_ANCHOR, lx.MODE_FULL):
+        outs[m] = lx.verify_attn(qt, qkv[S.S_K], qkv[S.S_V], 0, table, ctx, sm, m, workspace=ws).clone()
+    res = {}
+    for name, m in (("full", lx.MODE_FULL), ("anchor", lx.MODE_ANCHOR)):
+        for _ in range(max(args.warmup, 3)):
+            lx.verify_attn(qt, qkv[S.S_K], qkv[S.S_V], 0, table, ctx, sm, m, workspace=ws)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with ClockSampler(0) as clk:
+            e0.record()
+            for _ in range(args.steps):
+                lx.verify_attn(qt, qkv[S.S_K], qkv[S.S_V], 0, table, ctx, sm, m, workspace=ws)
+            e1.record()
+            torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / args.steps
+        visible = sum(T - Tq + i + 1 for i in range(Tq))
+        flops = 4.0 * Hq * visible * D
+        res[name] = {"ms": ms, "tflops": flops / (ms * 1e-3) / 1e12,
+                     "hbm_gbs": H * T * (B_ATTN_FULL if m == lx.MODE_FULL else B_ATTN_ANCHOR) / (ms * 1e-3) / 1e9,
+                     "clocks": clk.summary()}
+    agree = (outs[lx.MODE_ANCHOR].argmax(-1) == outs[lx.MODE_FULL].argmax(-1)).float().mean(dim=(0, 2))
+    peak = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))["bf16_tflops"] \
+        if os.path.exists(os.path.join(ROOT, "MEASURED_PEAKS.json")) else 1900.0
+    cpu = None
+    if not args.no_cpu_baseline:
+        import oracle as orc
+        orc.build()
+        kx = S.laplace_bf16(w.key(S.S_K), w.scales(S.S_K), 1, H, T, heads=[0], t0=0, t1=8192)
+        vx = S.laplace_bf16(w.key(S.S_V), w.scales(S.S_V), 1, H, T, heads=[0], t0=0, t1=8192)
+        kq, vq = orc.quantize(kx), orc.quantize(vx)
+        qs = qb.reshape(1, Tq, Hq, D)[:, :4, : Hq // H]
+        pt = np.arange(32, dtype=np.int32)[None]
+        t0 = time.perf_counter()
+        reps = 0
+        while time.perf_counter() - t0 < 10.0:
+            orc.verify_attn(qs, kq, vq, 0, pt, np.array([8192], np.int32), sm, True)
+            reps += 1
+        dt = time.perf_counter() - t0
+        fl = reps * 4.0 * (Hq // H) * sum(8192 - 4 + i + 1 for i in range(4)) * D
+        cpu = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": orc.num_threads(), "kind": "oracle",
+               "sample": f"1 KV head, 8K tokens, 4 draft positions x 16 heads, full mode, {reps} passes, {dt:.1f} s"}
+    f = res["full"]
+    print(json.dumps({
+        "report": "verify", "metric": "verify attention TFLOP/s vs tensor roofline (1 GB300)",
+        "value": f["tflops"], "unit": "TFLOP/s", "ms_per_call": f["ms"], "steps": args.steps,
+        "config": {"workload": f"{w.name}, block of {Tq} draft positions", "kv_heads": H, "tokens": T,
+                   "q_heads": Hq, "draft": Tq, "batch": 1},
+        "roofline": {"bound": "tensor", "achieved": f["tflops"], "peak": peak, "unit": "TFLOP/s",
+                     "frac": f["tflops"] / peak, "peak_kind": "measured bf16 (f16 operands, same nominal rate)",
+                     "note": "algorithmic FLOPs; the hi/lo split costs three MMAs per product"},
+        "modes": res, "acceptance_proxy_per_position": [round(float(v), 4) for v in agree.cpu()],
+        "acceptance_proxy_mean": float(agree.mean()), "cpu_baseline": cpu}))
+
+
 def run_gpu(args):
     import torch
     import torch.distributed as dist
@@ -698,10 +784,11 @@ def main():
                                        "decode_attn_full"], default=None,
                     help="time one kernel group only (for profiler captures on smaller cases)")
     ap.add_argument("--layers", type=int, default=None, help="layers of the cache (default: all 94)")
-    ap.add_argument("--report", choices=["progressive", "append", "split-stream"], default=None,
+    ap.add_argument("--report", choices=["progressive", "append", "split-stream", "verify"], default=None,
                     help="progressive: residual layers arriving one by one (8 layers, 64K tokens); "
                          "append: quantize-on-append of 32 requests' tail pages over 94 layers x 8 KV heads; "
-                         "split-stream: anchors then residuals over an emulated link, decode on anchors first")
+                         "split-stream: anchors then residuals over an emulated link, decode on anchors first; "
+                         "verify: multi-token verify attention (64 draft positions, 32K context)")
     ap.add_argument("--no-graph", action="store_true",
                     help="issue every library call from Python instead of replaying CUDA graphs of them")
     args = ap.parse_args()
@@ -719,6 +806,8 @@ def main():
         append_report(args)
     elif args.report == "split-stream":
         split_stream_report(args)
+    elif args.report == "verify":
+        verify_report(args)
     else:
         run_gpu(args)
 
