@@ -417,7 +417,7 @@ def append_report(args):
     import progressive_kv_cache_gb300 as lx
 
     w = S.WORKLOADS[4]
-    L, H, n = W3.L, w.H, w.B
+    L, H, n = (args.layers or W3.L), w.H, w.B
     ctx, pool, table = S.batched_layout(w)
     last = (ctx - 1) // 256
     phys = torch.from_numpy(table[np.arange(n), last].astype(np.int32)).cuda()
@@ -474,7 +474,7 @@ def append_report(args):
     line = {"report": "append", "metric": "quantize-on-append HBM GB/s vs HBM roofline (1 GB300)", "value": gbs,
             "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms,
             "higher_is_better": True, "dtype": "bf16 in, 4+4-bit planes", "data": "synthetic",
-            "config": {"workload": f"{w.name} tails on the 94-layer model", "requests": n, "layers": L,
+            "config": {"workload": f"{w.name} tails on a {L}-layer model", "requests": n, "layers": L,
                        "kv_heads": H, "pages_per_step": 2 * n * L * H, "l2": "inputs larger than L2, no flush"},
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
                          "peak_kind": peak_kind, "traffic": None},

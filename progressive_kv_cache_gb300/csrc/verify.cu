@@ -47,7 +47,7 @@ template <bool FULL>
 struct Smem {
     Page<FULL> k[2], v[2];                    // double-buffered pages
     uint8_t tile[2][4][kTile];                // per chunk buffer: K hi, K lo, V hi, V lo
-    float lev[256];                           // level of a code byte (anchor: of an anchor nibble)
+    float lev[256 * 8];                       // level of a code byte (anchor: of an anchor nibble), 8 copies
     alignas(8) uint64_t bar[2];
 };
 
@@ -100,43 +100,43 @@ __device__ __forceinline__ uint32_t tile_off(int t, int slot)
 }
 
 // Decode chunk j of one tensor's page into fp16 hi/lo tiles. Thread u takes
-// token u / 8 and channels 16 (u % 8) .. + 15.
+// channel pair p = u % 64 (channels 2p, 2p + 1) of tokens 8 (u / 64) .. + 7:
+// its affines are computed once, consecutive threads read consecutive code
+// bytes and metadata and write consecutive 4-byte words of a tile row. The
+// level table is replicated 8 times (copy u % 8).
 template <bool FULL>
 __device__ __forceinline__ void decode_chunk(const Page<FULL> &pg, int j, const float *lev, uint8_t *hi_tile,
                                              uint8_t *lo_tile, int tid)
 {
-    const int t = tid >> 3, c0 = 16 * (tid & 7);
-    const int row = j * kChunk + t;
-    const uint2 aw = *reinterpret_cast<const uint2 *>(pg.a + row * kRow + c0 / 2);
-    uint2 rw = make_uint2(0x77777777u, 0x77777777u);
-    if (FULL)
-        rw = *reinterpret_cast<const uint2 *>(pg.r + row * kRow + c0 / 2);
-    const uint32_t words_a[2] = {aw.x, aw.y}, words_r[2] = {rw.x, rw.y};
-    uint32_t hi[8], lo[8];
+    const int p = tid & 63, t0 = (tid >> 6) * 8;
+    const int d = 2 * p;
+    const float2 mn = *reinterpret_cast<const float2 *>(pg.pm + d);
+    const float2 rg = *reinterpret_cast<const float2 *>(pg.pm + kD + d);
+    const float2 mu = __half22float2(*reinterpret_cast<const __half2 *>(pg.cm + (2 * j) * kD + d));
+    const float2 sc = __half22float2(*reinterpret_cast<const __half2 *>(pg.cm + (2 * j + 1) * kD + d));
+    const float2 a = __ffma2_rn(rg, mu, mn), b = __fmul2_rn(rg, sc);
+    const float *lv = lev + (tid & 7);
 #pragma unroll
-    for (int p = 0; p < 8; ++p) {           // channel pairs c0 + 2p, + 1
-        const uint32_t a8 = (words_a[p >> 2] >> (8 * (p & 3))) & 0xFFu;
-        const uint32_t r8 = (words_r[p >> 2] >> (8 * (p & 3))) & 0xFFu;
+    for (int k = 0; k < 8; ++k) {
+        const int t = t0 + k;
+        const int row = j * kChunk + t;
+        const uint32_t a8 = pg.a[row * kRow + p];
         float L0, L1;
         if (FULL) {
-            L0 = lev[((a8 & 0x0Fu) << 4) | (r8 & 0x0Fu)];
-            L1 = lev[(a8 & 0xF0u) | (r8 >> 4)];
+            const uint32_t r8 = pg.r[row * kRow + p];
+            L0 = lv[8 * (((a8 & 0x0Fu) << 4) | (r8 & 0x0Fu))];
+            L1 = lv[8 * ((a8 & 0xF0u) | (r8 >> 4))];
         } else {
-            L0 = lev[a8 & 0x0Fu];
-            L1 = lev[a8 >> 4];
+            L0 = lv[8 * (a8 & 0x0Fu)];
+            L1 = lv[8 * (a8 >> 4)];
         }
-        const int d = c0 + 2 * p;
-        const float2 mn = *reinterpret_cast<const float2 *>(pg.pm + d);
-        const float2 rg = *reinterpret_cast<const float2 *>(pg.pm + kD + d);
-        const float2 mu = __half22float2(*reinterpret_cast<const __half2 *>(pg.cm + (2 * j) * kD + d));
-        const float2 sc = __half22float2(*reinterpret_cast<const __half2 *>(pg.cm + (2 * j + 1) * kD + d));
-        const float2 a = __ffma2_rn(rg, mu, mn), b = __fmul2_rn(rg, sc);
-        split2(__ffma2_rn(b, make_float2(L0, L1), a), hi[p], lo[p]);
+        uint32_t hi, lo;
+        split2(__ffma2_rn(b, make_float2(L0, L1), a), hi, lo);
+        // word p % 4 of 16-byte slot p / 4 of token t's row
+        const uint32_t off = tile_off(t, p >> 2) + 4 * (p & 3);
+        *reinterpret_cast<uint32_t *>(hi_tile + off) = hi;
+        *reinterpret_cast<uint32_t *>(lo_tile + off) = lo;
     }
-    *reinterpret_cast<uint4 *>(hi_tile + tile_off(t, 2 * (tid & 7))) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-    *reinterpret_cast<uint4 *>(hi_tile + tile_off(t, 2 * (tid & 7) + 1)) = make_uint4(hi[4], hi[5], hi[6], hi[7]);
-    *reinterpret_cast<uint4 *>(lo_tile + tile_off(t, 2 * (tid & 7))) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-    *reinterpret_cast<uint4 *>(lo_tile + tile_off(t, 2 * (tid & 7) + 1)) = make_uint4(lo[4], lo[5], lo[6], lo[7]);
 }
 
 template <bool FULL>
@@ -151,8 +151,8 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(VerifyArgs a, Level
     const int G = a.G, Tq = a.Tq;
     const int64_t T = (int64_t)a.pool_pages * kPage;
 
-    for (int i = tid; i < 256; i += kThreads)
-        sm.lev[i] = FULL ? levt.full[i] : levt.anchor[i & 15];
+    for (int i = tid; i < 256 * 8; i += kThreads)
+        sm.lev[i] = FULL ? levt.full[i >> 3] : levt.anchor[(i >> 3) & 15];
     if (tid == 0) {
         mbar_init(&sm.bar[0], 1);
         mbar_init(&sm.bar[1], 1);
