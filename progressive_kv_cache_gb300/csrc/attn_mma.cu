@@ -421,6 +421,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(AttnArgs a, Level
             }
             gdown = exp2f((float)-ge);
             gscale = exp2f((float)ge);
+            if (ge != 0) {                   // rare: fold 2^-e into this lane's b values
+                float4 *bv = reinterpret_cast<float4 *>(kbf + 4 * lane + 4 * (lane >> 3));
+                const float4 v = *bv;
+                *bv = make_float4(v.x * gdown, v.y * gdown, v.z * gdown, v.w * gdown);
+            }
             __syncwarp();
             if (lane == 0)
                 release(xk);
@@ -445,10 +450,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(AttnArgs a, Level
                 beta2[r] = __ffma2_rn(make_float2(qv.z, qv.w), make_float2(aa.z, aa.w), beta2[r]);
                 float2 x01 = __fmul2_rn(make_float2(qv.x, qv.y), make_float2(bb.x, bb.y));
                 float2 x23 = __fmul2_rn(make_float2(qv.z, qv.w), make_float2(bb.z, bb.w));
-                if (ge != 0) {
-                    x01 = __fmul2_rn(x01, make_float2(gdown, gdown));
-                    x23 = __fmul2_rn(x23, make_float2(gdown, gdown));
-                }
                 if (G16) {
                     split2(x01, A0[r], A1[r]);
                     split2(x23, A0[2 + r], A1[2 + r]);
