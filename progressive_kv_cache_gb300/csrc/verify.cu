@@ -1,5 +1,6 @@
 // verify.cu -- multi-token verify attention over the quantized paged cache
-// (a block of draft positions per request, causal within the block).
+// (a block of draft positions per request, causal within the block), on the
+// fifth-generation tensor cores (tcgen05).
 //
 // The Lynx reading, section 4: decoding runs speculatively on the anchor-only
 // draft cache, and once the residuals land a verify pass re-reads the refined
@@ -9,13 +10,25 @@
 // context up to and including draft token i. Dequantization stays on chip
 // ("KV-cache quantization" explainer, "Bottom-right").
 //
-// With T_q x G query rows per KV head, Q.K^T and P.V are dense contractions:
-// each 32-token chunk of K and V is decoded once per CTA (x = a + b L, fp32)
-// into shared-memory fp16 hi/lo tiles, and every warp runs 16 query rows over
-// them on the tensor cores (mma.sync m16n8k16, fp32 accumulation) with the
-// three-product split (hi.hi + hi.lo + lo.hi) that keeps fp32-level accuracy.
-// Softmax is online per row; split-K partials are merged by the decode path's
-// combine kernel.
+// With T_q x G query rows per KV head, Q.K^T and P.V are dense contractions.
+// A CTA owns 128 query rows (the MMA's M) and a range of pages; per 32-token
+// chunk:
+//  - decode warps expand the chunk's K and V codes (x = a + b L in fp32, split
+//    into fp16 hi + lo) into shared-memory operand tiles in the tensor cores'
+//    K-major swizzled layouts (K: rows of 128 channels, 128-byte swizzle; V
+//    transposed: rows of 32 tokens, 64-byte swizzle);
+//  - one thread issues tcgen05.mma: S = Q.K^T into tensor memory with Q hi/lo
+//    resident in tensor memory as the A operand (three products hi.hi + hi.lo
+//    + lo.hi keep fp32-level accuracy), and after the softmax O += P.V with P
+//    hi/lo in tensor memory as the A operand; only K and V^T are read from
+//    shared memory by the tensor cores;
+//  - softmax warps own one query row per thread: they read the row's 32
+//    scores from tensor memory, apply the causal mask and the online softmax
+//    (the reference moves only when a score passes it by 2^8; then O is
+//    rescaled in tensor memory), and write P hi/lo back to tensor memory.
+// Chunk codes arrive by bulk copy into a ring of slots; every wait is bounded.
+// Split-K partials are merged by the decode path's combine kernel.
+#include <cstddef>
 #include <cuda_fp16.h>
 
 #include "lynx_internal.cuh"
@@ -24,53 +37,173 @@
 namespace lynx {
 namespace {
 
-constexpr uint32_t kPlane = kPage * kD / 2;   // 16 KiB: one page of one plane
 constexpr int kRow = kD / 2;                  // code bytes per token
-constexpr int kTileRow = kD * 2;              // bytes per token of an fp16 tile
-constexpr int kTile = kChunk * kTileRow;      // 8 KiB
 constexpr int kPart = kD + 2;
-constexpr int kWarps = 8;                     // 16 query rows each
-constexpr int kRows = kWarps * 16;            // rows per CTA
-constexpr int kThreads = kWarps * 32;
+constexpr int kRows = 128;                    // query rows per CTA (MMA M)
+constexpr int kSoftWarps = 4, kDecWarps = 8;
+constexpr int kMmaWarp = kSoftWarps + kDecWarps;      // issues the MMAs, owns the tensor memory
+constexpr int kProdWarp = kMmaWarp + 1;                // issues the bulk copies of chunk codes
+constexpr int kThreads = (kProdWarp + 1) * 32;
+constexpr int kRing = 6;                      // chunk slots of codes in flight
+constexpr int kBufs = 3;                      // K / V operand tiles and S buffers
+constexpr int kPBufs = 2;                     // P buffers
 constexpr uint32_t kWaitLimit = 1u << 22;
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kLevCopies = 32;                // one level-table copy per lane: conflict-free lookups
+// tensor memory columns (fp32 / f16x2 words; lane = query row)
+constexpr uint32_t kColS = 0;                           // S [buffer][Q.K_hi 32 tokens, Q_hi.K_lo 32 tokens]
+constexpr uint32_t kColP = kColS + 64 * kBufs;          // P [buffer][hi 16 words, lo 16 words]
+constexpr uint32_t kColO = kColP + 32 * kPBufs;         // O [128 channels]
+constexpr uint32_t kColQ = kColO + kD;                  // Q hi [64 words], Q lo [64 words]
+constexpr uint32_t kColsUsed = kColQ + kD;
+constexpr uint32_t kTmemCols = 512;
+static_assert(kColsUsed <= kTmemCols, "tensor memory columns");
 
+// One chunk of K and V as it arrives (codes of 32 tokens, page and chunk metadata).
 template <bool FULL>
-struct Page {                                 // one tensor's page as it arrives
-    uint8_t a[kPlane];
-    uint8_t r[FULL ? kPlane : 16];
-    float pm[2 * kD];
-    uint16_t cm[kNChunk * 2 * kD];
+struct Slot {
+    uint8_t ka[kChunk * kRow], va[kChunk * kRow];
+    uint8_t kr[FULL ? kChunk * kRow : 16], vr[FULL ? kChunk * kRow : 16];
+    float kpm[2 * kD], vpm[2 * kD];           // page min, range
+    uint16_t kcm[2 * kD], vcm[2 * kD];        // chunk mean, scale
 };
 
+// Operand tiles. 128-byte swizzle: 16-byte piece c of a 128-byte row r sits at
+// piece c ^ (r & 7), atoms of 8 rows x 128 bytes; 64-byte swizzle: piece c of
+// a 64-byte row r at c ^ ((r >> 1) & 3). Every tile starts on 1024 bytes.
 template <bool FULL>
 struct Smem {
-    Page<FULL> k[2], v[2];                    // double-buffered pages
-    uint8_t tile[2][4][kTile];                // per chunk buffer: K hi, K lo, V hi, V lo
-    float lev[256 * 8];                       // level of a code byte (anchor: of an anchor nibble), 8 copies
-    alignas(8) uint64_t bar[2];
+    uint8_t k[kBufs][2][2][kChunk * 128];     // K [buffer][k-atom][hi, lo][token][64 channels] (128B): per
+                                              // k-atom, the hi rows then the lo rows form one 64-row operand
+    uint8_t v[kBufs][2][kD * 64];             // V [buffer][hi, lo][channel][32 tokens] (64B)
+    Slot<FULL> slot[kRing];
+    float lev[256 * kLevCopies];              // level of a code byte (anchor: of a nibble), entry-major
+    int slot_page[kRing];                     // physical page of the chunk in each slot (-1: invalid)
+    uint32_t tmem;
+    alignas(8) uint64_t ring_full[kRing], slot_free[kRing];
+    uint64_t k_full[kBufs], v_full[kBufs], s_full[kBufs], s_free[kBufs], pv_done[kBufs], p_full[kPBufs];
+    uint64_t drained;
 };
 
-__device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
+__device__ __forceinline__ uint32_t sw128(int row, int byte)
 {
-    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    return (uint32_t)(row * 128 + ((((byte >> 4) ^ (row & 7)) << 4) | (byte & 15)));
+}
+__device__ __forceinline__ uint32_t sw64(int row, int byte)
+{
+    return (uint32_t)(row * 64 + ((((byte >> 4) ^ ((row >> 1) & 3)) << 4) | (byte & 15)));
 }
 
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4])
+// Shared-memory matrix descriptor of a K-major swizzled operand (SBO = bytes
+// between 8-row groups; layout 2 = 128-byte swizzle, 4 = 64-byte swizzle).
+__device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t sbo, uint32_t layout)
 {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(addr));
+    return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) | ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) |
+           ((uint64_t)1 << 46) | ((uint64_t)layout << 61);
 }
 
-__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4])
+// Instruction descriptor: f32 accumulator, f16 A and B, both K-major, N, M.
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N)
 {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(addr));
+    return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// D (tensor memory) (+)= A (tensor memory: row i in lane i, two f16 per
+// column) x B (shared-memory descriptor).
+__device__ __forceinline__ void umma_ts(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t acc)
+{
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
+                 "r"(a), "l"(b), "r"(idesc), "r"(acc)
+                 : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint64_t *bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+#define LYNX_R32(v)                                                                                                    \
+    "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]), "=f"(v[4]), "=f"(v[5]), "=f"(v[6]), "=f"(v[7]), "=f"(v[8]),       \
+        "=f"(v[9]), "=f"(v[10]), "=f"(v[11]), "=f"(v[12]), "=f"(v[13]), "=f"(v[14]), "=f"(v[15]), "=f"(v[16]),        \
+        "=f"(v[17]), "=f"(v[18]), "=f"(v[19]), "=f"(v[20]), "=f"(v[21]), "=f"(v[22]), "=f"(v[23]), "=f"(v[24]),       \
+        "=f"(v[25]), "=f"(v[26]), "=f"(v[27]), "=f"(v[28]), "=f"(v[29]), "=f"(v[30]), "=f"(v[31])
+#define LYNX_W32(v)                                                                                                    \
+    "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]), "f"(v[8]), "f"(v[9]),     \
+        "f"(v[10]), "f"(v[11]), "f"(v[12]), "f"(v[13]), "f"(v[14]), "f"(v[15]), "f"(v[16]), "f"(v[17]), "f"(v[18]),   \
+        "f"(v[19]), "f"(v[20]), "f"(v[21]), "f"(v[22]), "f"(v[23]), "f"(v[24]), "f"(v[25]), "f"(v[26]), "f"(v[27]),   \
+        "f"(v[28]), "f"(v[29]), "f"(v[30]), "f"(v[31])
+
+// 32 consecutive tensor-memory columns of this lane's row.
+__device__ __forceinline__ void tmem_ld32(uint32_t t, float (&v)[32])
+{
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+                 "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+                 : LYNX_R32(v)
+                 : "r"(t)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t t, const float (&v)[32])
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+                 "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(t),
+                 LYNX_W32(v)
+                 : "memory");
+}
+#undef LYNX_R32
+#undef LYNX_W32
+
+// 32 consecutive tensor-memory columns of this lane's row, from words.
+__device__ __forceinline__ void tmem_st32u(uint32_t t, const uint32_t (&w)[32])
+{
+    float v[32];
+#pragma unroll
+    for (int k = 0; k < 32; ++k)
+        v[k] = __uint_as_float(w[k]);
+    tmem_st32(t, v);
+}
+
+// 16 consecutive tensor-memory columns of this lane's row.
+__device__ __forceinline__ void tmem_st16(uint32_t t, const uint32_t (&v)[16])
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+                 "%16};" ::"r"(t),
+                 "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+                 "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Non-blocking test of an mbarrier phase.
+__device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok)
+                 : "r"(smem_u32(bar)), "r"(parity)
+                 : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ float neg_inf() { return -__int_as_float(0x7F800000); }
+
+__device__ __forceinline__ float exp2_sm(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
 // (x0, x1) -> fp16 pairs hi and lo with hi + lo = (x0, x1) to ~22 bits.
@@ -83,329 +216,486 @@ __device__ __forceinline__ void split2(float2 x, uint32_t &hi, uint32_t &lo)
     lo = *reinterpret_cast<const uint32_t *>(&l);
 }
 
-__device__ __forceinline__ float neg_inf() { return -__int_as_float(0x7F800000); }
-
-__device__ __forceinline__ float exp2_sm(float x)
+// Chunk affines a = mn + rng mu and b = rng s of channel pair pr.
+__device__ __forceinline__ void pair_affine(const float *pm, const uint16_t *cm, int pr, float2 &a, float2 &b)
 {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
+    const int d = 2 * pr;
+    const float2 mn = *reinterpret_cast<const float2 *>(pm + d);
+    const float2 rg = *reinterpret_cast<const float2 *>(pm + kD + d);
+    const float2 mu = __half22float2(*reinterpret_cast<const __half2 *>(cm + d));
+    const float2 sc = __half22float2(*reinterpret_cast<const __half2 *>(cm + kD + d));
+    a = __ffma2_rn(rg, mu, mn);
+    b = __fmul2_rn(rg, sc);
 }
 
-// Byte offset of 16-byte slot `slot` of token `t` in a chunk tile: the slots
-// of 8 consecutive tokens (an ldmatrix 8x8 matrix) fall in distinct banks.
-__device__ __forceinline__ uint32_t tile_off(int t, int slot)
+// The same for the four channel pairs 4 g .. 4 g + 3 (channels 8 g .. 8 g + 7).
+__device__ __forceinline__ void quad_affine(const float *pm, const uint16_t *cm, int g, float2 (&a)[4], float2 (&b)[4])
 {
-    return (uint32_t)(t * kTileRow + ((slot ^ (t & 7)) << 4));
-}
-
-// Decode chunk j of one tensor's page into fp16 hi/lo tiles. Thread u takes
-// channel pair p = u % 64 (channels 2p, 2p + 1) of tokens 8 (u / 64) .. + 7:
-// its affines are computed once, consecutive threads read consecutive code
-// bytes and metadata and write consecutive 4-byte words of a tile row. The
-// level table is replicated 8 times (copy u % 8).
-template <bool FULL>
-__device__ __forceinline__ void decode_chunk(const Page<FULL> &pg, int j, const float *lev, uint8_t *hi_tile,
-                                             uint8_t *lo_tile, int tid)
-{
-    const int p = tid & 63, t0 = (tid >> 6) * 8;
-    const int d = 2 * p;
-    const float2 mn = *reinterpret_cast<const float2 *>(pg.pm + d);
-    const float2 rg = *reinterpret_cast<const float2 *>(pg.pm + kD + d);
-    const float2 mu = __half22float2(*reinterpret_cast<const __half2 *>(pg.cm + (2 * j) * kD + d));
-    const float2 sc = __half22float2(*reinterpret_cast<const __half2 *>(pg.cm + (2 * j + 1) * kD + d));
-    const float2 a = __ffma2_rn(rg, mu, mn), b = __fmul2_rn(rg, sc);
-    const float *lv = lev + (tid & 7);
+    const int d = 8 * g;
+    const float4 mn0 = *reinterpret_cast<const float4 *>(pm + d), mn1 = *reinterpret_cast<const float4 *>(pm + d + 4);
+    const float4 rg0 = *reinterpret_cast<const float4 *>(pm + kD + d);
+    const float4 rg1 = *reinterpret_cast<const float4 *>(pm + kD + d + 4);
+    const uint4 mu = *reinterpret_cast<const uint4 *>(cm + d), sc = *reinterpret_cast<const uint4 *>(cm + kD + d);
+    const float2 mn[4] = {make_float2(mn0.x, mn0.y), make_float2(mn0.z, mn0.w), make_float2(mn1.x, mn1.y),
+                          make_float2(mn1.z, mn1.w)};
+    const float2 rg[4] = {make_float2(rg0.x, rg0.y), make_float2(rg0.z, rg0.w), make_float2(rg1.x, rg1.y),
+                          make_float2(rg1.z, rg1.w)};
+    const uint32_t muw[4] = {mu.x, mu.y, mu.z, mu.w}, scw[4] = {sc.x, sc.y, sc.z, sc.w};
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-        const int t = t0 + k;
-        const int row = j * kChunk + t;
-        const uint32_t a8 = pg.a[row * kRow + p];
-        float L0, L1;
-        if (FULL) {
-            const uint32_t r8 = pg.r[row * kRow + p];
-            L0 = lv[8 * (((a8 & 0x0Fu) << 4) | (r8 & 0x0Fu))];
-            L1 = lv[8 * ((a8 & 0xF0u) | (r8 >> 4))];
-        } else {
-            L0 = lv[8 * (a8 & 0x0Fu)];
-            L1 = lv[8 * (a8 >> 4)];
-        }
-        uint32_t hi, lo;
-        split2(__ffma2_rn(b, make_float2(L0, L1), a), hi, lo);
-        // word p % 4 of 16-byte slot p / 4 of token t's row
-        const uint32_t off = tile_off(t, p >> 2) + 4 * (p & 3);
-        *reinterpret_cast<uint32_t *>(hi_tile + off) = hi;
-        *reinterpret_cast<uint32_t *>(lo_tile + off) = lo;
+    for (int i = 0; i < 4; ++i) {
+        a[i] = __ffma2_rn(rg[i], __half22float2(*reinterpret_cast<const __half2 *>(&muw[i])), mn[i]);
+        b[i] = __fmul2_rn(rg[i], __half22float2(*reinterpret_cast<const __half2 *>(&scw[i])));
     }
+}
+
+// Levels of the two channels of a code byte (anchor byte a8, residual byte
+// r8), the channel in the nibble at bit `sh` first (sh = 0: low channel
+// first; sh = 4: high channel first). Full: entry (anchor nibble << 4) |
+// residual nibble. Anchor: every entry e holds the level of nibble e & 15, so
+// a byte shifted right indexes its upper nibble's channel directly. Table
+// copies interleave: entry e of this lane's copy is lv[kLevCopies e].
+template <bool FULL>
+__device__ __forceinline__ float2 levels(const float *lv, uint32_t a8, uint32_t r8, uint32_t sh = 0)
+{
+    const uint32_t sh2 = 4u - sh;
+    if (FULL)
+        return make_float2(lv[kLevCopies * ((((a8 >> sh) & 0x0Fu) << 4) | ((r8 >> sh) & 0x0Fu))],
+                           lv[kLevCopies * ((((a8 >> sh2) & 0x0Fu) << 4) | ((r8 >> sh2) & 0x0Fu))]);
+    return make_float2(lv[kLevCopies * (a8 >> sh)], lv[kLevCopies * (a8 >> sh2)]);
+}
+
+// K of one chunk into tiles kt[k-atom][hi/lo] (rows = tokens, 128-byte rows of
+// 64 channels). Decode thread u (0..255) takes the 16-byte piece of channels
+// 8 g .. 8 g + 7, g = u % 16, of tokens u / 16 and u / 16 + 16: one 32-bit
+// code load per plane and one 16-byte store per tile.
+template <bool FULL>
+__device__ __forceinline__ void decode_k(const Slot<FULL> &sl, bool valid, const float *lv, uint8_t (&kt)[2][2][kChunk * 128],
+                                         int u)
+{
+    const int g = u & 15, ka = g >> 3, piece = g & 7;
+    float2 aa[4], bb[4];
+    quad_affine(sl.kpm, sl.kcm, g, aa, bb);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int t = (u >> 4) + 16 * h;
+        uint32_t hi[4] = {0, 0, 0, 0}, lo[4] = {0, 0, 0, 0};
+        if (valid) {
+            const uint32_t a4 = *reinterpret_cast<const uint32_t *>(sl.ka + t * kRow + 4 * g);
+            const uint32_t r4 = FULL ? *reinterpret_cast<const uint32_t *>(sl.kr + t * kRow + 4 * g) : 0u;
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                split2(__ffma2_rn(bb[i], levels<FULL>(lv, (a4 >> (8 * i)) & 0xFFu, (r4 >> (8 * i)) & 0xFFu), aa[i]),
+                       hi[i], lo[i]);
+        }
+        const uint32_t off = sw128(t, 16 * piece);
+        *reinterpret_cast<uint4 *>(&kt[ka][0][off]) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4 *>(&kt[ka][1][off]) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    }
+}
+
+// V of one chunk, transposed, into tiles vt[hi/lo] (rows = channels, 64-byte
+// rows of 32 tokens). Decode thread u takes channel pair pr = u % 64 of the
+// eight tokens 8 o .. 8 o + 7, o = u / 64: one 16-byte store per row and
+// tile. Lanes with bit 2 of pr set store row 2 pr + 1 first, so that the 8
+// lanes of a store phase cover all 32 banks.
+template <bool FULL>
+__device__ __forceinline__ void decode_v(const Slot<FULL> &sl, bool valid, const float *lv, uint8_t (&vt)[2][kD * 64],
+                                         int u)
+{
+    const int pr = u & 63, o = u >> 6, sw = (pr >> 2) & 1;
+    const uint32_t sh = 4u * (uint32_t)sw;
+    float2 aa, bb;
+    pair_affine(sl.vpm, sl.vcm, pr, aa, bb);
+    if (sw) {
+        aa = make_float2(aa.y, aa.x);
+        bb = make_float2(bb.y, bb.x);
+    }
+    uint32_t h0[4], h1[4], l0[4], l1[4];     // rows 2 pr + sw and 2 pr + 1 - sw; word j = tokens 8 o + 2 j, + 1
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        float2 x[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int t = 8 * o + 2 * j + e;
+            x[e] = make_float2(0.0f, 0.0f);
+            if (valid) {
+                const uint32_t a8 = sl.va[t * kRow + pr];
+                const uint32_t r8 = FULL ? sl.vr[t * kRow + pr] : 0u;
+                x[e] = __ffma2_rn(bb, levels<FULL>(lv, a8, r8, sh), aa);
+            }
+        }
+        split2(make_float2(x[0].x, x[1].x), h0[j], l0[j]);
+        split2(make_float2(x[0].y, x[1].y), h1[j], l1[j]);
+    }
+    const uint32_t o0 = sw64(2 * pr + sw, 16 * o), o1 = sw64(2 * pr + 1 - sw, 16 * o);
+    *reinterpret_cast<uint4 *>(&vt[0][o0]) = make_uint4(h0[0], h0[1], h0[2], h0[3]);
+    *reinterpret_cast<uint4 *>(&vt[0][o1]) = make_uint4(h1[0], h1[1], h1[2], h1[3]);
+    *reinterpret_cast<uint4 *>(&vt[1][o0]) = make_uint4(l0[0], l0[1], l0[2], l0[3]);
+    *reinterpret_cast<uint4 *>(&vt[1][o1]) = make_uint4(l1[0], l1[1], l1[2], l1[3]);
 }
 
 template <bool FULL>
 __global__ void __launch_bounds__(kThreads, 1) verify_kernel(VerifyArgs a, LevelTable levt)
 {
-    extern __shared__ __align__(128) unsigned char smem_raw[];
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
     Smem<FULL> &sm = *reinterpret_cast<Smem<FULL> *>(smem_raw);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int g = lane >> 2, q = lane & 3;
-    const int lm = lane >> 3, lr = lane & 7;   // ldmatrix: this lane addresses row lr of matrix lm
     const int split = blockIdx.x, kvh = blockIdx.y / a.RB, rb = blockIdx.y % a.RB, b = blockIdx.z;
     const int G = a.G, Tq = a.Tq;
     const int64_t T = (int64_t)a.pool_pages * kPage;
-
-    for (int i = tid; i < 256 * 8; i += kThreads)
-        sm.lev[i] = FULL ? levt.full[i >> 3] : levt.anchor[(i >> 3) & 15];
-    if (tid == 0) {
-        mbar_init(&sm.bar[0], 1);
-        mbar_init(&sm.bar[1], 1);
-        fence_mbar_init();
+    if (smem_u32(smem_raw) & 1023u) {        // the swizzled tiles need a 1024-byte aligned window
+        if (a.dev_err && tid == 0)
+            atomicOr(a.dev_err, LYNX_DEVERR_TIMEOUT);
+        return;
     }
 
+    // ---- set-up: level table, barriers, tensor memory ---------------------
+    for (int i = tid; i < 256 * kLevCopies; i += kThreads) {
+        const int e = i / kLevCopies;
+        sm.lev[i] = FULL ? levt.full[e] : levt.anchor[e & 15];
+    }
+    if (tid == 0) {
+        for (int s = 0; s < kRing; ++s) {
+            mbar_init(&sm.ring_full[s], 1);
+            mbar_init(&sm.slot_free[s], kDecWarps);
+        }
+        for (int s = 0; s < kBufs; ++s) {
+            mbar_init(&sm.k_full[s], kDecWarps);
+            mbar_init(&sm.v_full[s], kDecWarps);
+            mbar_init(&sm.s_full[s], 1);
+            mbar_init(&sm.s_free[s], kSoftWarps);
+            mbar_init(&sm.pv_done[s], 1);
+        }
+        for (int s = 0; s < kPBufs; ++s)
+            mbar_init(&sm.p_full[s], kSoftWarps);
+        mbar_init(&sm.drained, 1);
+        fence_mbar_init();
+    }
+    if (warp == kMmaWarp) {                  // the MMA warp owns the tensor memory
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&sm.tmem)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sm.tmem;
     int ctx = a.ctx[b];
     if (ctx < 0 || ctx > a.max_pages * kPage) {
         if (a.dev_err && split == 0 && blockIdx.y == 0 && tid == 0)
             atomicOr(a.dev_err, LYNX_DEVERR_CTX);
         ctx = min(max(ctx, 0), a.max_pages * kPage);
     }
-
-    // this lane's two query rows (r = position * G + head in group); a row past
-    // the block is padding: zero query, nothing visible, never written
-    int rowi[2], rowh[2], nvis[2];
-    bool rowok[2];
+    // softmax thread: query row rl of this block (draft position pos, head h)
+    const int rl = 32 * (warp & 3) + lane, r = rb * kRows + rl;
+    const bool rowok = warp < kSoftWarps && r < Tq * G;
+    const int pos = rowok ? r / G : 0, h = kvh * G + (rowok ? r % G : 0);
+    const uint32_t trow = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+    if (warp < kSoftWarps) {                 // Q (scaled to log2 units) hi / lo and O = 0 into tensor memory
+        const float qscale = a.sm_scale * kLog2e;
+        const uint16_t *qrow = a.q + (((int64_t)b * Tq + pos) * a.Hq + h) * kD;
 #pragma unroll
-    for (int e = 0; e < 2; ++e) {
-        const int r = rb * kRows + warp * 16 + g + 8 * e;
-        rowok[e] = r < Tq * G;
-        rowi[e] = rowok[e] ? r / G : 0;
-        rowh[e] = kvh * G + (rowok[e] ? r % G : 0);
-        nvis[e] = rowok[e] ? ctx - Tq + rowi[e] + 1 : 0;   // draft position i sees tokens < nvis
-    }
-    // query fragments (hi and lo), scaled by sm_scale log2(e)
-    const float qscale = a.sm_scale * kLog2e;
-    uint32_t QH[8][4], QL[8][4];
+        for (int grp = 0; grp < 2; ++grp) {
+            uint32_t hi[32], lo[32];
 #pragma unroll
-    for (int ks = 0; ks < 8; ++ks)
+            for (int w8 = 0; w8 < 8; ++w8) {
+                const uint4 w = rowok ? *reinterpret_cast<const uint4 *>(qrow + 64 * grp + 8 * w8) : make_uint4(0, 0, 0, 0);
+                const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-        for (int f = 0; f < 4; ++f) {
-            const int e = f & 1, coff = (f >> 1) * 8;
-            float2 x = make_float2(0.0f, 0.0f);
-            if (rowok[e]) {
-                const uint32_t w = *reinterpret_cast<const uint32_t *>(
-                    a.q + (((int64_t)b * Tq + rowi[e]) * a.Hq + rowh[e]) * kD + 16 * ks + coff + 2 * q);
-                x = make_float2(bf16_lo(w) * qscale, bf16_hi(w) * qscale);
+                for (int i = 0; i < 4; ++i)
+                    split2(make_float2(bf16_lo(ws[i]) * qscale, bf16_hi(ws[i]) * qscale), hi[4 * w8 + i], lo[4 * w8 + i]);
             }
-            split2(x, QH[ks][f], QL[ks][f]);
+            tmem_st32u(trow + kColQ + 32 * grp, hi);
+            tmem_st32u(trow + kColQ + 64 + 32 * grp, lo);
         }
+        float z[32];
+#pragma unroll
+        for (int k = 0; k < 32; ++k)
+            z[k] = 0.0f;
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            tmem_st32(trow + kColO + 32 * k, z);
+        tmem_wait_st();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
 
     const int p_begin = split * a.pages_per_split;
     const int p_end = min(p_begin + a.pages_per_split, a.max_pages);
     const int p_live = min(p_end, (ctx + kPage - 1) / kPage);
     const int np = max(p_live - p_begin, 0);
-    const uint8_t *ka = a.ka + (int64_t)kvh * T * kRow, *va = a.va + (int64_t)kvh * T * kRow;
-    const uint8_t *kr = FULL ? a.kr + (int64_t)kvh * T * kRow : nullptr;
-    const uint8_t *vr = FULL ? a.vr + (int64_t)kvh * T * kRow : nullptr;
-    const float *kpm = a.kpm + (int64_t)kvh * a.pool_pages * (2 * kD);
-    const float *vpm = a.vpm + (int64_t)kvh * a.pool_pages * (2 * kD);
-    const uint16_t *kcm = a.kcm + (int64_t)kvh * a.pool_pages * (kNChunk * 2 * kD);
-    const uint16_t *vcm = a.vcm + (int64_t)kvh * a.pool_pages * (kNChunk * 2 * kD);
-
+    const int nch = kNChunk * np;
     auto phys_of = [&](int i) -> int {
         const int p = a.page_table[(int64_t)b * a.max_pages + p_begin + i];
         return (p >= 0 && p < a.pool_pages) ? p : -1;
     };
-    // page i of the range into buffer i & 1 (thread 0); an invalid page
-    // completes the phase without data and is skipped
-    int last_issued = -1;           // thread 0: the last page whose copies were issued
-    auto issue = [&](int i) {
-        const int buf = i & 1, p = phys_of(i);
-        uint64_t *bar = &sm.bar[buf];
-        if (p < 0) {
-            if (a.dev_err)
-                atomicOr(a.dev_err, LYNX_DEVERR_PAGE);
-            asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-            return;
-        }
-        last_issued = i;
-        if (i >= 2)
-            fence_proxy_async_smem();   // the buffer's previous page was read through the generic proxy
-        mbar_arrive_expect_tx(bar, 2u * ((FULL ? 2u : 1u) * kPlane + 2 * kD * 4 + kNChunk * 2 * kD * 2));
-        const int64_t off = (int64_t)p * kPlane;
-        bulk_g2s(sm.k[buf].a, ka + off, kPlane, bar);
-        bulk_g2s(sm.v[buf].a, va + off, kPlane, bar);
-        if (FULL) {
-            bulk_g2s(sm.k[buf].r, kr + off, kPlane, bar);
-            bulk_g2s(sm.v[buf].r, vr + off, kPlane, bar);
-        }
-        bulk_g2s(sm.k[buf].pm, kpm + (int64_t)p * (2 * kD), 2 * kD * 4, bar);
-        bulk_g2s(sm.v[buf].pm, vpm + (int64_t)p * (2 * kD), 2 * kD * 4, bar);
-        bulk_g2s(sm.k[buf].cm, kcm + (int64_t)p * (kNChunk * 2 * kD), kNChunk * 2 * kD * 2, bar);
-        bulk_g2s(sm.v[buf].cm, vcm + (int64_t)p * (kNChunk * 2 * kD), kNChunk * 2 * kD * 2, bar);
-    };
-    __syncthreads();
-    if (tid == 0 && np > 0)
-        issue(0);
-
-    float m_run[2] = {neg_inf(), neg_inf()}, l_run[2] = {0.0f, 0.0f};
-    float O[16][4];
-#pragma unroll
-    for (int nt = 0; nt < 16; ++nt)
-        O[nt][0] = O[nt][1] = O[nt][2] = O[nt][3] = 0.0f;
-
-    // chunk c = chunk c % 8 of page c / 8: decode chunk c + 1 into tile buffer
-    // (c + 1) & 1 while the warps run chunk c from buffer c & 1
-    const int nchunks = kNChunk * np;
     bool timed_out = false;
-    bool pvalid = false;            // whether the page of the chunk being decoded holds data
-    auto decode = [&](int c) -> bool {
-        const int i = c >> 3, j = c & 7;
-        if (j == 0) {
-            if (tid == 0 && i + 1 < np)
-                issue(i + 1);       // its buffer held page i - 1, fully decoded by now
-            const bool ok = mbar_wait_bounded(&sm.bar[i & 1], (uint32_t)((i >> 1) & 1), kWaitLimit);
-            if (__syncthreads_or(!ok))
-                return false;
-            pvalid = phys_of(i) >= 0;
-        }
-        if (pvalid) {
-            uint8_t(&tl)[4][kTile] = sm.tile[c & 1];
-            decode_chunk<FULL>(sm.k[i & 1], j, sm.lev, tl[0], tl[1], tid);
-            decode_chunk<FULL>(sm.v[i & 1], j, sm.lev, tl[2], tl[3], tid);
-        }
-        return true;
-    };
-    bool cvalid_next = false;
-    if (nchunks > 0) {
-        timed_out = !decode(0);
-        cvalid_next = pvalid;
-    }
-    __syncthreads();
-    for (int c = 0; c < nchunks && !timed_out; ++c) {
-        const bool cvalid = cvalid_next;
-        if (c + 1 < nchunks) {
-            timed_out = !decode(c + 1);
-            cvalid_next = pvalid;
-            if (timed_out)
-                break;
-        }
-        const int t0 = (p_begin + (c >> 3)) * kPage + (c & 7) * kChunk;   // first token of chunk c
-        // a warp none of whose rows sees the chunk skips it
-        const bool seen = __any_sync(0xFFFFFFFFu, t0 < max(nvis[0], nvis[1]));
-        if (cvalid && seen) {
-            const uint32_t kh = smem_u32(sm.tile[c & 1][0]), kl = smem_u32(sm.tile[c & 1][1]);
-            const uint32_t vh = smem_u32(sm.tile[c & 1][2]), vl = smem_u32(sm.tile[c & 1][3]);
-            // ---- S = Q.K^T over the chunk's 32 tokens (four n-tiles of 8)
-            float S[4][4];
-#pragma unroll
-            for (int nt = 0; nt < 4; ++nt)
-                S[nt][0] = S[nt][1] = S[nt][2] = S[nt][3] = 0.0f;
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks)
-#pragma unroll
-                for (int pp = 0; pp < 2; ++pp) {
-                    // matrices (n-tile 2pp + m / 2, k-half m % 2) of 8 tokens x 8 channels
-                    const uint32_t off = tile_off(8 * (2 * pp + (lm >> 1)) + lr, 2 * ks + (lm & 1));
-                    uint32_t bh[4], bl[4];
-                    ldsm_x4(kh + off, bh);
-                    ldsm_x4(kl + off, bl);
-                    mma16816(S[2 * pp], QH[ks], bh[0], bh[1]);
-                    mma16816(S[2 * pp + 1], QH[ks], bh[2], bh[3]);
-                    mma16816(S[2 * pp], QH[ks], bl[0], bl[1]);
-                    mma16816(S[2 * pp + 1], QH[ks], bl[2], bl[3]);
-                    mma16816(S[2 * pp], QL[ks], bh[0], bh[1]);
-                    mma16816(S[2 * pp + 1], QL[ks], bh[2], bh[3]);
-                }
-            // ---- causal mask and online softmax of rows g (e = 0) and g + 8 (e = 1)
-            float mx[2] = {neg_inf(), neg_inf()};
-#pragma unroll
-            for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-                for (int f = 0; f < 4; ++f) {
-                    const int e = f >> 1;
-                    const int tok = t0 + 8 * nt + 2 * q + (f & 1);
-                    if (tok >= nvis[e])
-                        S[nt][f] = neg_inf();
-                    mx[e] = fmaxf(mx[e], S[nt][f]);
-                }
-            float scale[2];
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                mx[e] = fmaxf(mx[e], __shfl_xor_sync(0xFFFFFFFFu, mx[e], 1));
-                mx[e] = fmaxf(mx[e], __shfl_xor_sync(0xFFFFFFFFu, mx[e], 2));
-                // the reference moves only when a score passes it by 2^8
-                const bool up = mx[e] > m_run[e] + 8.0f;
-                const float m_new = up ? mx[e] : m_run[e];
-                scale[e] = up ? exp2_sm(m_run[e] - m_new) : 1.0f;
-                m_run[e] = m_new;
-                l_run[e] *= scale[e];
-            }
-            if (__any_sync(0xFFFFFFFFu, scale[0] != 1.0f || scale[1] != 1.0f)) {
-#pragma unroll
-                for (int nt = 0; nt < 16; ++nt) {
-                    O[nt][0] *= scale[0];
-                    O[nt][1] *= scale[0];
-                    O[nt][2] *= scale[1];
-                    O[nt][3] *= scale[1];
-                }
-            }
-            uint32_t PH[2][4], PL[2][4];
-#pragma unroll
-            for (int nt = 0; nt < 4; ++nt) {
-                float p[4];
-#pragma unroll
-                for (int f = 0; f < 4; ++f) {
-                    const int e = f >> 1;
-                    p[f] = m_run[e] == neg_inf() ? 0.0f : exp2_sm(S[nt][f] - m_run[e]);
-                    l_run[e] += p[f];
-                }
-                // A fragment of k-step nt / 2: rows g, g + 8 and tokens 2q (+8 for odd nt)
-                const int kk = nt >> 1, hf = (nt & 1) * 2;
-                split2(make_float2(p[0], p[1]), PH[kk][hf], PL[kk][hf]);
-                split2(make_float2(p[2], p[3]), PH[kk][hf + 1], PL[kk][hf + 1]);
-            }
-            // ---- O += P.V (sixteen n-tiles of 8 channels)
-#pragma unroll
-            for (int pp = 0; pp < 8; ++pp)
-#pragma unroll
-                for (int kk = 0; kk < 2; ++kk) {
-                    // matrices (tokens 16 kk + 8 (m % 2) .., channels of n-tile 2pp + m / 2), transposed
-                    const uint32_t off = tile_off(16 * kk + 8 * (lm & 1) + lr, 2 * pp + (lm >> 1));
-                    uint32_t bh[4], bl[4];
-                    ldsm_x4_trans(vh + off, bh);
-                    ldsm_x4_trans(vl + off, bl);
-                    mma16816(O[2 * pp], PH[kk], bh[0], bh[1]);
-                    mma16816(O[2 * pp + 1], PH[kk], bh[2], bh[3]);
-                    mma16816(O[2 * pp], PH[kk], bl[0], bl[1]);
-                    mma16816(O[2 * pp + 1], PH[kk], bl[2], bl[3]);
-                    mma16816(O[2 * pp], PL[kk], bh[0], bh[1]);
-                    mma16816(O[2 * pp + 1], PL[kk], bh[2], bh[3]);
-                }
-        }
-        __syncthreads();   // chunk c's tiles are free for chunk c + 2
-    }
-    if (timed_out) {
-        if (tid == 0) {
-            // let a copy still in flight land (bounded) before the CTA ends
-            if (last_issued >= 0)
-                mbar_wait_bounded(&sm.bar[last_issued & 1], (uint32_t)((last_issued >> 1) & 1), kWaitLimit);
-            if (a.dev_err)
-                atomicOr(a.dev_err, LYNX_DEVERR_TIMEOUT);
-        }
-    }
 
-    // ---- this range's partial of each row
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-        float l = l_run[e];
-        l += __shfl_xor_sync(0xFFFFFFFFu, l, 1);
-        l += __shfl_xor_sync(0xFFFFFFFFu, l, 2);
-        if (!rowok[e])
-            continue;
-        float *part = a.part + ((((int64_t)b * Tq + rowi[e]) * a.Hq + rowh[e]) * a.n_splits + split) * kPart;
-#pragma unroll
-        for (int nt = 0; nt < 16; ++nt)
-            *reinterpret_cast<float2 *>(part + 8 * nt + 2 * q) = make_float2(O[nt][2 * e], O[nt][2 * e + 1]);
-        if (q == 0) {
-            part[kD] = m_run[e];
-            part[kD + 1] = l;
+    if (warp == kProdWarp) {
+        // ---- producer: chunk codes into the ring of slots by bulk copy --------
+        if (lane == 0) {
+            int cur_i = -1, cur_p = -1;
+            for (int c = 0; c < nch; ++c) {
+                const int s = c % kRing, i = c >> 3, j = c & 7;
+                // slot s was last decoded for chunk c - kRing
+                if (c >= kRing && !mbar_wait_bounded(&sm.slot_free[s], (uint32_t)(((c - kRing) / kRing) & 1), kWaitLimit)) {
+                    timed_out = true;
+                    break;
+                }
+                if (i != cur_i) {            // one page-table read a page
+                    cur_i = i;
+                    cur_p = phys_of(i);
+                    if (cur_p < 0 && a.dev_err)
+                        atomicOr(a.dev_err, LYNX_DEVERR_PAGE);
+                }
+                Slot<FULL> &sl = sm.slot[s];
+                uint64_t *bar = &sm.ring_full[s];
+                sm.slot_page[s] = cur_p;
+                if (cur_p < 0) {
+                    mbar_arrive(bar);
+                    continue;
+                }
+                fence_proxy_async_smem();    // the decoders' reads of the slot come before the copies' writes
+                const int64_t rows = ((int64_t)kvh * T + (int64_t)cur_p * kPage + j * kChunk) * kRow;
+                const int64_t pmo = ((int64_t)kvh * a.pool_pages + cur_p) * (2 * kD);
+                const int64_t cmo = (((int64_t)kvh * a.pool_pages + cur_p) * kNChunk + j) * (2 * kD);
+                mbar_arrive_expect_tx(bar, (FULL ? 4u : 2u) * kChunk * kRow + 2 * (2 * kD * 4) + 2 * (2 * kD * 2));
+                bulk_g2s(sl.ka, a.ka + rows, kChunk * kRow, bar);
+                bulk_g2s(sl.va, a.va + rows, kChunk * kRow, bar);
+                if (FULL) {
+                    bulk_g2s(sl.kr, a.kr + rows, kChunk * kRow, bar);
+                    bulk_g2s(sl.vr, a.vr + rows, kChunk * kRow, bar);
+                }
+                bulk_g2s(sl.kpm, a.kpm + pmo, 2 * kD * 4, bar);
+                bulk_g2s(sl.vpm, a.vpm + pmo, 2 * kD * 4, bar);
+                bulk_g2s(sl.kcm, a.kcm + cmo, 2 * kD * 2, bar);
+                bulk_g2s(sl.vcm, a.vcm + cmo, 2 * kD * 2, bar);
+            }
+            // let every copy issued land before the CTA exits (bounded)
+            for (int c = max(nch - kRing, 0); c < nch; ++c)
+                mbar_wait_bounded(&sm.ring_full[c % kRing], (uint32_t)((c / kRing) & 1), kWaitLimit);
         }
+    } else if (warp >= kSoftWarps && warp < kMmaWarp) {
+        // ---- decode warps ----------------------------------------------------
+        const int u = 32 * (warp - kSoftWarps) + lane;
+        const float *lv = sm.lev + lane;
+        for (int c = 0; c < nch; ++c) {
+            const int s = c % kRing, buf = c % kBufs;
+            const uint32_t prev = (uint32_t)(((c - kBufs) / kBufs) & 1);
+            // codes in; K tile `buf` last read by the Q.K^T of chunk c - kBufs
+            bool ok = mbar_wait_bounded(&sm.ring_full[s], (uint32_t)((c / kRing) & 1), kWaitLimit);
+            if (ok && c >= kBufs)
+                ok = mbar_wait_bounded(&sm.s_full[buf], prev, kWaitLimit);
+            if (!__all_sync(0xFFFFFFFFu, ok)) {
+                timed_out = true;
+                break;
+            }
+            tc_fence_after();
+            const bool valid = sm.slot_page[s] >= 0;
+            decode_k<FULL>(sm.slot[s], valid, lv, sm.k[buf], u);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&sm.k_full[buf]);
+            // V tile `buf` last read by the P.V of chunk c - kBufs
+            if (c >= kBufs && !__all_sync(0xFFFFFFFFu, mbar_wait_bounded(&sm.pv_done[buf], prev, kWaitLimit))) {
+                timed_out = true;
+                break;
+            }
+            tc_fence_after();
+            decode_v<FULL>(sm.slot[s], valid, lv, sm.v[buf], u);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&sm.v_full[buf]);
+                mbar_arrive(&sm.slot_free[s]);
+            }
+        }
+    } else if (warp == kMmaWarp) {
+        // ---- MMA warp: one thread issues every tcgen05.mma in a fixed order,
+        // S = Q.K^T of chunk c + 1 (as soon as its K tile is decoded), then
+        // O += P.V of chunk c (as soon as its P is written and its V tile
+        // decoded); each wait blocks in hardware (bounded)
+        if (lane == 0 && nch > 0) {
+            // Q_hi against the stacked [K_hi; K_lo] (64 rows) gives both cross
+            // terms in one product: columns 0-31 Q_hi.K_hi, 32-63 Q_hi.K_lo;
+            // Q_lo.K_hi accumulates into columns 0-31
+            constexpr uint32_t id64 = idesc_f16(kRows, 2 * kChunk), id32 = idesc_f16(kRows, kChunk);
+            constexpr uint32_t idpv = idesc_f16(kRows, kD);
+            const uint32_t tO = tmem + kColO, tQh = tmem + kColQ, tQl = tmem + kColQ + kD / 2;
+            const uint32_t k0 = smem_u32(sm.k), v0 = smem_u32(sm.v);
+            auto issue_qk = [&](int c) -> bool {
+                const int buf = c % kBufs;
+                if (!mbar_wait_bounded(&sm.k_full[buf], (uint32_t)((c / kBufs) & 1), kWaitLimit))
+                    return false;
+                if (c >= kBufs && !mbar_wait_bounded(&sm.s_free[buf], (uint32_t)(((c - kBufs) / kBufs) & 1), kWaitLimit))
+                    return false;
+                tc_fence_after();
+                const uint32_t tS = tmem + kColS + 64u * buf;
+                const uint32_t kb = k0 + (uint32_t)buf * (uint32_t)sizeof(sm.k[0]);
+#pragma unroll
+                for (int st = 0; st < 8; ++st) {  // 16 channels a step: 8 columns of Q, 32 bytes of a K row
+                    const uint64_t kd = sdesc(kb + (uint32_t)(st >> 2) * (uint32_t)sizeof(sm.k[0][0]) + 32 * (st & 3), 1024, 2);
+                    umma_ts(tS, tQh + 8 * st, kd, id64, st > 0 ? 1u : 0u);
+                    umma_ts(tS, tQl + 8 * st, kd, id32, 1u);
+                }
+                umma_commit(&sm.s_full[buf]);
+                return true;
+            };
+            bool ok = issue_qk(0);
+            for (int c = 0; ok && c < nch; ++c) {
+                if (c + 1 < nch && !(ok = issue_qk(c + 1)))
+                    break;
+                const int buf = c % kBufs, pb = c % kPBufs;
+                ok = mbar_wait_bounded(&sm.p_full[pb], (uint32_t)((c / kPBufs) & 1), kWaitLimit) &&
+                     mbar_wait_bounded(&sm.v_full[buf], (uint32_t)((c / kBufs) & 1), kWaitLimit);
+                if (!ok)
+                    break;
+                tc_fence_after();
+                const uint32_t tPh = tmem + kColP + 32u * pb, tPl = tPh + 16;
+                const uint32_t vb = v0 + (uint32_t)buf * (uint32_t)sizeof(sm.v[0]);
+#pragma unroll
+                for (int kk = 0; kk < 2; ++kk) {  // 16 tokens a step: 8 columns of P, 32 bytes of a V^T row
+                    const uint64_t vh = sdesc(vb + 32 * kk, 512, 4);
+                    const uint64_t vl = sdesc(vb + (uint32_t)sizeof(sm.v[0][0]) + 32 * kk, 512, 4);
+                    umma_ts(tO, tPh + 8 * kk, vh, idpv, 1u);
+                    umma_ts(tO, tPh + 8 * kk, vl, idpv, 1u);
+                    umma_ts(tO, tPl + 8 * kk, vh, idpv, 1u);
+                }
+                umma_commit(&sm.pv_done[buf]);
+            }
+            timed_out = !ok;
+            // every MMA issued must finish before the tensor memory is freed
+            // (the commit tracks all of this thread's earlier MMAs; bounded)
+            umma_commit(&sm.drained);
+            mbar_wait_bounded(&sm.drained, 0u, kWaitLimit);
+        }
+    } else {
+        // ---- softmax warps: one query row per thread -------------------------
+        const int nvis = rowok ? ctx - Tq + pos + 1 : 0;           // tokens this draft position sees
+        // chunks wholly inside every row's view need no mask
+        const int vis_all = ctx - Tq + 1;
+        int vpage = -1;
+        bool pvalid = false;
+        float m_run = neg_inf(), l_run = 0.0f;
+        for (int c = 0; c < nch; ++c) {
+            const int buf = c % kBufs, pb = c % kPBufs;
+            if (!mbar_wait_bounded(&sm.s_full[buf], (uint32_t)((c / kBufs) & 1), kWaitLimit)) {
+                timed_out = true;
+                break;
+            }
+            tc_fence_after();
+            float S[32], S2[32];
+            tmem_ld32(trow + kColS + 64 * buf, S);
+            tmem_ld32(trow + kColS + 64 * buf + 32, S2);
+            tmem_wait_ld();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&sm.s_free[buf]);
+            const int t0 = (p_begin + (c >> 3)) * kPage + (c & 7) * kChunk;
+            if ((c >> 3) != vpage) {         // one page-table read a page
+                vpage = c >> 3;
+                pvalid = phys_of(vpage) >= 0;
+            }
+            const bool valid = pvalid;
+            float mx = neg_inf();
+            if (valid && t0 + kChunk <= vis_all) {
+#pragma unroll
+                for (int k = 0; k < 32; ++k) {
+                    S[k] += S2[k];
+                    mx = fmaxf(mx, S[k]);
+                }
+            } else {
+#pragma unroll
+                for (int k = 0; k < 32; ++k) {
+                    S[k] = (!valid || t0 + k >= nvis) ? neg_inf() : S[k] + S2[k];
+                    mx = fmaxf(mx, S[k]);
+                }
+            }
+            // the reference moves only when a score passes it by 2^8 (weights
+            // up to 2^8 are exact in fp32 and fine in fp16)
+            const bool up = mx > m_run + 8.0f;
+            if (__any_sync(0xFFFFFFFFu, up)) {
+                // rare: rescale this row's output, complete up to chunk c - 1
+                if (c >= 1 && !mbar_wait_bounded(&sm.pv_done[(c - 1) % kBufs], (uint32_t)(((c - 1) / kBufs) & 1),
+                                                  kWaitLimit)) {
+                    timed_out = true;
+                    break;
+                }
+                tc_fence_after();
+                const float alpha = up ? (m_run == neg_inf() ? 0.0f : exp2_sm(m_run - mx)) : 1.0f;
+                if (up) {
+                    m_run = mx;
+                    l_run *= alpha;
+                }
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    float o[32];
+                    tmem_ld32(trow + kColO + 32 * k, o);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        o[e] *= alpha;
+                    tmem_st32(trow + kColO + 32 * k, o);
+                }
+                tmem_wait_st();
+            }
+            // P buffer `pb` was last read by the P.V of chunk c - kPBufs
+            if (c >= kPBufs && !mbar_wait_bounded(&sm.pv_done[(c - kPBufs) % kBufs],
+                                                  (uint32_t)(((c - kPBufs) / kBufs) & 1), kWaitLimit)) {
+                timed_out = true;
+                break;
+            }
+            tc_fence_after();
+            // m_run is -inf only while every score so far (this chunk's too) is
+            // masked: then every weight is exp2(-inf) = 0
+            const float m_eff = m_run == neg_inf() ? 0.0f : m_run;
+            uint32_t ph[16], pl[16];
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                const float p0 = exp2_sm(S[2 * k] - m_eff), p1 = exp2_sm(S[2 * k + 1] - m_eff);
+                l_run += p0 + p1;
+                split2(make_float2(p0, p1), ph[k], pl[k]);
+            }
+            tmem_st16(trow + kColP + 32 * pb, ph);
+            tmem_st16(trow + kColP + 32 * pb + 16, pl);
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&sm.p_full[pb]);
+        }
+        // ---- this range's partial of the row
+        if (!timed_out && nch > 0 &&
+            !mbar_wait_bounded(&sm.pv_done[(nch - 1) % kBufs], (uint32_t)(((nch - 1) / kBufs) & 1), kWaitLimit))
+            timed_out = true;
+        tc_fence_after();
+        float *part = a.part + ((((int64_t)b * Tq + pos) * a.Hq + h) * a.n_splits + split) * kPart;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            float o[32];
+            tmem_ld32(trow + kColO + 32 * k, o);
+            tmem_wait_ld();
+            if (rowok)                       // a partial is 130 floats: 8-byte aligned
+#pragma unroll
+                for (int e = 0; e < 32; e += 2)
+                    *reinterpret_cast<float2 *>(part + 32 * k + e) = make_float2(o[e], o[e + 1]);
+        }
+        if (rowok) {
+            part[kD] = m_run;
+            part[kD + 1] = l_run;
+        }
+    }
+    if (timed_out && a.dev_err)
+        atomicOr(a.dev_err, LYNX_DEVERR_TIMEOUT);
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
     }
 }
 
@@ -413,6 +703,14 @@ template <bool FULL>
 cudaError_t run(const VerifyArgs &a, cudaStream_t s)
 {
     static_assert(sizeof(Smem<FULL>) <= 227 * 1024, "shared memory per CTA");
+    // bulk copies land on 16-byte boundaries; swizzled tiles start on 1024 bytes
+    static_assert(sizeof(Slot<FULL>) % 16 == 0 && offsetof(Slot<FULL>, kpm) % 16 == 0 &&
+                      offsetof(Slot<FULL>, vpm) % 16 == 0 && offsetof(Slot<FULL>, kcm) % 16 == 0 &&
+                      offsetof(Slot<FULL>, vcm) % 16 == 0 && offsetof(Slot<FULL>, vr) % 16 == 0,
+                  "slot layout");
+    static_assert(offsetof(Smem<FULL>, k) % 1024 == 0 && offsetof(Smem<FULL>, v) % 1024 == 0 &&
+                      offsetof(Smem<FULL>, slot) % 16 == 0,
+                  "tile layout");
     const size_t smem = sizeof(Smem<FULL>);
     cudaError_t e = cudaFuncSetAttribute(verify_kernel<FULL>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess)
