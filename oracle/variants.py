@@ -29,10 +29,10 @@ Readings (where the pages leave a step open):
 - no bias: the cut is a plain floor (the residual is one-sided, which is what
   the page says the bias avoids), anchor-only decoding still takes 2^r A;
 - no sign-aware mapping: c = -q for w < 0 (small negatives collapse to 0);
-- uniform INTb comparator: per (page, channel) min and range, 2^b levels,
-  code = floor((x - mn) * ((2^b - 1) / rng) + 1/2) with every step in fp32
-  (the integer decision is taken in the precision the GPU takes it), decoded
-  in fp64;
+- uniform INTb comparator: per (page, channel) min and range (or per token,
+  over its 128 channels), 2^b levels, code = floor((x - mn) * ((2^b - 1) /
+  rng) + 1/2) with every step in fp32 (the integer decision is taken in the
+  precision the GPU takes it), decoded in fp64;
 - vNMSE: sum (x_hat - x)^2 / sum x^2 over the tensor.
 
 The encoder follows the same numeric contract as the main oracle: fp32 with
@@ -71,6 +71,7 @@ class Variant:
     bias: bool = True
     sign_aware: bool = True
     uniform_bits: int = 0           # > 0: the uniform INTb comparator instead of the method
+    uniform_per_token: bool = False # comparator grid per token (over its 128 channels), not per (page, channel)
 
     @property
     def qmax(self) -> int:
@@ -210,17 +211,24 @@ def _decode(mn, rng, mu_bits, s_bits, c, v: Variant) -> np.ndarray:
 
 
 def _uniform(x: np.ndarray, v: Variant):
-    """The uniform comparator: per (page, channel) min-max grid of 2^b levels."""
+    """The uniform comparator: min-max grid of 2^b levels per (page, channel),
+    or per token. Returns (mn, rng) of shape [P, 128] per (page, channel), or
+    [P, 256, 1] per token."""
     f32 = np.float32
-    mn, rng, _ = _stage1(x, Variant())
+    if v.uniform_per_token:
+        mn, rng, _ = _stage1(np.swapaxes(x, 1, 2), Variant())        # tokens as channels
+        mn, rng = mn[:, :, None], rng[:, :, None]
+    else:
+        mn, rng, _ = _stage1(x, Variant())
+        mn, rng = mn[:, None, :], rng[:, None, :]
     top = f32((1 << v.uniform_bits) - 1)
     with np.errstate(divide="ignore", invalid="ignore", over="ignore"):
         inv_step = np.where(rng > 0, top / np.where(rng > 0, rng, f32(1.0)), f32(0.0)).astype(f32)
-        t = ((x - mn[:, None, :]) * inv_step[:, None, :]).astype(f32)
+        t = ((x - mn) * inv_step).astype(f32)
         code = np.floor((t + f32(0.5)).astype(f32))
     code = np.clip(np.nan_to_num(code, nan=0.0), 0, float(top)).astype(np.int32)
     step = rng.astype(np.float64) / float(top)
-    xh = mn.astype(np.float64)[:, None, :] + code * step[:, None, :]
+    xh = mn.astype(np.float64) + code * step
     return mn, rng, code, xh
 
 
@@ -241,6 +249,10 @@ def encode(x_bf16, v: Variant = Variant()) -> dict:
         mn, rng, code, xh = _uniform(xp, v)
         out["codes"] = code.reshape(N, T, D)
         xa = xf = xh
+        if v.uniform_per_token:                     # no per-(page, channel) metadata
+            mn, rng = np.zeros((N * P, D), np.float32), np.zeros((N * P, D), np.float32)
+        else:
+            mn, rng = mn[:, 0, :], rng[:, 0, :]
     else:
         assert v.chunk in (16, 32, 64) and 1 <= v.residual_bits <= 4 and 1 <= v.anchor_bits <= 6
         assert v.anchor_bits + v.residual_bits <= 8

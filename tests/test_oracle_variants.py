@@ -172,3 +172,17 @@ def test_chunk_statistics_against_fp64(xb, C):
     assert np.all(np.abs(mu - uc.mean(axis=3)) <= ulp * 0.5 + 1e-6)
     dev = np.abs(uc - mu[:, :, :, None, :]).max(axis=3)
     assert np.all(s >= dev * (1 - 1e-6)) and np.all(s <= dev * (1 + 2.0 ** -10) + 2.0 ** -24)
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+def test_uniform_per_token_half_step(xb, bits):
+    o = V.encode(xb, V.Variant(uniform_bits=bits, uniform_per_token=True))
+    x = (xb.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    step = (x.max(axis=-1) - x.min(axis=-1)) / (2 ** bits - 1)
+    e = np.abs(o["x_full"] - x)
+    assert np.all(e <= step[..., None] * (0.5 + 1e-5) + 1e-12)
+    c = o["codes"]
+    assert np.all(c.min(axis=-1) == 0) and np.all(c.max(axis=-1) == 2 ** bits - 1)
+    # outlier channels widen every token's grid: per token is coarser here
+    per_chan = V.vnmse(V.encode(xb, V.Variant(uniform_bits=bits))["err"])[1]
+    assert V.vnmse(o["err"])[1] > per_chan
