@@ -623,6 +623,101 @@ def verify_report(args):
         "acceptance_proxy_mean": float(agree.mean()), "cpu_baseline": cpu}))
 
 
+ABLATION = [
+    ("lynx (C=32, 4+4, alpha=255)", {}),
+    ("C=16", {"chunk": 16}), ("C=64", {"chunk": 64}),
+    ("alpha=15", {"alpha": 15.0}), ("alpha=63", {"alpha": 63.0}), ("alpha=1023", {"alpha": 1023.0}),
+    ("split 2+4 (6-bit codes)", {"anchor_bits": 2, "residual_bits": 4}),
+    ("split 3+3 (6-bit codes)", {"anchor_bits": 3, "residual_bits": 3}),
+    ("split 6+2", {"anchor_bits": 6, "residual_bits": 2}),
+    ("no page normalisation", {"flags": 1}), ("no chunk isolation", {"flags": 2}),
+    ("no log map (linear grid)", {"alpha": 0.0}), ("no bias", {"flags": 4}), ("no sign-aware mapping", {"flags": 8}),
+    ("lynx 4-bit code (split 2+2)", {"anchor_bits": 2, "residual_bits": 2}),
+    ("uniform INT4 per page-channel", {"uniform_bits": 4}), ("uniform INT8 per page-channel", {"uniform_bits": 8}),
+    ("uniform INT4 per token", {"uniform_bits": 4, "flags": 16}),
+    ("uniform INT8 per token", {"uniform_bits": 8, "flags": 16}),
+]
+
+
+def ablation_report(args):
+    """Section 7's unmeasured knobs on synthetic data: vNMSE (sum (x_hat - x)^2
+    / sum x^2) of the anchor-only and the full reconstruction for each variant
+    of the quantizer and for the uniform comparators, on the K and V of the
+    Qwen3-235B-like layer (4 KV heads x 32K tokens, Laplace with outlier
+    channels), and the variant encoder's throughput on 2 layers of the full
+    cache's shape (268 MB of bf16 per tensor, larger than L2)."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    import progressive_kv_cache_gb300 as lx
+
+    w = S.WORKLOADS[2]
+    dev = torch.device("cuda")
+    gen = S.DeviceGenerator()
+    xs = {}
+    for s_ in (S.S_K, S.S_V):
+        xs[s_] = torch.empty((1, w.H, w.T, D), dtype=torch.bfloat16, device=dev)
+        gen.fill(xs[s_], w.key(s_), w.scales(s_))
+    rows = []
+    for name, kw in ABLATION:
+        r = {"name": name, "knobs": kw}
+        for s_, lab in ((S.S_K, "k"), (S.S_V, "v")):
+            e = lx.quantize_variant(xs[s_], **kw)["err"].sum(dim=(0, 1)).cpu().numpy()
+            r[lab] = {"anchor": float(e[1] / e[0]), "full": float(e[2] / e[0])}
+        rows.append(r)
+    by = {r["name"]: r for r in rows}
+    ratio = {  # vNMSE of uniform INT4 / vNMSE of a Lynx reconstruction from 4 bits a value
+        f"{u} / lynx {lab_l}": {t: by[u][t]["full"] / by[l][t][part] for t in ("k", "v")}
+        for u in ("uniform INT4 per page-channel", "uniform INT4 per token")
+        for lab_l, l, part in (("anchor-only of 4+4", "lynx (C=32, 4+4, alpha=255)", "anchor"),
+                               ("4-bit code (2+2)", "lynx 4-bit code (split 2+2)", "full"))}
+    del xs
+    # throughput: the base variant and the comparator, errors only
+    wt = S.WORKLOADS[3]
+    big = torch.empty((2, wt.H, wt.T, D), dtype=torch.bfloat16, device=dev)
+    gen.fill(big, wt.key(S.S_K), wt.scales(S.S_K)[:2])
+    elems = big.numel()
+    hbm, kind = peaks()
+    timing = {}
+    for name, kw in (("lynx", {}), ("C=16", {"chunk": 16}), ("C=64", {"chunk": 64}), ("uniform INT4", {"uniform_bits": 4})):
+        for _ in range(max(args.warmup, 3)):
+            lx.quantize_variant(big, **kw)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with ClockSampler(0) as clk:
+            e0.record()
+            for _ in range(args.steps):
+                lx.quantize_variant(big, **kw)
+            e1.record()
+            torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / args.steps
+        timing[name] = {"ms": ms, "gbs": 2.0 * elems / (ms * 1e-3) / 1e9, "clocks": clk.summary()}
+    cpu = None
+    if not args.no_cpu_baseline:
+        from oracle import variants as V
+        xc = S.laplace_bf16(w.key(S.S_K), w.scales(S.S_K), 1, w.H, w.T, heads=[0], t0=0, t1=4096)
+        xc = xc.reshape(1, 4096, D)
+        t0 = time.perf_counter()
+        reps = 0
+        while time.perf_counter() - t0 < 8.0:
+            V.encode(xc)
+            reps += 1
+        dt = time.perf_counter() - t0
+        cpu = {"value": 2.0 * xc.size * reps / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": f"1 KV head x 4096 tokens (16 pages), base variant, {reps} passes, {dt:.1f} s (numpy)"}
+    g = timing["lynx"]["gbs"]
+    print(json.dumps({
+        "report": "ablation",
+        "metric": "quantizer variants: vNMSE on synthetic KV, and the variant encoder's GB/s vs HBM roofline (1 GB300)",
+        "value": g, "unit": "GB/s", "steps": args.steps,
+        "config": {"workload": f"quality: {w.name} (K and V); throughput: 2 layers x {wt.H} KV heads x "
+                               f"{wt.T} tokens (K), errors only", "vnmse": "sum (x_hat - x)^2 / sum x^2"},
+        "roofline": {"bound": "hbm", "achieved": g, "peak": hbm, "unit": "GB/s", "frac": g / hbm,
+                     "peak_kind": kind, "note": "algorithmic bytes: 2 B read per element, outputs negligible"},
+        "timing": timing, "variants": rows, "uniform_int4_over_lynx_4bit_vnmse": ratio,
+        "cpu_baseline": cpu}))
+
+
 def run_gpu(args):
     import torch
     import torch.distributed as dist
@@ -784,11 +879,12 @@ def main():
                                        "decode_attn_full"], default=None,
                     help="time one kernel group only (for profiler captures on smaller cases)")
     ap.add_argument("--layers", type=int, default=None, help="layers of the cache (default: all 94)")
-    ap.add_argument("--report", choices=["progressive", "append", "split-stream", "verify"], default=None,
+    ap.add_argument("--report", choices=["progressive", "append", "split-stream", "verify", "ablation"], default=None,
                     help="progressive: residual layers arriving one by one (8 layers, 64K tokens); "
                          "append: quantize-on-append of 32 requests' tail pages over 94 layers x 8 KV heads; "
                          "split-stream: anchors then residuals over an emulated link, decode on anchors first; "
-                         "verify: multi-token verify attention (64 draft positions, 32K context)")
+                         "verify: multi-token verify attention (64 draft positions, 32K context); "
+                         "ablation: quantizer variants and uniform comparators, vNMSE and encoder GB/s")
     ap.add_argument("--no-graph", action="store_true",
                     help="issue every library call from Python instead of replaying CUDA graphs of them")
     args = ap.parse_args()
@@ -808,6 +904,8 @@ def main():
         split_stream_report(args)
     elif args.report == "verify":
         verify_report(args)
+    elif args.report == "ablation":
+        ablation_report(args)
     else:
         run_gpu(args)
 

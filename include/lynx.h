@@ -243,6 +243,63 @@ lynx_status lynx_verify_attn(const void *q_bf16, const lynx_qkv *k, const lynx_q
 const char *lynx_status_string(lynx_status s);
 
 /*
+ * Variants and ablations of the quantizer, for quality studies. Section 7 of
+ * the Lynx reading ("What the paper does not establish") lists what was never
+ * measured: other splits (INT6 and INT2 splits are future work), the chunk
+ * size (only C = 32; smaller chunks are claimed to reduce error), and which
+ * stage of the bundle earns its gain over uniform INT4. A lynx_variant selects:
+ *   chunk          C: 16, 32 or 64 tokens per chunk
+ *   anchor_bits    a in 1..6, residual_bits r in 1..4, a + r <= 8: codes have
+ *                  2^(a+r-1) - 1 levels (4 + 4: the page's 127), the bias is
+ *                  2^(r-1) - 1 (+7 at r = 4), anchor-only decoding takes 2^r A
+ *   alpha          > 0: the alpha-law map; 0: its limit, the linear grid
+ *   flags          LYNX_VAR_* below, each switching one stage off:
+ *                  NO_PAGE_NORM (u = x), NO_CHUNK_ISOLATION (mean = scale = 1/2,
+ *                  i.e. w = 2u - 1), NO_BIAS (a plain floor cut), NO_SIGN_AWARE
+ *                  (c = -q for w < 0)
+ *   uniform_bits   > 0 (1..8): instead of the method, the uniform comparator: per
+ *                  (page, channel) min and range, code = floor((x - mn) *
+ *                  ((2^b - 1) / rng) + 1/2) in fp32, decoded mn + code rng / (2^b - 1);
+ *                  with flags = LYNX_VAR_UNIFORM_PER_TOKEN the grid is per token
+ *                  (min and range over its 128 channels; page_meta is then zeros)
+ * The default configuration {32, 4, 4, 255, 0, 0} encodes exactly as
+ * lynx_quantize_pages.
+ */
+#define LYNX_VAR_NO_PAGE_NORM 1u
+#define LYNX_VAR_NO_CHUNK_ISOLATION 2u
+#define LYNX_VAR_NO_BIAS 4u
+#define LYNX_VAR_NO_SIGN_AWARE 8u
+#define LYNX_VAR_UNIFORM_PER_TOKEN 16u
+typedef struct {
+    int32_t chunk;
+    int32_t anchor_bits;
+    int32_t residual_bits;
+    float alpha;
+    uint32_t flags;
+    int32_t uniform_bits;
+} lynx_variant;
+
+/*
+ * Encode n tensors of `tokens` x 128 bf16 values (tokens % 256 == 0) page by
+ * page with variant *v, in one pass. Every output is optional (NULL skips it);
+ * all are device memory, 16-byte aligned, caller-owned:
+ *   x_bf16      [n][tokens][128] bf16
+ *   codes       [n][tokens][128] int16: the signed code c (uniform: the grid code)
+ *   anchor      [n][tokens][128] int8: A = floor((c + bias) / 2^r) (method only)
+ *   residual    [n][tokens][128] uint8: c + bias - 2^r A (method only)
+ *   page_meta   [n][tokens/256][2][128] fp32 (min, range)
+ *   chunk_meta  [n][tokens/256][256/C][2][128] fp16 bits (mean, scale; method only)
+ *   err         [n][tokens/256][3] fp64 per page: sum x^2, sum (x_anchor - x)^2,
+ *               sum (x_full - x)^2 (uniform: the last two are equal); the
+ *               reconstructions are evaluated in fp32
+ * Returns LYNX_ERR_SHAPE / LYNX_ERR_UNSUPPORTED for sizes or knobs outside
+ * the ranges above, LYNX_ERR_ALIGN for misaligned pointers.
+ */
+lynx_status lynx_quantize_variant(const void *x_bf16, int32_t n, int32_t tokens, const lynx_variant *v,
+                                  int16_t *codes, int8_t *anchor, uint8_t *residual, float *page_meta,
+                                  uint16_t *chunk_meta, double *err, void *stream);
+
+/*
  * Diagnostics (no counterpart in the method: they expose the library's own
  * tables and its stage-3 code path so that tests can compare them with an
  * independent implementation).

@@ -44,6 +44,13 @@ class LynxQKV(ctypes.Structure):
                 ("page_meta", ctypes.c_void_p), ("chunk_meta", ctypes.c_void_p)]
 
 
+class LynxVariant(ctypes.Structure):
+    _fields_ = [("chunk", ctypes.c_int32), ("anchor_bits", ctypes.c_int32), ("residual_bits", ctypes.c_int32),
+                ("alpha", ctypes.c_float), ("flags", ctypes.c_uint32), ("uniform_bits", ctypes.c_int32)]
+
+
+VAR_NO_PAGE_NORM, VAR_NO_CHUNK_ISOLATION, VAR_NO_BIAS, VAR_NO_SIGN_AWARE, VAR_UNIFORM_PER_TOKEN = 1, 2, 4, 8, 16
+
 _lock = threading.Lock()
 _L = None
 
@@ -80,8 +87,10 @@ def _lib():
             L.lynx_host_tables.argtypes = [vp, vp]
             L.lynx_host_tables.restype = None
             L.lynx_level_codes.argtypes = [vp, i64, vp, vp]
+            L.lynx_quantize_variant.argtypes = [vp, i32, i32, ctypes.POINTER(LynxVariant), vp, vp, vp, vp, vp, vp,
+                                                vp]
             for f in ("lynx_quantize_pages", "lynx_quantize_append", "lynx_dequant_anchor", "lynx_refine_residual",
-                      "lynx_decode_attn", "lynx_verify_attn", "lynx_level_codes"):
+                      "lynx_decode_attn", "lynx_verify_attn", "lynx_level_codes", "lynx_quantize_variant"):
                 getattr(L, f).restype = ctypes.c_int
             _L = L
     return _L
@@ -312,3 +321,37 @@ def level_codes(w, stream=None):
     codes = torch.empty(w.shape, dtype=torch.int8, device=w.device)
     _check(_lib().lynx_level_codes(_ptr(w), w.numel(), _ptr(codes), _stream(stream)), "lynx_level_codes")
     return codes
+
+
+def quantize_variant(x, chunk=32, anchor_bits=4, residual_bits=4, alpha=255.0, flags=0, uniform_bits=0,
+                     codes=False, planes=False, meta=False, stream=None):
+    """lynx_quantize_variant: encode x (bfloat16 [..., tokens, 128], tokens a
+    multiple of 256) with one variant of the quantizer in a single pass.
+    Returns a dict with "err" (float64 [n, pages, 3]: sum x^2, anchor-only and
+    full squared errors per page) and, on request, "codes" (int16), "anchor"
+    (int8) / "residual" (uint8) and "page_meta" / "chunk_meta"."""
+    _dev(x, torch.bfloat16, "x")
+    if x.dim() < 2 or x.shape[-1] != HEAD_DIM:
+        raise ValueError("x must be [..., tokens, 128]")
+    T = x.shape[-2]
+    n = x.numel() // (T * HEAD_DIM)
+    P = T // 256
+    dev = x.device
+    v = LynxVariant(chunk, anchor_bits, residual_bits, alpha, flags, uniform_bits)
+    out = {"err": torch.empty((n, P, 3), dtype=torch.float64, device=dev)}
+    if codes:
+        out["codes"] = torch.empty((n, T, HEAD_DIM), dtype=torch.int16, device=dev)
+    if planes and not uniform_bits:
+        out["anchor"] = torch.empty((n, T, HEAD_DIM), dtype=torch.int8, device=dev)
+        out["residual"] = torch.empty((n, T, HEAD_DIM), dtype=torch.uint8, device=dev)
+    if meta:
+        out["page_meta"] = torch.empty((n, P, 2, HEAD_DIM), dtype=torch.float32, device=dev)
+        if not uniform_bits:
+            out["chunk_meta"] = torch.empty((n, P, 256 // chunk, 2, HEAD_DIM), dtype=torch.int16, device=dev)
+    _check(_lib().lynx_quantize_variant(_ptr(x), n, T, ctypes.byref(v), _ptr(out.get("codes")),
+                                        _ptr(out.get("anchor")), _ptr(out.get("residual")),
+                                        _ptr(out.get("page_meta")), _ptr(out.get("chunk_meta")), _ptr(out["err"]),
+                                        _stream(stream)),
+           "lynx_quantize_variant")
+    return out
+

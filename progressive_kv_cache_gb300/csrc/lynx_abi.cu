@@ -301,4 +301,40 @@ lynx_status lynx_level_codes(const float *w, int64_t n, int8_t *codes, void *str
     return from_cuda(launch_level_codes(w, n, codes, (cudaStream_t)stream));
 }
 
+lynx_status lynx_quantize_variant(const void *x_bf16, int32_t n, int32_t tokens, const lynx_variant *v,
+                                  int16_t *codes, int8_t *anchor, uint8_t *residual, float *page_meta,
+                                  uint16_t *chunk_meta, double *err, void *stream)
+{
+    if (!v)
+        return LYNX_ERR_NULL;
+    if (n < 0 || tokens < 0 || tokens % kPage)
+        return LYNX_ERR_SHAPE;
+    if (v->uniform_bits < 0 || v->uniform_bits > 8)
+        return LYNX_ERR_UNSUPPORTED;
+    if (v->uniform_bits > 0 && (v->flags & ~LYNX_VAR_UNIFORM_PER_TOKEN))
+        return LYNX_ERR_UNSUPPORTED;
+    if (v->uniform_bits == 0) {
+        if (v->chunk != 16 && v->chunk != 32 && v->chunk != 64)
+            return LYNX_ERR_UNSUPPORTED;
+        if (v->anchor_bits < 1 || v->anchor_bits > 6 || v->residual_bits < 1 || v->residual_bits > 4 ||
+            v->anchor_bits + v->residual_bits > 8 || v->anchor_bits + v->residual_bits < 3)
+            return LYNX_ERR_UNSUPPORTED;
+        if (!(v->alpha >= 0.0f) || !(v->alpha <= 3.0e38f))
+            return LYNX_ERR_UNSUPPORTED;
+        if (v->flags & ~(LYNX_VAR_NO_PAGE_NORM | LYNX_VAR_NO_CHUNK_ISOLATION | LYNX_VAR_NO_BIAS | LYNX_VAR_NO_SIGN_AWARE))
+            return LYNX_ERR_UNSUPPORTED;
+    }
+    const int64_t pages = (int64_t)n * (tokens / kPage);
+    if (pages == 0)
+        return LYNX_OK;
+    if (!x_bf16)
+        return LYNX_ERR_NULL;
+    const void *ptrs[] = {x_bf16, codes, anchor, residual, page_meta, chunk_meta, err};
+    for (const void *p : ptrs)
+        if (p && !aligned(p, 16))
+            return LYNX_ERR_ALIGN;
+    return from_cuda(launch_quantize_variant(static_cast<const uint16_t *>(x_bf16), pages, *v, codes, anchor,
+                                             residual, page_meta, chunk_meta, err, (cudaStream_t)stream));
+}
+
 } // extern "C"

@@ -69,6 +69,9 @@ cudaError_t launch_quantize_append(const uint16_t *tail, const int32_t *dst_page
                                    const lynx_qkv &o, uint32_t *dev_err, cudaStream_t s);
 cudaError_t launch_level_codes(const float *w, int64_t n, int8_t *codes, cudaStream_t s);
 cudaError_t launch_dequant(const lynx_qkv &in, void *out, bool full, bool f32, cudaStream_t s);
+cudaError_t launch_quantize_variant(const uint16_t *x, int64_t pages, const lynx_variant &v, int16_t *codes,
+                                    int8_t *anchor, uint8_t *resid, float *page_meta, uint16_t *chunk_meta,
+                                    double *err, cudaStream_t s);
 
 struct AttnArgs {
     const uint16_t *q;

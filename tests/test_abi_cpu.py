@@ -174,3 +174,31 @@ def test_verify_attn_rejects_bad_arguments(lx):
     assert lib.lynx_verify_attn_workspace(1, 0, 64, 8) == 0
     assert lib.lynx_verify_attn_workspace(1, 65, 64, 8) == 0
     assert lib.lynx_verify_attn_workspace(2, 64, 64, 512) % 16 == 0
+
+
+def test_quantize_variant_rejects_bad_arguments(lx):
+    lib = lx.library()
+
+    def call(n=1, T=256, x=0x400000, err=0x500000, codes=None, **kw):
+        v = lx.LynxVariant(kw.get("chunk", 32), kw.get("a", 4), kw.get("r", 4), kw.get("alpha", 255.0),
+                           kw.get("flags", 0), kw.get("ub", 0))
+        return lib.lynx_quantize_variant(ctypes.c_void_p(x) if x else None, n, T, ctypes.byref(v),
+                                         ctypes.c_void_p(codes) if codes else None, None, None, None, None,
+                                         ctypes.c_void_p(err) if err else None, None)
+
+    assert lib.lynx_quantize_variant(None, 1, 256, None, None, None, None, None, None, None, None) == lx.ERR_NULL
+    assert call(x=0) == lx.ERR_NULL
+    assert call(T=300) == lx.ERR_SHAPE
+    assert call(n=-1) == lx.ERR_SHAPE
+    assert call(chunk=8) == lx.ERR_UNSUPPORTED
+    assert call(a=7) == lx.ERR_UNSUPPORTED
+    assert call(r=5) == lx.ERR_UNSUPPORTED
+    assert call(a=6, r=4) == lx.ERR_UNSUPPORTED              # more than 8 bits
+    assert call(alpha=-1.0) == lx.ERR_UNSUPPORTED
+    assert call(alpha=float("nan")) == lx.ERR_UNSUPPORTED
+    assert call(flags=16) == lx.ERR_UNSUPPORTED
+    assert call(ub=9) == lx.ERR_UNSUPPORTED
+    assert call(x=0x400008) == lx.ERR_ALIGN
+    assert call(codes=0x600002) == lx.ERR_ALIGN
+    assert call(n=0) == lx.OK                                 # nothing to do, no launch
+    assert call(T=0) == lx.OK
