@@ -47,7 +47,8 @@ constexpr int kThreads = (kProdWarp + 1) * 32;
 constexpr int kRing = 6;                      // chunk slots of codes in flight
 constexpr int kBufs = 3;                      // K / V operand tiles and S buffers
 constexpr int kPBufs = 2;                     // P buffers
-constexpr uint32_t kWaitLimit = 1u << 22;
+constexpr uint32_t kWaitLimit = 1u << 18;   // waits of up to kSleepNs each: about 1 s in all
+constexpr uint32_t kSleepNs = 4096;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kLevCopies = 32;                // one level-table copy per lane: conflict-free lookups
 // tensor memory columns (fp32 / f16x2 words; lane = query row)
@@ -179,6 +180,24 @@ __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Bounded wait that sleeps in hardware: each try_wait suspends the thread
+// until the phase completes or the hinted time (ns) passes, so waiting
+// threads take no issue slots from the ones doing work.
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t limit)
+{
+    for (uint32_t i = 0; i < limit; ++i) {
+        uint32_t ok;
+        asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+                     "selp.u32 %0, 1, 0, p;\n\t}"
+                     : "=r"(ok)
+                     : "r"(smem_u32(bar)), "r"(parity), "r"(kSleepNs)
+                     : "memory");
+        if (ok)
+            return true;
+    }
+    return false;
+}
 
 // Non-blocking test of an mbarrier phase.
 __device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity)
@@ -440,7 +459,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(VerifyArgs a, Level
             for (int c = 0; c < nch; ++c) {
                 const int s = c % kRing, i = c >> 3, j = c & 7;
                 // slot s was last decoded for chunk c - kRing
-                if (c >= kRing && !mbar_wait_bounded(&sm.slot_free[s], (uint32_t)(((c - kRing) / kRing) & 1), kWaitLimit)) {
+                if (c >= kRing && !mbar_wait_sleep(&sm.slot_free[s], (uint32_t)(((c - kRing) / kRing) & 1), kWaitLimit)) {
                     timed_out = true;
                     break;
                 }
@@ -475,7 +494,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(VerifyArgs a, Level
             }
             // let every copy issued land before the CTA exits (bounded)
             for (int c = max(nch - kRing, 0); c < nch; ++c)
-                mbar_wait_bounded(&sm.ring_full[c % kRing], (uint32_t)((c / kRing) & 1), kWaitLimit);
+                mbar_wait_sleep(&sm.ring_full[c % kRing], (uint32_t)((c / kRing) & 1), kWaitLimit);
         }
     } else if (warp >= kSoftWarps && warp < kMmaWarp) {
         // ---- decode warps ----------------------------------------------------
@@ -485,9 +504,9 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(VerifyArgs a, Level
             const int s = c % kRing, buf = c % kBufs;
             const uint32_t prev = (uint32_t)(((c - kBufs) / kBufs) & 1);
             // codes in; K tile `buf` last read by the Q.K^T of chunk c - kBufs
-            bool ok = mbar_wait_bounded(&sm.ring_full[s], (uint32_t)((c / kRing) & 1), kWaitLimit);
+            bool ok = mbar_wait_sleep(&sm.ring_full[s], (uint32_t)((c / kRing) & 1), kWaitLimit);
             if (ok && c >= kBufs)
-                ok = mbar_wait_bounded(&sm.s_full[buf], prev, kWaitLimit);
+                ok = mbar_wait_sleep(&sm.s_full[buf], prev, kWaitLimit);
             if (!__all_sync(0xFFFFFFFFu, ok)) {
                 timed_out = true;
                 break;
@@ -500,7 +519,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(VerifyArgs a, Level
             if (lane == 0)
                 mbar_arrive(&sm.k_full[buf]);
             // V tile `buf` last read by the P.V of chunk c - kBufs
-            if (c >= kBufs && !__all_sync(0xFFFFFFFFu, mbar_wait_bounded(&sm.pv_done[buf], prev, kWaitLimit))) {
+            if (c >= kBufs && !__all_sync(0xFFFFFFFFu, mbar_wait_sleep(&sm.pv_done[buf], prev, kWaitLimit))) {
                 timed_out = true;
                 break;
             }
@@ -528,9 +547,9 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(VerifyArgs a, Level
             const uint32_t k0 = smem_u32(sm.k), v0 = smem_u32(sm.v);
             auto issue_qk = [&](int c) -> bool {
                 const int buf = c % kBufs;
-                if (!mbar_wait_bounded(&sm.k_full[buf], (uint32_t)((c / kBufs) & 1), kWaitLimit))
+                if (!mbar_wait_sleep(&sm.k_full[buf], (uint32_t)((c / kBufs) & 1), kWaitLimit))
                     return false;
-                if (c >= kBufs && !mbar_wait_bounded(&sm.s_free[buf], (uint32_t)(((c - kBufs) / kBufs) & 1), kWaitLimit))
+                if (c >= kBufs && !mbar_wait_sleep(&sm.s_free[buf], (uint32_t)(((c - kBufs) / kBufs) & 1), kWaitLimit))
                     return false;
                 tc_fence_after();
                 const uint32_t tS = tmem + kColS + 64u * buf;
@@ -549,8 +568,8 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(VerifyArgs a, Level
                 if (c + 1 < nch && !(ok = issue_qk(c + 1)))
                     break;
                 const int buf = c % kBufs, pb = c % kPBufs;
-                ok = mbar_wait_bounded(&sm.p_full[pb], (uint32_t)((c / kPBufs) & 1), kWaitLimit) &&
-                     mbar_wait_bounded(&sm.v_full[buf], (uint32_t)((c / kBufs) & 1), kWaitLimit);
+                ok = mbar_wait_sleep(&sm.p_full[pb], (uint32_t)((c / kPBufs) & 1), kWaitLimit) &&
+                     mbar_wait_sleep(&sm.v_full[buf], (uint32_t)((c / kBufs) & 1), kWaitLimit);
                 if (!ok)
                     break;
                 tc_fence_after();
@@ -570,7 +589,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(VerifyArgs a, Level
             // every MMA issued must finish before the tensor memory is freed
             // (the commit tracks all of this thread's earlier MMAs; bounded)
             umma_commit(&sm.drained);
-            mbar_wait_bounded(&sm.drained, 0u, kWaitLimit);
+            mbar_wait_sleep(&sm.drained, 0u, kWaitLimit);
         }
     } else {
         // ---- softmax warps: one query row per thread -------------------------
@@ -582,7 +601,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(VerifyArgs a, Level
         float m_run = neg_inf(), l_run = 0.0f;
         for (int c = 0; c < nch; ++c) {
             const int buf = c % kBufs, pb = c % kPBufs;
-            if (!mbar_wait_bounded(&sm.s_full[buf], (uint32_t)((c / kBufs) & 1), kWaitLimit)) {
+            if (!mbar_wait_sleep(&sm.s_full[buf], (uint32_t)((c / kBufs) & 1), kWaitLimit)) {
                 timed_out = true;
                 break;
             }
@@ -620,7 +639,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(VerifyArgs a, Level
             const bool up = mx > m_run + 8.0f;
             if (__any_sync(0xFFFFFFFFu, up)) {
                 // rare: rescale this row's output, complete up to chunk c - 1
-                if (c >= 1 && !mbar_wait_bounded(&sm.pv_done[(c - 1) % kBufs], (uint32_t)(((c - 1) / kBufs) & 1),
+                if (c >= 1 && !mbar_wait_sleep(&sm.pv_done[(c - 1) % kBufs], (uint32_t)(((c - 1) / kBufs) & 1),
                                                   kWaitLimit)) {
                     timed_out = true;
                     break;
@@ -644,7 +663,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(VerifyArgs a, Level
                 tmem_wait_st();
             }
             // P buffer `pb` was last read by the P.V of chunk c - kPBufs
-            if (c >= kPBufs && !mbar_wait_bounded(&sm.pv_done[(c - kPBufs) % kBufs],
+            if (c >= kPBufs && !mbar_wait_sleep(&sm.pv_done[(c - kPBufs) % kBufs],
                                                   (uint32_t)(((c - kPBufs) / kBufs) & 1), kWaitLimit)) {
                 timed_out = true;
                 break;
@@ -670,7 +689,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(VerifyArgs a, Level
         }
         // ---- this range's partial of the row
         if (!timed_out && nch > 0 &&
-            !mbar_wait_bounded(&sm.pv_done[(nch - 1) % kBufs], (uint32_t)(((nch - 1) / kBufs) & 1), kWaitLimit))
+            !mbar_wait_sleep(&sm.pv_done[(nch - 1) % kBufs], (uint32_t)(((nch - 1) / kBufs) & 1), kWaitLimit))
             timed_out = true;
         tc_fence_after();
         float *part = a.part + ((((int64_t)b * Tq + pos) * a.Hq + h) * a.n_splits + split) * kPart;
