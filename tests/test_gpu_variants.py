@@ -103,3 +103,40 @@ def test_report_size_sampled_pages(lx, case):
     sub = torch.cat([xs[:, 256 * p:256 * p + 256] for p in pages], dim=1).contiguous()
     o = V.encode(sub.view(torch.int16).cpu().numpy().view(np.uint16), _variant(case))
     _compare(o, g, case, pages=pages)
+
+
+@pytest.mark.parametrize("case", [dict(), dict(chunk=16, flags=1), dict(flags=2), dict(uniform_bits=4),
+                                  dict(uniform_bits=8, flags=16)],
+                         ids=["default", "C16-nopagenorm", "noiso", "int4", "int8-token"])
+def test_edge_pages(lx, case):
+    """Degenerate pages: a constant channel (range 0), a channel with a NaN, an
+    all-zero page, a channel whose chunk holds one outlier, +/-0 mixtures, and
+    large magnitudes. Codes and metadata bit for bit; error sums where finite."""
+    from oracle import variants as V
+    rng = np.random.default_rng(11)
+    x = rng.laplace(size=(2, 768, 128)).astype(np.float32)
+    x[0, :256, 3] = 1.5                              # constant channel
+    x[0, 17, 5] = np.nan                             # NaN channel (page 0)
+    x[1, 256:512, :] = 0.0                           # all-zero page
+    x[1, 300, 9] = -0.0
+    x[0, 600, 7] = 3.0e4                             # one outlier in a chunk
+    x[1, 512:, 11] *= 1.0e3                          # large magnitudes
+    xb = (x.view(np.uint32) >> 16).astype(np.uint16)  # truncation to bf16 is fine for a test input
+    g = lx.quantize_variant(bf16_dev(xb), codes=True, planes=True, meta=True, **case)
+    o = V.encode(xb, _variant(case))
+    assert np.array_equal(g["codes"].cpu().numpy().astype(np.int32), o["codes"])
+    pm_g, pm_o = g["page_meta"].cpu().numpy(), o["page_meta"].astype(np.float32)
+    assert np.array_equal(np.isnan(pm_g), np.isnan(pm_o))
+    assert np.array_equal(np.nan_to_num(pm_g).view(np.uint32), np.nan_to_num(pm_o).view(np.uint32))
+    if not case.get("uniform_bits"):
+        assert np.array_equal(g["anchor"].cpu().numpy().astype(np.int32), o["anchor"])
+        assert np.array_equal(g["residual"].cpu().numpy().astype(np.int32), o["residual"])
+        cg = g["chunk_meta"].cpu().numpy().view(np.uint16)
+        hg, ho = cg.view(np.float16), o["chunk_meta"].view(np.float16)
+        nan = np.isnan(hg)                            # NaN payloads may differ: any NaN matches any NaN
+        assert np.array_equal(nan, np.isnan(ho)) and np.array_equal(cg[~nan], o["chunk_meta"][~nan])
+    ge, oe = g["err"].cpu().numpy(), o["err"]
+    fin = np.isfinite(oe).all(axis=-1)
+    assert np.array_equal(np.isfinite(ge).all(axis=-1), fin)
+    assert np.allclose(ge[fin][:, 0], oe[fin][:, 0], rtol=1e-4)
+    assert np.allclose(ge[fin][:, 1:], oe[fin][:, 1:], rtol=2e-3, atol=1e-9)
