@@ -13,11 +13,12 @@
 // With T_q x G query rows per KV head, Q.K^T and P.V are dense contractions.
 // A CTA owns 128 query rows (the MMA's M) and a range of pages; per 32-token
 // chunk:
-//  - decode warps expand the chunk's K and V codes (x = a + b L in fp32, split
+//  - 16 decode warps expand the chunk's K and V codes (x = a + b L in fp32, split
 //    into fp16 hi + lo) into shared-memory operand tiles in the tensor cores'
 //    K-major swizzled layouts (K: rows of 128 channels, 128-byte swizzle; V
 //    transposed: rows of 32 tokens, 64-byte swizzle);
-//  - one thread issues tcgen05.mma: S = Q.K^T into tensor memory with Q hi/lo
+//  - one thread issues the Q.K^T MMAs and another the P.V MMAs (tcgen05.mma):
+//    S = Q.K^T into tensor memory with Q hi/lo
 //    resident in tensor memory as the A operand (three products hi.hi + hi.lo
 //    + lo.hi keep fp32-level accuracy), and after the softmax O += P.V with P
 //    hi/lo in tensor memory as the A operand; only K and V^T are read from
@@ -26,7 +27,9 @@
 //    scores from tensor memory, apply the causal mask and the online softmax
 //    (the reference moves only when a score passes it by 2^8; then O is
 //    rescaled in tensor memory), and write P hi/lo back to tensor memory.
-// Chunk codes arrive by bulk copy into a ring of slots; every wait is bounded.
+// Chunk codes arrive by bulk copy into a ring of slots, where the producer
+// warp also turns each chunk's metadata into its affines once; every wait is
+// bounded and sleeps in hardware.
 // Split-K partials are merged by the decode path's combine kernel.
 #include <cstddef>
 #include <cuda_fp16.h>
@@ -40,10 +43,11 @@ namespace {
 constexpr int kRow = kD / 2;                  // code bytes per token
 constexpr int kPart = kD + 2;
 constexpr int kRows = 128;                    // query rows per CTA (MMA M)
-constexpr int kSoftWarps = 4, kDecWarps = 8;
-constexpr int kMmaWarp = kSoftWarps + kDecWarps;      // issues the MMAs, owns the tensor memory
-constexpr int kProdWarp = kMmaWarp + 1;                // issues the bulk copies of chunk codes
-constexpr int kThreads = (kProdWarp + 1) * 32;
+constexpr int kSoftWarps = 4, kDecWarps = 16;
+constexpr int kMmaWarp = kSoftWarps + kDecWarps;      // issues the Q.K^T MMAs, owns the tensor memory
+constexpr int kProdWarp = kMmaWarp + 1;                // issues the bulk copies, computes the chunk affines
+constexpr int kPvWarp = kProdWarp + 1;                 // issues the P.V MMAs (kMmaWarp issues Q.K^T)
+constexpr int kThreads = (kPvWarp + 1) * 32;
 constexpr int kRing = 6;                      // chunk slots of codes in flight
 constexpr int kBufs = 3;                      // K / V operand tiles and S buffers
 constexpr int kPBufs = 2;                     // P buffers
@@ -67,6 +71,9 @@ struct Slot {
     uint8_t kr[FULL ? kChunk * kRow : 16], vr[FULL ? kChunk * kRow : 16];
     float kpm[2 * kD], vpm[2 * kD];           // page min, range
     uint16_t kcm[2 * kD], vcm[2 * kD];        // chunk mean, scale
+    // chunk affines a = mn + rng mu and b = rng s, computed once per chunk:
+    // K as [part][group][4] (channel 8 group + 4 part + i), V in channel order
+    float kaf[2][16][4], kbf[2][16][4], vaf[kD], vbf[kD];
 };
 
 // Operand tiles. 128-byte swizzle: 16-byte piece c of a 128-byte row r sits at
@@ -83,7 +90,8 @@ struct Smem {
     uint32_t tmem;
     alignas(8) uint64_t ring_full[kRing], slot_free[kRing];
     uint64_t k_full[kBufs], v_full[kBufs], s_full[kBufs], s_free[kBufs], pv_done[kBufs], p_full[kPBufs];
-    uint64_t drained;
+    uint64_t drained, drained_pv;
+    uint64_t aff_ready[kRing];                // the slot's chunk affines are written
 };
 
 __device__ __forceinline__ uint32_t sw128(int row, int byte)
@@ -166,6 +174,35 @@ __device__ __forceinline__ void tmem_st32u(uint32_t t, const uint32_t (&w)[32])
     tmem_st32(t, v);
 }
 
+// 16 consecutive tensor-memory columns of this lane's row, from floats.
+__device__ __forceinline__ void tmem_st16f(uint32_t t, const float (&v)[16])
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+                 "%16};" ::"r"(t),
+                 "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]), "f"(v[8]),
+                 "f"(v[9]), "f"(v[10]), "f"(v[11]), "f"(v[12]), "f"(v[13]), "f"(v[14]), "f"(v[15])
+                 : "memory");
+}
+
+// 8 consecutive tensor-memory columns of this lane's row, from words.
+__device__ __forceinline__ void tmem_st8(uint32_t t, const uint32_t (&v)[8])
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(t), "r"(v[0]),
+                 "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+                 : "memory");
+}
+
+// 16 consecutive tensor-memory columns of this lane's row, as floats.
+__device__ __forceinline__ void tmem_ld16(uint32_t t, float (&v)[16])
+{
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, "
+                 "[%16];"
+                 : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]), "=f"(v[4]), "=f"(v[5]), "=f"(v[6]), "=f"(v[7]),
+                   "=f"(v[8]), "=f"(v[9]), "=f"(v[10]), "=f"(v[11]), "=f"(v[12]), "=f"(v[13]), "=f"(v[14]), "=f"(v[15])
+                 : "r"(t)
+                 : "memory");
+}
+
 // 16 consecutive tensor-memory columns of this lane's row.
 __device__ __forceinline__ void tmem_st16(uint32_t t, const uint32_t (&v)[16])
 {
@@ -235,36 +272,20 @@ __device__ __forceinline__ void split2(float2 x, uint32_t &hi, uint32_t &lo)
     lo = *reinterpret_cast<const uint32_t *>(&l);
 }
 
-// Chunk affines a = mn + rng mu and b = rng s of channel pair pr.
-__device__ __forceinline__ void pair_affine(const float *pm, const uint16_t *cm, int pr, float2 &a, float2 &b)
+// Chunk affines a = mn + rng mu and b = rng s of the four channels d .. d + 3
+// (two packed pairs; each lane of the packed operations is one IEEE operation).
+__device__ __forceinline__ void affine4(const float *pm, const uint16_t *cm, int d, float4 &a, float4 &b)
 {
-    const int d = 2 * pr;
-    const float2 mn = *reinterpret_cast<const float2 *>(pm + d);
-    const float2 rg = *reinterpret_cast<const float2 *>(pm + kD + d);
-    const float2 mu = __half22float2(*reinterpret_cast<const __half2 *>(cm + d));
-    const float2 sc = __half22float2(*reinterpret_cast<const __half2 *>(cm + kD + d));
-    a = __ffma2_rn(rg, mu, mn);
-    b = __fmul2_rn(rg, sc);
-}
-
-// The same for the four channel pairs 4 g .. 4 g + 3 (channels 8 g .. 8 g + 7).
-__device__ __forceinline__ void quad_affine(const float *pm, const uint16_t *cm, int g, float2 (&a)[4], float2 (&b)[4])
-{
-    const int d = 8 * g;
-    const float4 mn0 = *reinterpret_cast<const float4 *>(pm + d), mn1 = *reinterpret_cast<const float4 *>(pm + d + 4);
-    const float4 rg0 = *reinterpret_cast<const float4 *>(pm + kD + d);
-    const float4 rg1 = *reinterpret_cast<const float4 *>(pm + kD + d + 4);
-    const uint4 mu = *reinterpret_cast<const uint4 *>(cm + d), sc = *reinterpret_cast<const uint4 *>(cm + kD + d);
-    const float2 mn[4] = {make_float2(mn0.x, mn0.y), make_float2(mn0.z, mn0.w), make_float2(mn1.x, mn1.y),
-                          make_float2(mn1.z, mn1.w)};
-    const float2 rg[4] = {make_float2(rg0.x, rg0.y), make_float2(rg0.z, rg0.w), make_float2(rg1.x, rg1.y),
-                          make_float2(rg1.z, rg1.w)};
-    const uint32_t muw[4] = {mu.x, mu.y, mu.z, mu.w}, scw[4] = {sc.x, sc.y, sc.z, sc.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        a[i] = __ffma2_rn(rg[i], __half22float2(*reinterpret_cast<const __half2 *>(&muw[i])), mn[i]);
-        b[i] = __fmul2_rn(rg[i], __half22float2(*reinterpret_cast<const __half2 *>(&scw[i])));
-    }
+    const float4 mn = *reinterpret_cast<const float4 *>(pm + d), rg = *reinterpret_cast<const float4 *>(pm + kD + d);
+    const uint2 mu = *reinterpret_cast<const uint2 *>(cm + d), sc = *reinterpret_cast<const uint2 *>(cm + kD + d);
+    const float2 a01 = __ffma2_rn(make_float2(rg.x, rg.y), __half22float2(*reinterpret_cast<const __half2 *>(&mu.x)),
+                                  make_float2(mn.x, mn.y));
+    const float2 a23 = __ffma2_rn(make_float2(rg.z, rg.w), __half22float2(*reinterpret_cast<const __half2 *>(&mu.y)),
+                                  make_float2(mn.z, mn.w));
+    const float2 b01 = __fmul2_rn(make_float2(rg.x, rg.y), __half22float2(*reinterpret_cast<const __half2 *>(&sc.x)));
+    const float2 b23 = __fmul2_rn(make_float2(rg.z, rg.w), __half22float2(*reinterpret_cast<const __half2 *>(&sc.y)));
+    a = make_float4(a01.x, a01.y, a23.x, a23.y);
+    b = make_float4(b01.x, b01.y, b23.x, b23.y);
 }
 
 // Levels of the two channels of a code byte (anchor byte a8, residual byte
@@ -283,74 +304,73 @@ __device__ __forceinline__ float2 levels(const float *lv, uint32_t a8, uint32_t 
     return make_float2(lv[kLevCopies * (a8 >> sh)], lv[kLevCopies * (a8 >> sh2)]);
 }
 
-// K of one chunk into tiles kt[k-atom][hi/lo] (rows = tokens, 128-byte rows of
-// 64 channels). Decode thread u (0..255) takes the 16-byte piece of channels
-// 8 g .. 8 g + 7, g = u % 16, of tokens u / 16 and u / 16 + 16: one 32-bit
-// code load per plane and one 16-byte store per tile.
+// K of one chunk into the tiles kt[k-atom][hi/lo] (rows = tokens, 128-byte
+// rows of 64 channels). Decode thread u (0..511) takes the 16-byte piece of
+// channels 8 g .. 8 g + 7, g = u % 16, of token u / 16: one 32-bit code load
+// per plane and one 16-byte store per tile (the 8 lanes of a store phase
+// write one whole row).
 template <bool FULL>
-__device__ __forceinline__ void decode_k(const Slot<FULL> &sl, bool valid, const float *lv, uint8_t (&kt)[2][2][kChunk * 128],
-                                         int u)
+__device__ __forceinline__ void decode_k(const Slot<FULL> &sl, bool valid, const float *lv,
+                                         uint8_t (&kt)[2][2][kChunk * 128], int u)
 {
-    const int g = u & 15, ka = g >> 3, piece = g & 7;
-    float2 aa[4], bb[4];
-    quad_affine(sl.kpm, sl.kcm, g, aa, bb);
+    const int g = u & 15, t = u >> 4, ka = g >> 3, piece = g & 7;
+    const float4 a0 = *reinterpret_cast<const float4 *>(sl.kaf[0][g]), a1 = *reinterpret_cast<const float4 *>(sl.kaf[1][g]);
+    const float4 b0 = *reinterpret_cast<const float4 *>(sl.kbf[0][g]), b1 = *reinterpret_cast<const float4 *>(sl.kbf[1][g]);
+    const float2 aa[4] = {make_float2(a0.x, a0.y), make_float2(a0.z, a0.w), make_float2(a1.x, a1.y), make_float2(a1.z, a1.w)};
+    const float2 bb[4] = {make_float2(b0.x, b0.y), make_float2(b0.z, b0.w), make_float2(b1.x, b1.y), make_float2(b1.z, b1.w)};
+    uint32_t hi[4] = {0, 0, 0, 0}, lo[4] = {0, 0, 0, 0};
+    if (valid) {
+        const uint32_t a4 = *reinterpret_cast<const uint32_t *>(sl.ka + t * kRow + 4 * g);
+        const uint32_t r4 = FULL ? *reinterpret_cast<const uint32_t *>(sl.kr + t * kRow + 4 * g) : 0u;
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        const int t = (u >> 4) + 16 * h;
-        uint32_t hi[4] = {0, 0, 0, 0}, lo[4] = {0, 0, 0, 0};
-        if (valid) {
-            const uint32_t a4 = *reinterpret_cast<const uint32_t *>(sl.ka + t * kRow + 4 * g);
-            const uint32_t r4 = FULL ? *reinterpret_cast<const uint32_t *>(sl.kr + t * kRow + 4 * g) : 0u;
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-                split2(__ffma2_rn(bb[i], levels<FULL>(lv, (a4 >> (8 * i)) & 0xFFu, (r4 >> (8 * i)) & 0xFFu), aa[i]),
-                       hi[i], lo[i]);
-        }
-        const uint32_t off = sw128(t, 16 * piece);
-        *reinterpret_cast<uint4 *>(&kt[ka][0][off]) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        *reinterpret_cast<uint4 *>(&kt[ka][1][off]) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        for (int i = 0; i < 4; ++i)
+            split2(__ffma2_rn(bb[i], levels<FULL>(lv, (a4 >> (8 * i)) & 0xFFu, (r4 >> (8 * i)) & 0xFFu), aa[i]), hi[i],
+                   lo[i]);
     }
+    const uint32_t off = sw128(t, 16 * piece);
+    *reinterpret_cast<uint4 *>(&kt[ka][0][off]) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+    *reinterpret_cast<uint4 *>(&kt[ka][1][off]) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
 }
 
-// V of one chunk, transposed, into tiles vt[hi/lo] (rows = channels, 64-byte
-// rows of 32 tokens). Decode thread u takes channel pair pr = u % 64 of the
-// eight tokens 8 o .. 8 o + 7, o = u / 64: one 16-byte store per row and
-// tile. Lanes with bit 2 of pr set store row 2 pr + 1 first, so that the 8
-// lanes of a store phase cover all 32 banks.
+// V of one chunk, transposed, into the tiles vt[hi/lo] (rows = channels,
+// 64-byte rows of 32 tokens). Decode thread u takes channel pair pr = u % 64
+// of the four tokens 4 o .. 4 o + 3, where o is the warp's quad u / 64,
+// exchanged with its neighbour (o ^ 1) by lanes with bit 3 of pr set; lanes
+// with bit 2 of pr set store row 2 pr + 1 first. Together the 16 lanes of an
+// 8-byte store phase cover all 32 banks.
 template <bool FULL>
 __device__ __forceinline__ void decode_v(const Slot<FULL> &sl, bool valid, const float *lv, uint8_t (&vt)[2][kD * 64],
                                          int u)
 {
-    const int pr = u & 63, o = u >> 6, sw = (pr >> 2) & 1;
+    const int pr = u & 63, sw = (pr >> 2) & 1, o = (u >> 6) ^ ((pr >> 3) & 1);
     const uint32_t sh = 4u * (uint32_t)sw;
-    float2 aa, bb;
-    pair_affine(sl.vpm, sl.vcm, pr, aa, bb);
+    float2 aa = *reinterpret_cast<const float2 *>(sl.vaf + 2 * pr), bb = *reinterpret_cast<const float2 *>(sl.vbf + 2 * pr);
     if (sw) {
         aa = make_float2(aa.y, aa.x);
         bb = make_float2(bb.y, bb.x);
     }
-    uint32_t h0[4], h1[4], l0[4], l1[4];     // rows 2 pr + sw and 2 pr + 1 - sw; word j = tokens 8 o + 2 j, + 1
+    float2 x[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        float2 x[2];
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            const int t = 8 * o + 2 * j + e;
-            x[e] = make_float2(0.0f, 0.0f);
-            if (valid) {
-                const uint32_t a8 = sl.va[t * kRow + pr];
-                const uint32_t r8 = FULL ? sl.vr[t * kRow + pr] : 0u;
-                x[e] = __ffma2_rn(bb, levels<FULL>(lv, a8, r8, sh), aa);
-            }
+    for (int e = 0; e < 4; ++e) {
+        const int t = 4 * o + e;
+        x[e] = make_float2(0.0f, 0.0f);
+        if (valid) {
+            const uint32_t a8 = sl.va[t * kRow + pr];
+            const uint32_t r8 = FULL ? sl.vr[t * kRow + pr] : 0u;
+            x[e] = __ffma2_rn(bb, levels<FULL>(lv, a8, r8, sh), aa);
         }
-        split2(make_float2(x[0].x, x[1].x), h0[j], l0[j]);
-        split2(make_float2(x[0].y, x[1].y), h1[j], l1[j]);
     }
-    const uint32_t o0 = sw64(2 * pr + sw, 16 * o), o1 = sw64(2 * pr + 1 - sw, 16 * o);
-    *reinterpret_cast<uint4 *>(&vt[0][o0]) = make_uint4(h0[0], h0[1], h0[2], h0[3]);
-    *reinterpret_cast<uint4 *>(&vt[0][o1]) = make_uint4(h1[0], h1[1], h1[2], h1[3]);
-    *reinterpret_cast<uint4 *>(&vt[1][o0]) = make_uint4(l0[0], l0[1], l0[2], l0[3]);
-    *reinterpret_cast<uint4 *>(&vt[1][o1]) = make_uint4(l1[0], l1[1], l1[2], l1[3]);
+    uint32_t h0[2], h1[2], l0[2], l1[2];     // rows 2 pr + sw and 2 pr + 1 - sw; word j = tokens 4 o + 2 j, + 1
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        split2(make_float2(x[2 * j].x, x[2 * j + 1].x), h0[j], l0[j]);
+        split2(make_float2(x[2 * j].y, x[2 * j + 1].y), h1[j], l1[j]);
+    }
+    const uint32_t o0 = sw64(2 * pr + sw, 8 * o), o1 = sw64(2 * pr + 1 - sw, 8 * o);
+    *reinterpret_cast<uint2 *>(&vt[0][o0]) = make_uint2(h0[0], h0[1]);
+    *reinterpret_cast<uint2 *>(&vt[0][o1]) = make_uint2(h1[0], h1[1]);
+    *reinterpret_cast<uint2 *>(&vt[1][o0]) = make_uint2(l0[0], l0[1]);
+    *reinterpret_cast<uint2 *>(&vt[1][o1]) = make_uint2(l1[0], l1[1]);
 }
 
 template <bool FULL>
@@ -388,6 +408,9 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(VerifyArgs a, Level
         for (int s = 0; s < kPBufs; ++s)
             mbar_init(&sm.p_full[s], kSoftWarps);
         mbar_init(&sm.drained, 1);
+        mbar_init(&sm.drained_pv, 1);
+        for (int s = 0; s < kRing; ++s)
+            mbar_init(&sm.aff_ready[s], 1);
         fence_mbar_init();
     }
     if (warp == kMmaWarp) {                  // the MMA warp owns the tensor memory
@@ -414,27 +437,27 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(VerifyArgs a, Level
     if (warp < kSoftWarps) {                 // Q (scaled to log2 units) hi / lo and O = 0 into tensor memory
         const float qscale = a.sm_scale * kLog2e;
         const uint16_t *qrow = a.q + (((int64_t)b * Tq + pos) * a.Hq + h) * kD;
+#pragma unroll 1
+        for (int grp = 0; grp < 8; ++grp) {  // 16 channels (8 words) at a time
+            uint32_t hi[8], lo[8];
 #pragma unroll
-        for (int grp = 0; grp < 2; ++grp) {
-            uint32_t hi[32], lo[32];
-#pragma unroll
-            for (int w8 = 0; w8 < 8; ++w8) {
-                const uint4 w = rowok ? *reinterpret_cast<const uint4 *>(qrow + 64 * grp + 8 * w8) : make_uint4(0, 0, 0, 0);
+            for (int w8 = 0; w8 < 2; ++w8) {
+                const uint4 w = rowok ? *reinterpret_cast<const uint4 *>(qrow + 16 * grp + 8 * w8) : make_uint4(0, 0, 0, 0);
                 const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
                     split2(make_float2(bf16_lo(ws[i]) * qscale, bf16_hi(ws[i]) * qscale), hi[4 * w8 + i], lo[4 * w8 + i]);
             }
-            tmem_st32u(trow + kColQ + 32 * grp, hi);
-            tmem_st32u(trow + kColQ + 64 + 32 * grp, lo);
+            tmem_st8(trow + kColQ + 8 * grp, hi);
+            tmem_st8(trow + kColQ + 64 + 8 * grp, lo);
         }
-        float z[32];
+        float z[16];
 #pragma unroll
-        for (int k = 0; k < 32; ++k)
+        for (int k = 0; k < 16; ++k)
             z[k] = 0.0f;
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-            tmem_st32(trow + kColO + 32 * k, z);
+#pragma unroll 1
+        for (int k = 0; k < 8; ++k)
+            tmem_st16f(trow + kColO + 16 * k, z);
         tmem_wait_st();
     }
     tc_fence_before();
@@ -453,16 +476,38 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(VerifyArgs a, Level
     bool timed_out = false;
 
     if (warp == kProdWarp) {
-        // ---- producer: chunk codes into the ring of slots by bulk copy --------
-        if (lane == 0) {
-            int cur_i = -1, cur_p = -1;
-            for (int c = 0; c < nch; ++c) {
-                const int s = c % kRing, i = c >> 3, j = c & 7;
-                // slot s was last decoded for chunk c - kRing
-                if (c >= kRing && !mbar_wait_sleep(&sm.slot_free[s], (uint32_t)(((c - kRing) / kRing) & 1), kWaitLimit)) {
-                    timed_out = true;
-                    break;
-                }
+        // ---- producer: chunk codes into the ring of slots by bulk copy (lane
+        // 0), and the affines of the chunk before (whole warp, once the copies
+        // of that chunk have landed) --------------------------------------------
+        int cur_i = -1, cur_p = -1;
+        auto affines = [&](int c) -> bool {  // whole warp; lane l takes channels 4 l .. 4 l + 3
+            const int s = c % kRing;
+            if (!__all_sync(0xFFFFFFFFu, mbar_wait_sleep(&sm.ring_full[s], (uint32_t)((c / kRing) & 1), kWaitLimit)))
+                return false;
+            Slot<FULL> &sl = sm.slot[s];
+            float4 ka4, kb4, va4, vb4;
+            affine4(sl.kpm, sl.kcm, 4 * lane, ka4, kb4);
+            affine4(sl.vpm, sl.vcm, 4 * lane, va4, vb4);
+            *reinterpret_cast<float4 *>(sl.kaf[lane & 1][lane >> 1]) = ka4;
+            *reinterpret_cast<float4 *>(sl.kbf[lane & 1][lane >> 1]) = kb4;
+            *reinterpret_cast<float4 *>(sl.vaf + 4 * lane) = va4;
+            *reinterpret_cast<float4 *>(sl.vbf + 4 * lane) = vb4;
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&sm.aff_ready[s]);
+            return true;
+        };
+        bool ok = true;
+        for (int c = 0; c < nch; ++c) {
+            const int s = c % kRing, i = c >> 3, j = c & 7;
+            // slot s was last decoded for chunk c - kRing
+            if (c >= kRing &&
+                !__all_sync(0xFFFFFFFFu,
+                            mbar_wait_sleep(&sm.slot_free[s], (uint32_t)(((c - kRing) / kRing) & 1), kWaitLimit))) {
+                ok = false;
+                break;
+            }
+            if (lane == 0) {
                 if (i != cur_i) {            // one page-table read a page
                     cur_i = i;
                     cur_p = phys_of(i);
@@ -474,28 +519,32 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(VerifyArgs a, Level
                 sm.slot_page[s] = cur_p;
                 if (cur_p < 0) {
                     mbar_arrive(bar);
-                    continue;
+                } else {
+                    fence_proxy_async_smem();    // the decoders' reads of the slot come before the copies' writes
+                    const int64_t rows = ((int64_t)kvh * T + (int64_t)cur_p * kPage + j * kChunk) * kRow;
+                    const int64_t pmo = ((int64_t)kvh * a.pool_pages + cur_p) * (2 * kD);
+                    const int64_t cmo = (((int64_t)kvh * a.pool_pages + cur_p) * kNChunk + j) * (2 * kD);
+                    mbar_arrive_expect_tx(bar, (FULL ? 4u : 2u) * kChunk * kRow + 2 * (2 * kD * 4) + 2 * (2 * kD * 2));
+                    bulk_g2s(sl.ka, a.ka + rows, kChunk * kRow, bar);
+                    bulk_g2s(sl.va, a.va + rows, kChunk * kRow, bar);
+                    if (FULL) {
+                        bulk_g2s(sl.kr, a.kr + rows, kChunk * kRow, bar);
+                        bulk_g2s(sl.vr, a.vr + rows, kChunk * kRow, bar);
+                    }
+                    bulk_g2s(sl.kpm, a.kpm + pmo, 2 * kD * 4, bar);
+                    bulk_g2s(sl.vpm, a.vpm + pmo, 2 * kD * 4, bar);
+                    bulk_g2s(sl.kcm, a.kcm + cmo, 2 * kD * 2, bar);
+                    bulk_g2s(sl.vcm, a.vcm + cmo, 2 * kD * 2, bar);
                 }
-                fence_proxy_async_smem();    // the decoders' reads of the slot come before the copies' writes
-                const int64_t rows = ((int64_t)kvh * T + (int64_t)cur_p * kPage + j * kChunk) * kRow;
-                const int64_t pmo = ((int64_t)kvh * a.pool_pages + cur_p) * (2 * kD);
-                const int64_t cmo = (((int64_t)kvh * a.pool_pages + cur_p) * kNChunk + j) * (2 * kD);
-                mbar_arrive_expect_tx(bar, (FULL ? 4u : 2u) * kChunk * kRow + 2 * (2 * kD * 4) + 2 * (2 * kD * 2));
-                bulk_g2s(sl.ka, a.ka + rows, kChunk * kRow, bar);
-                bulk_g2s(sl.va, a.va + rows, kChunk * kRow, bar);
-                if (FULL) {
-                    bulk_g2s(sl.kr, a.kr + rows, kChunk * kRow, bar);
-                    bulk_g2s(sl.vr, a.vr + rows, kChunk * kRow, bar);
-                }
-                bulk_g2s(sl.kpm, a.kpm + pmo, 2 * kD * 4, bar);
-                bulk_g2s(sl.vpm, a.vpm + pmo, 2 * kD * 4, bar);
-                bulk_g2s(sl.kcm, a.kcm + cmo, 2 * kD * 2, bar);
-                bulk_g2s(sl.vcm, a.vcm + cmo, 2 * kD * 2, bar);
             }
-            // let every copy issued land before the CTA exits (bounded)
-            for (int c = max(nch - kRing, 0); c < nch; ++c)
-                mbar_wait_sleep(&sm.ring_full[c % kRing], (uint32_t)((c / kRing) & 1), kWaitLimit);
+            __syncwarp();
+            if (c >= 1 && !(ok = affines(c - 1)))
+                break;
         }
+        // the last chunk's affines; every copy issued has then landed (bounded)
+        if (ok && nch > 0)
+            ok = affines(nch - 1);
+        timed_out = !ok;
     } else if (warp >= kSoftWarps && warp < kMmaWarp) {
         // ---- decode warps ----------------------------------------------------
         const int u = 32 * (warp - kSoftWarps) + lane;
@@ -504,7 +553,8 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(VerifyArgs a, Level
             const int s = c % kRing, buf = c % kBufs;
             const uint32_t prev = (uint32_t)(((c - kBufs) / kBufs) & 1);
             // codes in; K tile `buf` last read by the Q.K^T of chunk c - kBufs
-            bool ok = mbar_wait_sleep(&sm.ring_full[s], (uint32_t)((c / kRing) & 1), kWaitLimit);
+            bool ok = mbar_wait_sleep(&sm.ring_full[s], (uint32_t)((c / kRing) & 1), kWaitLimit) &&
+                      mbar_wait_sleep(&sm.aff_ready[s], (uint32_t)((c / kRing) & 1), kWaitLimit);
             if (ok && c >= kBufs)
                 ok = mbar_wait_sleep(&sm.s_full[buf], prev, kWaitLimit);
             if (!__all_sync(0xFFFFFFFFu, ok)) {
@@ -533,24 +583,23 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(VerifyArgs a, Level
             }
         }
     } else if (warp == kMmaWarp) {
-        // ---- MMA warp: one thread issues every tcgen05.mma in a fixed order,
-        // S = Q.K^T of chunk c + 1 (as soon as its K tile is decoded), then
-        // O += P.V of chunk c (as soon as its P is written and its V tile
-        // decoded); each wait blocks in hardware (bounded)
+        // ---- Q.K^T issuer: S of chunk c as soon as its K tile is decoded and
+        // S buffer c % kBufs has been read by the softmax
         if (lane == 0 && nch > 0) {
             // Q_hi against the stacked [K_hi; K_lo] (64 rows) gives both cross
             // terms in one product: columns 0-31 Q_hi.K_hi, 32-63 Q_hi.K_lo;
             // Q_lo.K_hi accumulates into columns 0-31
             constexpr uint32_t id64 = idesc_f16(kRows, 2 * kChunk), id32 = idesc_f16(kRows, kChunk);
-            constexpr uint32_t idpv = idesc_f16(kRows, kD);
-            const uint32_t tO = tmem + kColO, tQh = tmem + kColQ, tQl = tmem + kColQ + kD / 2;
-            const uint32_t k0 = smem_u32(sm.k), v0 = smem_u32(sm.v);
-            auto issue_qk = [&](int c) -> bool {
+            const uint32_t tQh = tmem + kColQ, tQl = tmem + kColQ + kD / 2;
+            const uint32_t k0 = smem_u32(sm.k);
+            for (int c = 0; c < nch; ++c) {
                 const int buf = c % kBufs;
-                if (!mbar_wait_sleep(&sm.k_full[buf], (uint32_t)((c / kBufs) & 1), kWaitLimit))
-                    return false;
-                if (c >= kBufs && !mbar_wait_sleep(&sm.s_free[buf], (uint32_t)(((c - kBufs) / kBufs) & 1), kWaitLimit))
-                    return false;
+                if (!mbar_wait_sleep(&sm.k_full[buf], (uint32_t)((c / kBufs) & 1), kWaitLimit) ||
+                    (c >= kBufs &&
+                     !mbar_wait_sleep(&sm.s_free[buf], (uint32_t)(((c - kBufs) / kBufs) & 1), kWaitLimit))) {
+                    timed_out = true;
+                    break;
+                }
                 tc_fence_after();
                 const uint32_t tS = tmem + kColS + 64u * buf;
                 const uint32_t kb = k0 + (uint32_t)buf * (uint32_t)sizeof(sm.k[0]);
@@ -561,17 +610,25 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(VerifyArgs a, Level
                     umma_ts(tS, tQl + 8 * st, kd, id32, 1u);
                 }
                 umma_commit(&sm.s_full[buf]);
-                return true;
-            };
-            bool ok = issue_qk(0);
-            for (int c = 0; ok && c < nch; ++c) {
-                if (c + 1 < nch && !(ok = issue_qk(c + 1)))
-                    break;
+            }
+            // every MMA this thread issued must finish before the tensor memory
+            // is freed (the commit tracks all of them; bounded)
+            umma_commit(&sm.drained);
+            mbar_wait_sleep(&sm.drained, 0u, kWaitLimit);
+        }
+    } else if (warp == kPvWarp) {
+        // ---- P.V issuer: O += P.V of chunk c as soon as its P is written and
+        // its V tile decoded
+        if (lane == 0 && nch > 0) {
+            constexpr uint32_t idpv = idesc_f16(kRows, kD);
+            const uint32_t tO = tmem + kColO, v0 = smem_u32(sm.v);
+            for (int c = 0; c < nch; ++c) {
                 const int buf = c % kBufs, pb = c % kPBufs;
-                ok = mbar_wait_sleep(&sm.p_full[pb], (uint32_t)((c / kPBufs) & 1), kWaitLimit) &&
-                     mbar_wait_sleep(&sm.v_full[buf], (uint32_t)((c / kBufs) & 1), kWaitLimit);
-                if (!ok)
+                if (!mbar_wait_sleep(&sm.p_full[pb], (uint32_t)((c / kPBufs) & 1), kWaitLimit) ||
+                    !mbar_wait_sleep(&sm.v_full[buf], (uint32_t)((c / kBufs) & 1), kWaitLimit)) {
+                    timed_out = true;
                     break;
+                }
                 tc_fence_after();
                 const uint32_t tPh = tmem + kColP + 32u * pb, tPl = tPh + 16;
                 const uint32_t vb = v0 + (uint32_t)buf * (uint32_t)sizeof(sm.v[0]);
@@ -585,11 +642,8 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(VerifyArgs a, Level
                 }
                 umma_commit(&sm.pv_done[buf]);
             }
-            timed_out = !ok;
-            // every MMA issued must finish before the tensor memory is freed
-            // (the commit tracks all of this thread's earlier MMAs; bounded)
-            umma_commit(&sm.drained);
-            mbar_wait_sleep(&sm.drained, 0u, kWaitLimit);
+            umma_commit(&sm.drained_pv);
+            mbar_wait_sleep(&sm.drained_pv, 0u, kWaitLimit);
         }
     } else {
         // ---- softmax warps: one query row per thread -------------------------
@@ -606,10 +660,17 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(VerifyArgs a, Level
                 break;
             }
             tc_fence_after();
-            float S[32], S2[32];
-            tmem_ld32(trow + kColS + 64 * buf, S);
-            tmem_ld32(trow + kColS + 64 * buf + 32, S2);
-            tmem_wait_ld();
+            float S[32];                     // Q_hi.K_hi + Q_lo.K_hi, plus Q_hi.K_lo, 16 columns at a time
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                float s0[16], s1[16];
+                tmem_ld16(trow + kColS + 64 * buf + 16 * hf, s0);
+                tmem_ld16(trow + kColS + 64 * buf + 32 + 16 * hf, s1);
+                tmem_wait_ld();
+#pragma unroll
+                for (int k = 0; k < 16; ++k)
+                    S[16 * hf + k] = s0[k] + s1[k];
+            }
             tc_fence_before();
             __syncwarp();
             if (lane == 0)
@@ -623,14 +684,12 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(VerifyArgs a, Level
             float mx = neg_inf();
             if (valid && t0 + kChunk <= vis_all) {
 #pragma unroll
-                for (int k = 0; k < 32; ++k) {
-                    S[k] += S2[k];
+                for (int k = 0; k < 32; ++k)
                     mx = fmaxf(mx, S[k]);
-                }
             } else {
 #pragma unroll
                 for (int k = 0; k < 32; ++k) {
-                    S[k] = (!valid || t0 + k >= nvis) ? neg_inf() : S[k] + S2[k];
+                    S[k] = (!valid || t0 + k >= nvis) ? neg_inf() : S[k];
                     mx = fmaxf(mx, S[k]);
                 }
             }
@@ -650,15 +709,15 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(VerifyArgs a, Level
                     m_run = mx;
                     l_run *= alpha;
                 }
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    float o[32];
-                    tmem_ld32(trow + kColO + 32 * k, o);
+#pragma unroll 1
+                for (int k = 0; k < 8; ++k) {    // 16 columns at a time (the scores stay live)
+                    float o[16];
+                    tmem_ld16(trow + kColO + 16 * k, o);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int e = 0; e < 32; ++e)
+                    for (int e = 0; e < 16; ++e)
                         o[e] *= alpha;
-                    tmem_st32(trow + kColO + 32 * k, o);
+                    tmem_st16f(trow + kColO + 16 * k, o);
                 }
                 tmem_wait_st();
             }
@@ -672,15 +731,19 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(VerifyArgs a, Level
             // m_run is -inf only while every score so far (this chunk's too) is
             // masked: then every weight is exp2(-inf) = 0
             const float m_eff = m_run == neg_inf() ? 0.0f : m_run;
-            uint32_t ph[16], pl[16];
 #pragma unroll
-            for (int k = 0; k < 16; ++k) {
-                const float p0 = exp2_sm(S[2 * k] - m_eff), p1 = exp2_sm(S[2 * k + 1] - m_eff);
-                l_run += p0 + p1;
-                split2(make_float2(p0, p1), ph[k], pl[k]);
+            for (int hf = 0; hf < 2; ++hf) {     // P hi words 8 hf .. + 7, then the lo words
+                uint32_t ph[8], pl[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const int c2 = 2 * (8 * hf + k);
+                    const float p0 = exp2_sm(S[c2] - m_eff), p1 = exp2_sm(S[c2 + 1] - m_eff);
+                    l_run += p0 + p1;
+                    split2(make_float2(p0, p1), ph[k], pl[k]);
+                }
+                tmem_st8(trow + kColP + 32 * pb + 8 * hf, ph);
+                tmem_st8(trow + kColP + 32 * pb + 16 + 8 * hf, pl);
             }
-            tmem_st16(trow + kColP + 32 * pb, ph);
-            tmem_st16(trow + kColP + 32 * pb + 16, pl);
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
@@ -693,15 +756,15 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(VerifyArgs a, Level
             timed_out = true;
         tc_fence_after();
         float *part = a.part + ((((int64_t)b * Tq + pos) * a.Hq + h) * a.n_splits + split) * kPart;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            float o[32];
-            tmem_ld32(trow + kColO + 32 * k, o);
+#pragma unroll 1
+        for (int k = 0; k < 8; ++k) {
+            float o[16];
+            tmem_ld16(trow + kColO + 16 * k, o);
             tmem_wait_ld();
             if (rowok)                       // a partial is 130 floats: 8-byte aligned
 #pragma unroll
-                for (int e = 0; e < 32; e += 2)
-                    *reinterpret_cast<float2 *>(part + 32 * k + e) = make_float2(o[e], o[e + 1]);
+                for (int e = 0; e < 16; e += 2)
+                    *reinterpret_cast<float2 *>(part + 16 * k + e) = make_float2(o[e], o[e + 1]);
         }
         if (rowok) {
             part[kD] = m_run;
