@@ -98,3 +98,23 @@ def test_positions_before_the_context_are_zero_and_bad_pages_flagged(lx, orc):
                          dev_err=err).cpu().numpy()
     assert np.all(out[0, :3] == 0.0) and np.all(np.abs(out[0, 3:]).sum(-1) > 0)
     assert int(err.item()) & 1
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_single_position_equals_decode_attention(lx, orc, mode):
+    """A block of one draft position is one decode step: the verify kernel
+    (tensor-memory accumulators, decoded tiles) and the decode kernel
+    (register-direct level operands) must agree, each within its bound of the
+    oracle, so within twice the bound of each other."""
+    w = S.WORKLOADS[4]
+    ctx, pool, table = S.batched_layout(w)
+    pick = [1, 8, 30]
+    ctx, table = ctx[pick], table[pick]
+    cache = _cache(lx, orc, w, 1, 8, pool * 256)
+    (kq, kr), (vq, vr) = cache[S.S_K], cache[S.S_V]
+    qb = _queries(w, len(pick), 1, 64)
+    full = mode == lx.MODE_FULL
+    ov = lx.verify_attn(bf16_dev(qb), kq, vq, 0, i32_dev(table), i32_dev(ctx), 128 ** -0.5, mode).cpu().numpy()[:, 0]
+    od = lx.decode_attn(bf16_dev(qb[:, 0]), kq, vq, 0, i32_dev(table), i32_dev(ctx), 128 ** -0.5, mode).cpu().numpy()
+    tol = attn_tolerance(orc, qb[:, 0], kr, vr, 0, table, np.asarray(ctx), 128 ** -0.5, full)
+    assert np.all(np.abs(ov - od) <= 2 * tol)
