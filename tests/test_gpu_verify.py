@@ -118,3 +118,15 @@ def test_single_position_equals_decode_attention(lx, orc, mode):
     od = lx.decode_attn(bf16_dev(qb[:, 0]), kq, vq, 0, i32_dev(table), i32_dev(ctx), 128 ** -0.5, mode).cpu().numpy()
     tol = attn_tolerance(orc, qb[:, 0], kr, vr, 0, table, np.asarray(ctx), 128 ** -0.5, full)
     assert np.all(np.abs(ov - od) <= 2 * tol)
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_odd_group_and_block(lx, orc, mode):
+    """G = 5 (20 query heads over 4 KV heads) and a block of 37 positions: row
+    blocks, head mapping and causal masks off every power-of-two boundary."""
+    w = S.WORKLOADS[2]
+    T = 2048
+    cache = _cache(lx, orc, w, 1, 4, T)
+    table = np.arange(T // 256, dtype=np.int32)[None]
+    _check(lx, orc, cache, _queries(w, 1, 37, 20), 0, table, np.array([T - 300]), mode,
+           positions=[0, 1, 18, 35, 36])
