@@ -13,9 +13,11 @@
 // fp32 step rounds to nearest with no fused multiply-add, so the codes are
 // those of the written definition. A split (a, r) gives 2^(a+r-1) - 1 levels.
 //
-// A CTA encodes one page (256 tokens x 128 channels, 64 KiB of bf16 staged in
-// shared memory); thread (d, half) owns channel d over tokens
-// 128 half .. 128 half + 127.
+// A CTA encodes one page (256 tokens x 128 channels); thread (d, half) owns
+// channel d over tokens 128 half .. 128 half + 127 and reads it straight from
+// global memory (a warp reads 64 contiguous bytes a token; the passes after
+// the first hit in L1), so occupancy is set by registers, not by a page
+// buffer.
 #include <cfloat>
 #include <cmath>
 #include <cuda_fp16.h>
@@ -42,7 +44,6 @@ struct VariantArgs {
 };
 
 struct SmemV {
-    uint16_t x[kPage * kD];
     float thr[kMaxQ + 1];
     float lv[kMaxQ + 2];
     float mn[2][kD], mx[2][kD];
@@ -55,19 +56,17 @@ __device__ __forceinline__ float bf16f(uint16_t b) { return __uint_as_float((uin
 // Floor division by 2^r of a signed integer.
 __device__ __forceinline__ int floor_shift(int b, int r) { return b >= 0 ? (b >> r) : -((-b + (1 << r) - 1) >> r); }
 
-// Stage the page, then each thread's channel minimum and maximum over its
-// half; returns (mn, rng) of the channel over the page, NaN if it holds a NaN.
-__device__ __forceinline__ void page_range(SmemV &sm, const uint16_t *xp, int d, int half, float &mn, float &rng)
+// Each thread's channel minimum and maximum over its half of the page (read
+// straight from global memory: consecutive threads read consecutive
+// channels), combined through shared memory; returns (mn, rng) of the channel
+// over the page, NaN if it holds a NaN.
+__device__ __forceinline__ void page_range(SmemV &sm, const uint16_t *__restrict__ xp, int d, int half, float &mn,
+                                           float &rng)
 {
-    const uint4 *src = reinterpret_cast<const uint4 *>(xp);
-    uint4 *dst = reinterpret_cast<uint4 *>(sm.x);
-    for (int i = threadIdx.x; i < kPage * kD / 8; i += kThreadsV)
-        dst[i] = src[i];
-    __syncthreads();
     float lo = __int_as_float(0x7F800000), hi = -lo;
     int nan = 0;
     for (int t = 128 * half; t < 128 * half + 128; ++t) {
-        const float v = bf16f(sm.x[t * kD + d]);
+        const float v = bf16f(__ldg(xp + t * kD + d));
         if (v != v) {
             nan = 1;
             continue;
@@ -141,8 +140,9 @@ __global__ void __launch_bounds__(kThreadsV) variant_kernel(const __grid_constan
         a.page_meta[(page * 2 + 0) * kD + d] = mn;
         a.page_meta[(page * 2 + 1) * kD + d] = rng;
     }
+    const uint16_t *__restrict__ xp = a.x + page * kPage * kD;
     auto u_of = [&](int t) -> float {    // stage 1 value of token t
-        const float x = bf16f(sm.x[t * kD + d]);
+        const float x = bf16f(__ldg(xp + t * kD + d));
         if (!page_norm)
             return x;
         return degenerate ? 0.0f : __fmul_rn(__fsub_rn(x, mn), inv);
@@ -206,7 +206,7 @@ __global__ void __launch_bounds__(kThreadsV) variant_kernel(const __grid_constan
             const int kf = min(abs(c), a.qmax + 1), ka = min(abs(ca), a.qmax + 1);
             const float lf = c > 0 ? sm.lv[kf] : (c < 0 ? -sm.lv[kf] : 0.0f);
             const float la = ca > 0 ? sm.lv[ka] : (ca < 0 ? -sm.lv[ka] : 0.0f);
-            const float x = bf16f(sm.x[t * kD + d]);
+            const float x = bf16f(__ldg(xp + t * kD + d));
             const float ef = __fsub_rn(__fmaf_rn(bm, lf, am), x), ea = __fsub_rn(__fmaf_rn(bm, la, am), x);
             e0 = __fmaf_rn(x, x, e0);
             e1 = __fmaf_rn(ea, ea, e1);
@@ -224,8 +224,9 @@ __global__ void __launch_bounds__(kThreadsV) uniform_kernel(const __grid_constan
     SmemV &sm = *reinterpret_cast<SmemV *>(smem_raw);
     const int64_t page = blockIdx.x;
     const int d = threadIdx.x & (kD - 1), half = threadIdx.x >> 7;
+    const uint16_t *__restrict__ xp = a.x + page * kPage * kD;
     float mn, rng;
-    page_range(sm, a.x + page * kPage * kD, d, half, mn, rng);
+    page_range(sm, xp, d, half, mn, rng);
     if (a.page_meta && half == 0) {
         const bool tok = a.flags & LYNX_VAR_UNIFORM_PER_TOKEN;   // no per-(page, channel) grid: zeros
         a.page_meta[(page * 2 + 0) * kD + d] = tok ? 0.0f : mn;
@@ -240,7 +241,7 @@ __global__ void __launch_bounds__(kThreadsV) uniform_kernel(const __grid_constan
         float lo = __int_as_float(0x7F800000), hi = -lo;
         int nan = 0;
         for (int j = 0; j < kD; ++j) {
-            const float v = bf16f(sm.x[t * kD + ((j + t) & (kD - 1))]);
+            const float v = bf16f(__ldg(xp + t * kD + ((j + t) & (kD - 1))));
             if (v != v) {
                 nan = 1;
                 continue;
@@ -255,7 +256,7 @@ __global__ void __launch_bounds__(kThreadsV) uniform_kernel(const __grid_constan
         const float step = __fdiv_rn(trg, top);
         for (int j = 0; j < kD; ++j) {
             const int dd = (j + t) & (kD - 1);
-            const float x = bf16f(sm.x[t * kD + dd]);
+            const float x = bf16f(__ldg(xp + t * kD + dd));
             float q = floorf(__fadd_rn(__fmul_rn(__fsub_rn(x, tmn), inv_step), 0.5f));
             q = q != q ? 0.0f : fminf(fmaxf(q, 0.0f), top);
             if (a.codes)
@@ -270,7 +271,7 @@ __global__ void __launch_bounds__(kThreadsV) uniform_kernel(const __grid_constan
     const float inv_step = rng > 0.0f ? __fdiv_rn(top, rng) : 0.0f;
     const float step = __fdiv_rn(rng, top);
     for (int t = 128 * half; t < 128 * half + 128; ++t) {
-        const float x = bf16f(sm.x[t * kD + d]);
+        const float x = bf16f(__ldg(xp + t * kD + d));
         float q = floorf(__fadd_rn(__fmul_rn(__fsub_rn(x, mn), inv_step), 0.5f));
         q = q != q ? 0.0f : fminf(fmaxf(q, 0.0f), top);
         if (a.codes)
