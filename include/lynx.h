@@ -70,7 +70,10 @@ typedef enum { LYNX_MODE_ANCHOR = 0, LYNX_MODE_FULL = 1 } lynx_mode;
 /* Device-error bits written (OR-ed) into *dev_err by lynx_decode_attn and lynx_quantize_append. */
 #define LYNX_DEVERR_PAGE 1u   /* a page-table entry outside [0, tokens/256) */
 #define LYNX_DEVERR_CTX 2u    /* a context length outside [0, max_pages*256] */
-#define LYNX_DEVERR_TIMEOUT 4u /* a bulk copy did not complete within the kernel's wait limit */
+#define LYNX_DEVERR_TIMEOUT 4u /* a wait (a bulk copy, a tensor-core completion, a barrier between the
+                                  kernel's warps) ran past its limit, or the kernel could not start
+                                  (its shared-memory window was not where it needs it); the outputs
+                                  the wait guarded are not valid */
 
 /*
  * One quantized tensor (K or V): a view of caller-owned device memory.
