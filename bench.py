@@ -681,7 +681,8 @@ def ablation_report(args):
     / sum x^2) of the anchor-only and the full reconstruction for each variant
     of the quantizer and for the uniform comparators, on the K and V of the
     Qwen3-235B-like layer (4 KV heads x 32K tokens, Laplace with outlier
-    channels), and the variant encoder's throughput on 2 layers of the full
+    channels); the vNMSE of the attention output over that layer (section 5's
+    measure); and the variant encoder's throughput on 2 layers of the full
     cache's shape (268 MB of bf16 per tensor, larger than L2)."""
     import torch
     import __graft_entry__
@@ -695,19 +696,39 @@ def ablation_report(args):
     for s_ in (S.S_K, S.S_V):
         xs[s_] = torch.empty((1, w.H, w.T, D), dtype=torch.bfloat16, device=dev)
         gen.fill(xs[s_], w.key(s_), w.scales(s_))
+    # attention-output vNMSE: one decode step of B_Q requests x 64 query heads
+    # over the layer, the reconstruction's output against the output over the
+    # original (bf16) values, both through the same fp32 dense attention
+    n_req = 8
+    q = torch.from_numpy(w.queries_bf16(n_req, w.Hq).view(np.int16)).to(dev).view(torch.bfloat16)
+    kf, vf = (xs[s_].view(w.H, w.T, D).float() for s_ in (S.S_K, S.S_V))
+    o_ref = lx.dense_attn(q, kf, vf).double()
+    ref_sq = float((o_ref * o_ref).sum())
+    del kf, vf
     rows = []
     for name, kw in ABLATION:
         r = {"name": name, "knobs": kw}
+        rec = {}
         for s_, lab in ((S.S_K, "k"), (S.S_V, "v")):
-            e = lx.quantize_variant(xs[s_], **kw)["err"].sum(dim=(0, 1)).cpu().numpy()
+            g = lx.quantize_variant(xs[s_], recon=True, **kw)
+            e = g["err"].sum(dim=(0, 1)).cpu().numpy()
             r[lab] = {"anchor": float(e[1] / e[0]), "full": float(e[2] / e[0])}
+            rec[lab] = g
+        r["attn"] = {}
+        for part in ("anchor", "full"):
+            o = lx.dense_attn(q, rec["k"]["x_" + part].view(w.H, w.T, D), rec["v"]["x_" + part].view(w.H, w.T, D))
+            r["attn"][part] = float(((o.double() - o_ref) ** 2).sum()) / ref_sq
+        del rec
         rows.append(r)
     by = {r["name"]: r for r in rows}
+    base, two = "lynx (C=32, 4+4, alpha=255)", "lynx 4-bit code (split 2+2)"
     ratio = {  # vNMSE of uniform INT4 / vNMSE of a Lynx reconstruction from 4 bits a value
-        f"{u} / lynx {lab_l}": {t: by[u][t]["full"] / by[l][t][part] for t in ("k", "v")}
+        f"{u} / lynx {lab_l}": {t: by[u][t]["full"] / by[l][t][part] for t in ("k", "v", "attn")}
         for u in ("uniform INT4 per page-channel", "uniform INT4 per token")
-        for lab_l, l, part in (("anchor-only of 4+4", "lynx (C=32, 4+4, alpha=255)", "anchor"),
-                               ("4-bit code (2+2)", "lynx 4-bit code (split 2+2)", "full"))}
+        for lab_l, l, part in (("anchor-only of 4+4", base, "anchor"), ("4-bit code (2+2)", two, "full"))}
+    ratio.update({  # uniform INT8 / the full 8-bit Lynx reconstruction
+        f"{u} / lynx full 4+4": {t: by[u][t]["full"] / by[base][t]["full"] for t in ("k", "v", "attn")}
+        for u in ("uniform INT8 per page-channel", "uniform INT8 per token")})
     del xs
     # throughput: the base variant and the comparator, errors only
     wt = S.WORKLOADS[3]
@@ -721,13 +742,14 @@ def ablation_report(args):
             lx.quantize_variant(big, **kw)
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = max(args.steps, 400)          # long enough for the clock sampler to see the region
         with ClockSampler(0) as clk:
             e0.record()
-            for _ in range(args.steps):
+            for _ in range(reps):
                 lx.quantize_variant(big, **kw)
             e1.record()
             torch.cuda.synchronize()
-        ms = e0.elapsed_time(e1) / args.steps
+        ms = e0.elapsed_time(e1) / reps
         timing[name] = {"ms": ms, "gbs": 2.0 * elems / (ms * 1e-3) / 1e9, "clocks": clk.summary()}
     cpu = None
     if not args.no_cpu_baseline:
@@ -747,8 +769,11 @@ def ablation_report(args):
         "report": "ablation",
         "metric": "quantizer variants: vNMSE on synthetic KV, and the variant encoder's GB/s vs HBM roofline (1 GB300)",
         "value": g, "unit": "GB/s", "steps": args.steps,
-        "config": {"workload": f"quality: {w.name} (K and V); throughput: 2 layers x {wt.H} KV heads x "
-                               f"{wt.T} tokens (K), errors only", "vnmse": "sum (x_hat - x)^2 / sum x^2"},
+        "config": {"workload": f"quality: {w.name} (K and V, {n_req} requests x {w.Hq} query heads for the "
+                               f"attention output); throughput: 2 layers x {wt.H} KV heads x {wt.T} tokens (K), "
+                               f"errors only",
+                   "vnmse": "k, v: sum (x_hat - x)^2 / sum x^2; attn: sum (o_hat - o)^2 / sum o^2, o the fp32 "
+                            "decode attention over the original bf16 K and V, o_hat over the reconstruction"},
         "roofline": {"bound": "hbm", "achieved": g, "peak": hbm, "unit": "GB/s", "frac": g / hbm,
                      "peak_kind": kind, "note": "algorithmic bytes: 2 B read per element, outputs negligible"},
         "timing": timing, "variants": rows, "uniform_int4_over_lynx_4bit_vnmse": ratio,

@@ -295,12 +295,32 @@ typedef struct {
  *   err         [n][tokens/256][3] fp64 per page: sum x^2, sum (x_anchor - x)^2,
  *               sum (x_full - x)^2 (uniform: the last two are equal); the
  *               reconstructions are evaluated in fp32
+ *   x_anchor    [n][tokens][128] fp32: the anchor-only reconstruction
+ *   x_full      [n][tokens][128] fp32: the full reconstruction (uniform: both
+ *               hold the comparator's reconstruction)
  * Returns LYNX_ERR_SHAPE / LYNX_ERR_UNSUPPORTED for sizes or knobs outside
  * the ranges above, LYNX_ERR_ALIGN for misaligned pointers.
  */
 lynx_status lynx_quantize_variant(const void *x_bf16, int32_t n, int32_t tokens, const lynx_variant *v,
                                   int16_t *codes, int8_t *anchor, uint8_t *residual, float *page_meta,
-                                  uint16_t *chunk_meta, double *err, void *stream);
+                                  uint16_t *chunk_meta, double *err, float *x_anchor, float *x_full,
+                                  void *stream);
+
+/*
+ * Decode attention over a DENSE fp32 cache, for quality studies: the Lynx
+ * reading's evaluation (section 5) measures the error of the attention
+ * output, so a reconstruction (x_anchor / x_full above) is scored by running
+ * this on it and on the original values. Not part of the method's path.
+ *   q_bf16  [batch][q_heads][128] bf16, one query per request
+ *   k, v    [kv_heads][tokens][128] fp32, shared by every request, 16-byte aligned
+ *   out     [batch][q_heads][128] fp32
+ * out[b][h] = sum_t softmax_t(sm_scale q[b][h] . k[g][t]) v[g][t] with
+ * g = h / (q_heads / kv_heads), fp32 arithmetic. Device memory, caller-owned,
+ * asynchronous on `stream`. Returns LYNX_ERR_SHAPE unless q_heads is a
+ * multiple of kv_heads and 1 <= tokens <= 49152 (batch or q_heads 0: no-op).
+ */
+lynx_status lynx_dense_attn(const void *q_bf16, const float *k, const float *v, int32_t batch, int32_t q_heads,
+                            int32_t kv_heads, int32_t tokens, float sm_scale, float *out, void *stream);
 
 /*
  * Diagnostics (no counterpart in the method: they expose the library's own

@@ -33,7 +33,10 @@ Readings (where the pages leave a step open):
   over its 128 channels), 2^b levels, code = floor((x - mn) * ((2^b - 1) /
   rng) + 1/2) with every step in fp32 (the integer decision is taken in the
   precision the GPU takes it), decoded in fp64;
-- vNMSE: sum (x_hat - x)^2 / sum x^2 over the tensor.
+- vNMSE: sum (x_hat - x)^2 / sum x^2 over the tensor; the section 5 figures
+  are the vNMSE of the attention output, so ``dense_attn`` runs one decode
+  step over a dense cache (the original values or a reconstruction) and
+  ``attn_vnmse`` takes the same ratio over the outputs [batch, heads, 128].
 
 The encoder follows the same numeric contract as the main oracle: fp32 with
 round-to-nearest and no fused multiply-add, a stride-halving tree for the
@@ -280,3 +283,31 @@ def vnmse(err: np.ndarray) -> tuple[float, float]:
     """(anchor-only, full) vNMSE of a tensor from its per-page error sums."""
     e = np.asarray(err, dtype=np.float64).reshape(-1, 3).sum(axis=0)
     return float(e[1] / e[0]), float(e[2] / e[0])
+
+
+def dense_attn(q_bf16, k, v, sm_scale: float) -> np.ndarray:
+    """fp64 decode attention of one query per (request, query head) over a
+    dense cache shared by every request: q [B, Hq, 128] bf16 bits, k and v
+    [H, T, 128] real values. out[b, h] = softmax(sm_scale K_g q) V_g with
+    g = h // (Hq / H), the textbook definition (max subtracted before exp)."""
+    q = _bf16_to_f32(q_bf16).astype(np.float64)
+    B, Hq, d = q.shape
+    K = np.asarray(k, dtype=np.float64)
+    Vv = np.asarray(v, dtype=np.float64)
+    H, T, _ = K.shape
+    assert d == D and Hq % H == 0 and T > 0
+    G = Hq // H
+    out = np.empty((B, Hq, D), np.float64)
+    for h in range(Hq):
+        g = h // G
+        s = sm_scale * (q[:, h, :] @ K[g].T)              # [B, T]
+        p = np.exp(s - s.max(axis=1, keepdims=True))
+        out[:, h, :] = (p @ Vv[g]) / p.sum(axis=1, keepdims=True)
+    return out
+
+
+def attn_vnmse(out_hat, out_ref) -> float:
+    """vNMSE of an attention output against the reference output."""
+    o = np.asarray(out_ref, dtype=np.float64)
+    e = np.asarray(out_hat, dtype=np.float64) - o
+    return float((e * e).sum() / (o * o).sum())

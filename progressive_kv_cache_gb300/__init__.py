@@ -88,9 +88,11 @@ def _lib():
             L.lynx_host_tables.restype = None
             L.lynx_level_codes.argtypes = [vp, i64, vp, vp]
             L.lynx_quantize_variant.argtypes = [vp, i32, i32, ctypes.POINTER(LynxVariant), vp, vp, vp, vp, vp, vp,
-                                                vp]
+                                                vp, vp, vp]
+            L.lynx_dense_attn.argtypes = [vp, vp, vp, i32, i32, i32, i32, ctypes.c_float, vp, vp]
             for f in ("lynx_quantize_pages", "lynx_quantize_append", "lynx_dequant_anchor", "lynx_refine_residual",
-                      "lynx_decode_attn", "lynx_verify_attn", "lynx_level_codes", "lynx_quantize_variant"):
+                      "lynx_decode_attn", "lynx_verify_attn", "lynx_level_codes", "lynx_quantize_variant",
+                      "lynx_dense_attn"):
                 getattr(L, f).restype = ctypes.c_int
             _L = L
     return _L
@@ -324,12 +326,13 @@ def level_codes(w, stream=None):
 
 
 def quantize_variant(x, chunk=32, anchor_bits=4, residual_bits=4, alpha=255.0, flags=0, uniform_bits=0,
-                     codes=False, planes=False, meta=False, stream=None):
+                     codes=False, planes=False, meta=False, recon=False, stream=None):
     """lynx_quantize_variant: encode x (bfloat16 [..., tokens, 128], tokens a
     multiple of 256) with one variant of the quantizer in a single pass.
     Returns a dict with "err" (float64 [n, pages, 3]: sum x^2, anchor-only and
     full squared errors per page) and, on request, "codes" (int16), "anchor"
-    (int8) / "residual" (uint8) and "page_meta" / "chunk_meta"."""
+    (int8) / "residual" (uint8), "page_meta" / "chunk_meta" and (recon=True)
+    the fp32 reconstructions "x_anchor" / "x_full" ([n, tokens, 128])."""
     _dev(x, torch.bfloat16, "x")
     if x.dim() < 2 or x.shape[-1] != HEAD_DIM:
         raise ValueError("x must be [..., tokens, 128]")
@@ -348,10 +351,32 @@ def quantize_variant(x, chunk=32, anchor_bits=4, residual_bits=4, alpha=255.0, f
         out["page_meta"] = torch.empty((n, P, 2, HEAD_DIM), dtype=torch.float32, device=dev)
         if not uniform_bits:
             out["chunk_meta"] = torch.empty((n, P, 256 // chunk, 2, HEAD_DIM), dtype=torch.int16, device=dev)
+    if recon:
+        out["x_anchor"] = torch.empty((n, T, HEAD_DIM), dtype=torch.float32, device=dev)
+        out["x_full"] = torch.empty((n, T, HEAD_DIM), dtype=torch.float32, device=dev)
     _check(_lib().lynx_quantize_variant(_ptr(x), n, T, ctypes.byref(v), _ptr(out.get("codes")),
                                         _ptr(out.get("anchor")), _ptr(out.get("residual")),
                                         _ptr(out.get("page_meta")), _ptr(out.get("chunk_meta")), _ptr(out["err"]),
-                                        _stream(stream)),
+                                        _ptr(out.get("x_anchor")), _ptr(out.get("x_full")), _stream(stream)),
            "lynx_quantize_variant")
+    return out
+
+
+def dense_attn(q, k, v, sm_scale=None, stream=None):
+    """lynx_dense_attn: decode attention over a dense fp32 cache (a quality
+    study tool). q: bfloat16 [batch, q_heads, 128]; k, v: float32
+    [kv_heads, tokens, 128], shared by every request. Returns float32
+    [batch, q_heads, 128]."""
+    _dev(q, torch.bfloat16, "q")
+    _dev(k, torch.float32, "k")
+    _dev(v, torch.float32, "v")
+    if q.dim() != 3 or k.dim() != 3 or q.shape[-1] != HEAD_DIM or k.shape != v.shape or k.shape[-1] != HEAD_DIM:
+        raise ValueError("q must be [batch, q_heads, 128], k and v [kv_heads, tokens, 128]")
+    B, Hq = q.shape[0], q.shape[1]
+    H, T = k.shape[0], k.shape[1]
+    scale = HEAD_DIM ** -0.5 if sm_scale is None else sm_scale
+    out = torch.empty((B, Hq, HEAD_DIM), dtype=torch.float32, device=q.device)
+    _check(_lib().lynx_dense_attn(_ptr(q), _ptr(k), _ptr(v), B, Hq, H, T, scale, _ptr(out), _stream(stream)),
+           "lynx_dense_attn")
     return out
 

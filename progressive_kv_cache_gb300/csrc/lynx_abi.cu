@@ -303,7 +303,8 @@ lynx_status lynx_level_codes(const float *w, int64_t n, int8_t *codes, void *str
 
 lynx_status lynx_quantize_variant(const void *x_bf16, int32_t n, int32_t tokens, const lynx_variant *v,
                                   int16_t *codes, int8_t *anchor, uint8_t *residual, float *page_meta,
-                                  uint16_t *chunk_meta, double *err, void *stream)
+                                  uint16_t *chunk_meta, double *err, float *x_anchor, float *x_full,
+                                  void *stream)
 {
     if (!v)
         return LYNX_ERR_NULL;
@@ -329,12 +330,30 @@ lynx_status lynx_quantize_variant(const void *x_bf16, int32_t n, int32_t tokens,
         return LYNX_OK;
     if (!x_bf16)
         return LYNX_ERR_NULL;
-    const void *ptrs[] = {x_bf16, codes, anchor, residual, page_meta, chunk_meta, err};
+    const void *ptrs[] = {x_bf16, codes, anchor, residual, page_meta, chunk_meta, err, x_anchor, x_full};
     for (const void *p : ptrs)
         if (p && !aligned(p, 16))
             return LYNX_ERR_ALIGN;
     return from_cuda(launch_quantize_variant(static_cast<const uint16_t *>(x_bf16), pages, *v, codes, anchor,
-                                             residual, page_meta, chunk_meta, err, (cudaStream_t)stream));
+                                             residual, page_meta, chunk_meta, err, x_anchor, x_full,
+                                             (cudaStream_t)stream));
+}
+
+lynx_status lynx_dense_attn(const void *q_bf16, const float *k, const float *v, int32_t batch, int32_t q_heads,
+                            int32_t kv_heads, int32_t tokens, float sm_scale, float *out, void *stream)
+{
+    if (batch < 0 || q_heads < 0 || kv_heads < 0 || tokens < 0)
+        return LYNX_ERR_SHAPE;
+    if (batch == 0 || q_heads == 0)
+        return LYNX_OK;
+    if (kv_heads == 0 || q_heads % kv_heads || tokens == 0 || tokens > dense_attn_max_tokens())
+        return LYNX_ERR_SHAPE;
+    if (!q_bf16 || !k || !v || !out)
+        return LYNX_ERR_NULL;
+    if (!aligned(k, 16) || !aligned(v, 16) || !aligned(q_bf16, 2) || !aligned(out, 4))
+        return LYNX_ERR_ALIGN;
+    return from_cuda(launch_dense_attn(static_cast<const uint16_t *>(q_bf16), k, v, batch, q_heads, kv_heads, tokens,
+                                       sm_scale, out, (cudaStream_t)stream));
 }
 
 } // extern "C"

@@ -71,7 +71,10 @@ cudaError_t launch_level_codes(const float *w, int64_t n, int8_t *codes, cudaStr
 cudaError_t launch_dequant(const lynx_qkv &in, void *out, bool full, bool f32, cudaStream_t s);
 cudaError_t launch_quantize_variant(const uint16_t *x, int64_t pages, const lynx_variant &v, int16_t *codes,
                                     int8_t *anchor, uint8_t *resid, float *page_meta, uint16_t *chunk_meta,
-                                    double *err, cudaStream_t s);
+                                    double *err, float *x_anchor, float *x_full, cudaStream_t s);
+cudaError_t launch_dense_attn(const uint16_t *q, const float *k, const float *v, int B, int Hq, int H, int T,
+                              float sm_scale, float *out, cudaStream_t s);
+int dense_attn_max_tokens();
 
 struct AttnArgs {
     const uint16_t *q;

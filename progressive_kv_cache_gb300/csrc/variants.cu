@@ -38,6 +38,7 @@ struct VariantArgs {
     float *page_meta;             // [pages][2][128] or null
     uint16_t *chunk_meta;         // [pages][256 / C][2][128] or null
     double *err;                  // [pages][3] or null
+    float *x_anchor, *x_full;     // [pages][256][128] fp32 reconstructions, or null
     int qmax, rbits, bias, flags, ubits;
     float thr[kMaxQ + 1];         // thr[k], k = 1..qmax, increasing; +inf above qmax (thr[0] unused)
     float lv[kMaxQ + 2];          // level value of |code| k = 0..qmax + 1 (fp16-exact)
@@ -207,7 +208,12 @@ __global__ void __launch_bounds__(kThreadsV) variant_kernel(const __grid_constan
             const float lf = c > 0 ? sm.lv[kf] : (c < 0 ? -sm.lv[kf] : 0.0f);
             const float la = ca > 0 ? sm.lv[ka] : (ca < 0 ? -sm.lv[ka] : 0.0f);
             const float x = bf16f(__ldg(xp + t * kD + d));
-            const float ef = __fsub_rn(__fmaf_rn(bm, lf, am), x), ea = __fsub_rn(__fmaf_rn(bm, la, am), x);
+            const float xf = __fmaf_rn(bm, lf, am), xa = __fmaf_rn(bm, la, am);
+            if (a.x_full)
+                a.x_full[o] = xf;
+            if (a.x_anchor)
+                a.x_anchor[o] = xa;
+            const float ef = __fsub_rn(xf, x), ea = __fsub_rn(xa, x);
             e0 = __fmaf_rn(x, x, e0);
             e1 = __fmaf_rn(ea, ea, e1);
             e2 = __fmaf_rn(ef, ef, e2);
@@ -261,7 +267,12 @@ __global__ void __launch_bounds__(kThreadsV) uniform_kernel(const __grid_constan
             q = q != q ? 0.0f : fminf(fmaxf(q, 0.0f), top);
             if (a.codes)
                 a.codes[(page * kPage + t) * kD + dd] = (int16_t)q;
-            const float e = __fsub_rn(__fmaf_rn(q, step, tmn), x);
+            const float xr = __fmaf_rn(q, step, tmn);
+            if (a.x_full)
+                a.x_full[(page * kPage + t) * kD + dd] = xr;
+            if (a.x_anchor)
+                a.x_anchor[(page * kPage + t) * kD + dd] = xr;
+            const float e = __fsub_rn(xr, x);
             e0 = __fmaf_rn(x, x, e0);
             e1 = __fmaf_rn(e, e, e1);
         }
@@ -276,7 +287,12 @@ __global__ void __launch_bounds__(kThreadsV) uniform_kernel(const __grid_constan
         q = q != q ? 0.0f : fminf(fmaxf(q, 0.0f), top);
         if (a.codes)
             a.codes[(page * kPage + t) * kD + d] = (int16_t)q;
-        const float e = __fsub_rn(__fmaf_rn(q, step, mn), x);
+        const float xr = __fmaf_rn(q, step, mn);
+        if (a.x_full)
+            a.x_full[(page * kPage + t) * kD + d] = xr;
+        if (a.x_anchor)
+            a.x_anchor[(page * kPage + t) * kD + d] = xr;
+        const float e = __fsub_rn(xr, x);
         e0 = __fmaf_rn(x, x, e0);
         e1 = __fmaf_rn(e, e, e1);
     }
@@ -287,7 +303,7 @@ __global__ void __launch_bounds__(kThreadsV) uniform_kernel(const __grid_constan
 
 cudaError_t launch_quantize_variant(const uint16_t *x, int64_t pages, const lynx_variant &v, int16_t *codes,
                                     int8_t *anchor, uint8_t *resid, float *page_meta, uint16_t *chunk_meta,
-                                    double *err, cudaStream_t s)
+                                    double *err, float *x_anchor, float *x_full, cudaStream_t s)
 {
     if (pages == 0)
         return cudaSuccess;
@@ -299,6 +315,8 @@ cudaError_t launch_quantize_variant(const uint16_t *x, int64_t pages, const lynx
     a.page_meta = page_meta;
     a.chunk_meta = chunk_meta;
     a.err = err;
+    a.x_anchor = x_anchor;
+    a.x_full = x_full;
     a.flags = (int)v.flags;
     a.ubits = v.uniform_bits;
     const size_t smem = sizeof(SmemV);

@@ -179,14 +179,16 @@ def test_verify_attn_rejects_bad_arguments(lx):
 def test_quantize_variant_rejects_bad_arguments(lx):
     lib = lx.library()
 
-    def call(n=1, T=256, x=0x400000, err=0x500000, codes=None, **kw):
+    def call(n=1, T=256, x=0x400000, err=0x500000, codes=None, xf=None, **kw):
         v = lx.LynxVariant(kw.get("chunk", 32), kw.get("a", 4), kw.get("r", 4), kw.get("alpha", 255.0),
                            kw.get("flags", 0), kw.get("ub", 0))
         return lib.lynx_quantize_variant(ctypes.c_void_p(x) if x else None, n, T, ctypes.byref(v),
                                          ctypes.c_void_p(codes) if codes else None, None, None, None, None,
-                                         ctypes.c_void_p(err) if err else None, None)
+                                         ctypes.c_void_p(err) if err else None, None,
+                                         ctypes.c_void_p(xf) if xf else None, None)
 
-    assert lib.lynx_quantize_variant(None, 1, 256, None, None, None, None, None, None, None, None) == lx.ERR_NULL
+    assert lib.lynx_quantize_variant(None, 1, 256, None, None, None, None, None, None, None, None, None,
+                                     None) == lx.ERR_NULL
     assert call(x=0) == lx.ERR_NULL
     assert call(T=300) == lx.ERR_SHAPE
     assert call(n=-1) == lx.ERR_SHAPE
@@ -200,5 +202,27 @@ def test_quantize_variant_rejects_bad_arguments(lx):
     assert call(ub=9) == lx.ERR_UNSUPPORTED
     assert call(x=0x400008) == lx.ERR_ALIGN
     assert call(codes=0x600002) == lx.ERR_ALIGN
+    assert call(xf=0x700004) == lx.ERR_ALIGN
     assert call(n=0) == lx.OK                                 # nothing to do, no launch
     assert call(T=0) == lx.OK
+
+
+def test_dense_attn_rejects_bad_arguments(lx):
+    lib = lx.library()
+    q, k, v, o = (ctypes.c_void_p(a) for a in (0x400000, 0x500000, 0x600000, 0x700000))
+
+    def call(B=1, Hq=8, H=2, T=64, q=q, k=k, v=v, o=o):
+        return lib.lynx_dense_attn(q, k, v, B, Hq, H, T, 0.088, o, None)
+
+    assert call(B=-1) == lx.ERR_SHAPE
+    assert call(T=-1) == lx.ERR_SHAPE
+    assert call(Hq=6, H=4) == lx.ERR_SHAPE                   # query heads not a multiple of KV heads
+    assert call(H=0) == lx.ERR_SHAPE
+    assert call(T=0) == lx.ERR_SHAPE
+    assert call(T=49153) == lx.ERR_SHAPE                     # scores no longer fit in shared memory
+    assert call(k=None) == lx.ERR_NULL
+    assert call(o=None) == lx.ERR_NULL
+    assert call(k=ctypes.c_void_p(0x500008)) == lx.ERR_ALIGN
+    assert call(q=ctypes.c_void_p(0x400001)) == lx.ERR_ALIGN
+    assert call(B=0) == lx.OK                                # nothing to do, no launch
+    assert call(Hq=0, q=None) == lx.OK

@@ -140,3 +140,83 @@ def test_edge_pages(lx, case):
     assert np.array_equal(np.isfinite(ge).all(axis=-1), fin)
     assert np.allclose(ge[fin][:, 0], oe[fin][:, 0], rtol=1e-4)
     assert np.allclose(ge[fin][:, 1:], oe[fin][:, 1:], rtol=2e-3, atol=1e-9)
+
+
+def _recon_bound(o, xb, case):
+    """Per-element bound on |fp32 reconstruction - fp64 oracle reconstruction|:
+    the kernel forms mn + rng mu and rng s sgn(c) in fp32, then one fused
+    multiply-add with the level (each step within half an ulp), the
+    comparator one fused multiply-add of the code with the fp32 step."""
+    x = (xb.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    N, T, D = x.shape
+    if case.get("uniform_bits"):
+        if case.get("flags", 0) & 16:
+            mn, rng = x.min(axis=-1, keepdims=True), x.max(axis=-1, keepdims=True) - x.min(axis=-1, keepdims=True)
+        else:
+            pm = np.repeat(o["page_meta"].astype(np.float64), 256, axis=1).reshape(N, T, 2, D)
+            mn, rng = pm[:, :, 0], pm[:, :, 1]
+        m = np.abs(mn) + np.abs(rng)
+    else:
+        C = case.get("chunk", 32)
+        pm = np.repeat(o["page_meta"].astype(np.float64), 256, axis=1).reshape(N, T, 2, D)
+        cm = np.repeat(o["chunk_meta"].view(np.float16).astype(np.float64), C, axis=2).reshape(N, T, 2, D)
+        m = np.abs(pm[:, :, 0]) + np.abs(pm[:, :, 1]) * (np.abs(cm[:, :, 0]) + np.abs(cm[:, :, 1]))
+    return 2.0 ** -21 * m
+
+
+@pytest.mark.parametrize("case", [dict(), dict(chunk=16), dict(anchor_bits=2, residual_bits=2), dict(flags=15),
+                                  dict(alpha=0.0), dict(uniform_bits=4), dict(uniform_bits=8, flags=16)],
+                         ids=["default", "C16", "2+2", "flags15", "linear", "int4", "int8-token"])
+def test_reconstructions_match_oracle(lx, xb, case):
+    """The optional fp32 reconstructions (anchor-only and full) against the
+    oracle's fp64 ones, within the rounding of the kernel's fp32 decode."""
+    from oracle import variants as V
+    g = lx.quantize_variant(bf16_dev(xb), recon=True, meta=True, **case)
+    o = V.encode(xb, _variant(case))
+    bound = _recon_bound(o, xb, case)
+    for key in ("x_anchor", "x_full"):
+        d = np.abs(g[key].cpu().numpy().astype(np.float64) - o[key])
+        assert np.all(d <= bound), (key, float((d / bound).max()))
+    # the error sums are those of the stored reconstructions
+    x = torch.from_numpy((xb.astype(np.uint32) << 16).view(np.float32)).cuda().double()
+    ge = g["err"].sum(dim=1)
+    for j, key in ((1, "x_anchor"), (2, "x_full")):
+        e = ((g[key].double() - x) ** 2).sum(dim=(1, 2))
+        assert torch.allclose(ge[:, j], e, rtol=1e-4, atol=1e-30)     # fp32 per-thread sums
+
+
+def _attn_tol(q, k, v, sm):
+    """fp32 bound per (request, head): each score is a 128-term fp32 dot
+    product (error within 128 ulp of sum |q_i k_i|); an error d in the scores
+    moves the output by at most 2 d max|v|, plus the fp32 sums over tokens."""
+    qf = S.bf16_bits_to_f32(q).astype(np.float64)
+    G = q.shape[1] // k.shape[0]
+    ka = np.abs(k).max(axis=1)                      # [H, 128]
+    mag = np.einsum("bhd,hd->bh", np.abs(qf), np.repeat(ka, G, axis=0)) * sm
+    vmax = np.abs(v).max()
+    return (2 * 128 * 2.0 ** -24 * mag * 2 + 1e-5)[..., None] * vmax
+
+
+@pytest.mark.parametrize("H,Hq,T,B", [(1, 1, 1, 1), (2, 8, 300, 3), (4, 64, 4113, 2), (1, 2, 49152, 2)],
+                         ids=["one-token", "ragged", "gqa16", "max-tokens"])
+def test_dense_attention_matches_oracle(lx, H, Hq, T, B):
+    from oracle import variants as V
+    rng = np.random.default_rng(T)
+    k = (rng.laplace(size=(H, T, 128)) * np.where(rng.random(128) < 0.03, 30.0, 1.0)).astype(np.float32)
+    v = rng.laplace(size=(H, T, 128)).astype(np.float32)
+    q = S.f32_to_bf16_bits(rng.laplace(size=(B, Hq, 128)).astype(np.float32))
+    sm = 128 ** -0.5
+    got = lx.dense_attn(torch.from_numpy(q.view(np.int16)).cuda().view(torch.bfloat16),
+                        torch.from_numpy(k).cuda(), torch.from_numpy(v).cuda(), sm).cpu().numpy()
+    want = V.dense_attn(q, k, v, sm)
+    assert np.all(np.abs(got - want) <= _attn_tol(q, k, v, sm))
+
+
+def test_dense_attention_argument_errors(lx):
+    q = torch.zeros((1, 3, 128), dtype=torch.bfloat16, device="cuda")
+    k = torch.zeros((2, 8, 128), dtype=torch.float32, device="cuda")
+    with pytest.raises(RuntimeError):
+        lx.dense_attn(q, k, k)                      # 3 query heads over 2 KV heads
+    big = torch.zeros((1, 49153, 128), dtype=torch.float32, device="cuda")
+    with pytest.raises(RuntimeError):
+        lx.dense_attn(q, big, big)

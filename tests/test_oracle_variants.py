@@ -186,3 +186,69 @@ def test_uniform_per_token_half_step(xb, bits):
     # outlier channels widen every token's grid: per token is coarser here
     per_chan = V.vnmse(V.encode(xb, V.Variant(uniform_bits=bits))["err"])[1]
     assert V.vnmse(o["err"])[1] > per_chan
+
+
+# ---- attention-output error (the measure of the section 5 figures) -------
+
+def test_dense_attention_equals_paged_decode_over_the_reconstruction(orc, xb):
+    """One decode step over the dense full reconstruction is the main
+    oracle's paged decode attention over the same cache (identity page table,
+    every request attending to all tokens): two independent codes."""
+    H, T = 2, 512
+    xk = xb.reshape(1, H, T, 128)
+    xv = xb[::-1].copy().reshape(1, H, T, 128)
+    k, v = orc.quantize(xk), orc.quantize(xv)
+    q = S.WORKLOADS[2].queries_bf16(3, 4)
+    sm = 1 / np.sqrt(128)
+    table = np.tile(np.arange(T // 256, dtype=np.int32), (3, 1))
+    ctx = np.full(3, T, np.int32)
+    for full in (False, True):
+        want = orc.decode_attn(q, k, v, 0, table, ctx, sm, full)
+        Kd = V.encode(xk[0])["x_full" if full else "x_anchor"]
+        Vd = V.encode(xv[0])["x_full" if full else "x_anchor"]
+        got = V.dense_attn(q, Kd, Vd, sm)
+        assert np.allclose(got, want, rtol=1e-10, atol=1e-12)
+
+
+def test_dense_attention_brute_force_with_head_groups():
+    """Pure-Python softmax on a tiny case with 4 query heads over 2 KV heads
+    (query head h reads KV head h // 2)."""
+    import math
+    rng = np.random.default_rng(11)
+    H, T, B, Hq = 2, 5, 2, 4
+    k = rng.normal(size=(H, T, 128))
+    v = rng.normal(size=(H, T, 128))
+    q = S.f32_to_bf16_bits(rng.normal(size=(B, Hq, 128)).astype(np.float32))
+    qf = S.bf16_bits_to_f32(q).astype(np.float64)
+    sm = 0.3
+    got = V.dense_attn(q, k, v, sm)
+    for b in range(B):
+        for h in range(Hq):
+            g = h // 2
+            s = [sm * sum(float(qf[b, h, i]) * float(k[g, t, i]) for i in range(128)) for t in range(T)]
+            e = [math.exp(x) for x in s]
+            z = sum(e)
+            for i in range(0, 128, 17):
+                want = sum(e[t] * float(v[g, t, i]) for t in range(T)) / z
+                assert abs(got[b, h, i] - want) <= 1e-12 * (1 + abs(want))
+
+
+def test_dense_attention_special_cases():
+    rng = np.random.default_rng(12)
+    v = rng.normal(size=(1, 7, 128))
+    q = S.f32_to_bf16_bits(rng.normal(size=(2, 3, 128)).astype(np.float32))
+    # one token: the output is its value row
+    assert np.allclose(V.dense_attn(q, rng.normal(size=(1, 1, 128)), v[:, :1], 0.1), v[0, 0], rtol=0, atol=1e-15)
+    # equal scores: the output is the mean of the values
+    assert np.allclose(V.dense_attn(q, np.zeros((1, 7, 128)), v, 0.1), v[0].mean(axis=0), rtol=0, atol=1e-14)
+    # a dominant key: the output is that key's value row
+    k = np.zeros((1, 7, 128))
+    k[0, 4] = 1e3 * np.sign(S.bf16_bits_to_f32(q[0, 0]))
+    assert np.allclose(V.dense_attn(q[:1, :1], k, v, 1.0)[0, 0], v[0, 4], atol=1e-12)
+
+
+def test_attention_vnmse_closed_forms():
+    o = np.random.default_rng(13).normal(size=(3, 4, 128))
+    assert V.attn_vnmse(o, o) == 0.0
+    assert abs(V.attn_vnmse(1.1 * o, o) - 0.01) < 1e-12
+    assert abs(V.attn_vnmse(np.zeros_like(o), o) - 1.0) < 1e-15

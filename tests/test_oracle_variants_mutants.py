@@ -2,7 +2,8 @@
 
 Each case loads a copy of oracle/variants.py with one planted mistake (a
 wrong bias or level count, a shifted threshold, a wrong divisor or rounding,
-a dropped rule, a wrong centre or axis) and runs the pins of
+a dropped rule, a wrong centre or axis, a wrong attention head group,
+scale, normaliser or error ratio) and runs the pins of
 tests/test_oracle_variants.py against it: at least one pin must fail. Nothing
 here touches the real oracle or the GPU."""
 import importlib.util
@@ -33,6 +34,11 @@ MUTANTS = {
                                  "xa = _decode(mn, rng, mu_b, s_b, (A << v.residual_bits) + 1, v)"),
     "page minimum dropped": ("u = ((x - mn[:, None, :]) * inv[:, None, :]).astype(f32)",
                              "u = (x * inv[:, None, :]).astype(f32)"),
+    "attention head group": ("        g = h // G\n", "        g = h % H\n"),
+    "attention scale dropped": ("s = sm_scale * (q[:, h, :] @ K[g].T)", "s = (q[:, h, :] @ K[g].T)"),
+    "attention normaliser": ("/ p.sum(axis=1, keepdims=True)", "/ T"),
+    "attention vnmse denominator": ("return float((e * e).sum() / (o * o).sum())",
+                                    "return float((e * e).sum() / np.abs(o).sum())"),
 }
 
 
@@ -58,6 +64,10 @@ def _pins(orc, xb):
         lambda: P.test_chunk_statistics_against_fp64(xb, 16),
         lambda: P.test_uniform_comparator_half_step(xb, 4),
         lambda: P.test_six_bit_split_range(xb),
+        lambda: P.test_dense_attention_equals_paged_decode_over_the_reconstruction(orc, xb),
+        lambda: P.test_dense_attention_brute_force_with_head_groups(),
+        lambda: P.test_dense_attention_special_cases(),
+        lambda: P.test_attention_vnmse_closed_forms(),
     ]
 
 
