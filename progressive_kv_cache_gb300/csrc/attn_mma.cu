@@ -29,15 +29,20 @@
 // memory. The lookup table is replicated per lane (conflict-free) with entries
 // 256 bytes apart, so that one byte permute forms the whole address.
 //
-// Work: a CTA per (page range, KV head, request) of 12 warps. The pages' K
+// Work: a CTA per (page range, KV head, request) of 16 warps. The pages' K
 // and V planes and metadata arrive by bulk copy in a ring of slots (one
 // tensor's page per slot); the warp that releases the last chunk of a slot
-// refills it. Warp w takes chunks w, w + 12, ... of the range, each for all
+// refills it. Warp w takes chunks w, w + 16, ... of the range, each for all
 // query heads of the group: with up to 8 heads the MMA rows are the heads' hi
 // parts over their lo parts; with up to 16 the rows are the heads and hi and
 // lo go through two MMAs into the same accumulators. The chunks' running (max,
 // sum, output) are merged in shared memory into one partial per query head; a
 // second kernel merges the partials of the ranges.
+//
+// Tensor memory as a register file extension. A warp's running output (16
+// heads x 128 channels, 64 fp32 values a lane) lives in tensor memory between
+// chunks and comes into registers half at a time for the P.V update. This
+// keeps the warp under 128 registers, so 16 warps (four per scheduler) fit.
 #include <cuda_fp16.h>
 
 #include <mutex>
@@ -51,7 +56,8 @@ namespace {
 constexpr uint32_t kPlane = kPage * kD / 2;   // 16 KiB: one page of one plane
 constexpr int kRow = kD / 2;                  // code bytes per token
 constexpr int kPart = kD + 2;
-constexpr int kWarps = 12;                    // three per scheduler
+constexpr int kWarps = 16;                    // four per scheduler
+constexpr uint32_t kTmemCols = 256;           // per warp 64 columns of its lane quarter: the running output
 constexpr int kThreads = kWarps * 32;
 constexpr int kAff = kD + 16;                 // channel c stored at c + 4 (c / 32): no bank conflicts
 constexpr uint32_t kWaitLimit = 1u << 22;
@@ -83,6 +89,7 @@ struct Head {
     float qmax;
     int rel[NS];                              // releases of the slot's current item
     int last[NS];                             // last item issued into each slot (its tag)
+    uint32_t tmem;                            // tensor-memory base of the running outputs
     alignas(8) uint64_t full_bar[NS];
 };
 
@@ -97,10 +104,13 @@ struct Smem {
     uint8_t plane[NS][FULL ? 2 : 1][kPlane];  // per slot: anchor (and residual) codes
 };
 
+constexpr int kMrow = 4 * 34;                 // a merge row: four 32-channel blocks, each padded by 2
 struct Merge {                                // overlays the table and the planes after the page loop
     float m[kWarps][16];                      // per warp and query head
     float l[kWarps][16];
-    float o[kWarps][16][kD];
+    float o[kWarps][16][kMrow];               // channel d at 34 (d / 32) + d % 32: a warp's stores hit two banks each
+    float sc[16][kWarps];                     // per query head: each warp's weight 2^(m_w - M)
+    float M[16], L[16];                       // per query head: the range's max and sum
 };
 
 __device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
@@ -221,44 +231,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(AttnArgs a, Level
     const int G = a.G;
     const int64_t T = (int64_t)a.pool_pages * kPage;
 
-    // ---- per-CTA set-up ------------------------------------------------
-    for (int i = tid; i < 256 * 32; i += kThreads) {
-        const int e = i >> 5, l = i & 31;
-        uint32_t v;
-        if (FULL) {
-            v = (uint32_t)__half_as_ushort(__float2half_rn(lev.full[e]));
-        } else {
-            const __half2 h = __floats2half2_rn(lev.anchor[e & 15], lev.anchor[e >> 4]);
-            v = *reinterpret_cast<const uint32_t *>(&h);
-        }
-        sm.lut[e * 64 + (FULL ? 32 : 0) + l] = v;
-    }
-    const float qscale = a.sm_scale * kLog2e;
-    const int64_t qrow0 = (int64_t)b * a.Hq + (int64_t)kvh * G;
-    float lq = 0.0f;
-    for (int i = tid; i < 8 * 2 * 32 * 4; i += kThreads) {
-        // element c of qf[s][r][l]
-        const int c = i & 3, l = (i >> 2) & 31, r = (i >> 7) & 1, s = i >> 8;
-        const int row = (l >> 2) + 8 * r;
-        const int d = 32 * (l & 3) + 4 * s + c;
-        float v = 0.0f;
-        if (row < G && (G16 || r == 0))
-            v = __uint_as_float((uint32_t)a.q[(qrow0 + row) * kD + d] << 16) * qscale;
-        reinterpret_cast<float *>(&sm.h.qf[s][r][l])[c] = v;
-        lq = fmaxf(lq, fabsf(v));
-    }
-    if (tid == 0) {
-        sm.h.qmax = 0.0f;
-        for (int s = 0; s < NS; ++s) {
-            mbar_init(&sm.h.full_bar[s], 1);
-            sm.h.rel[s] = 0;
-            sm.h.last[s] = -1;
-        }
-        fence_mbar_init();
-    }
-    __syncthreads();
-    atomicMax(reinterpret_cast<int *>(&sm.h.qmax), __float_as_int(lq));   // non-negative floats order as ints
-
     int ctx = a.ctx[b];
     if (ctx < 0 || ctx > a.max_pages * kPage) {
         if (a.dev_err && split == 0 && kvh == 0 && tid == 0)
@@ -276,25 +248,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(AttnArgs a, Level
         const int p = a.page_table[(int64_t)b * a.max_pages + p_begin + i];
         return (p >= 0 && p < a.pool_pages) ? p : -1;
     };
-
-    // pages of the range past the context: scores -inf
-    if (a.scores) {
-        for (int lp = max(p_live, p_begin); lp < p_end; ++lp)
-            for (int i = tid; i < G * kPage; i += kThreads)
-                a.scores[(qrow0 + i / kPage) * score_stride + (int64_t)lp * kPage + i % kPage] = neg_inf();
-    }
-    __syncthreads();   // qmax complete
-
-    float m_run[R], l_run[R];                // per row: running max (base 2) and this lane's sum
-    float2 Olo[R][8], Ohi[R][8];             // per row: channels 32q + 2m, + 1 and 32q + 16 + 2m, + 1
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-        m_run[r] = neg_inf();
-        l_run[r] = 0.0f;
-#pragma unroll
-        for (int m = 0; m < 8; ++m)
-            Olo[r][m] = Ohi[r][m] = make_float2(0.0f, 0.0f);
-    }
 
     // ---- the ring: page i's K is item 2i, its V item 2i + 1; item x goes
     // to slot x % NS. Each of the 8 chunks of an item releases it once its
@@ -321,6 +274,78 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(AttnArgs a, Level
         bulk_g2s(mt.pm, (t ? a.vpm : a.kpm) + pmo, 2 * kD * 4, bar);
         bulk_g2s(mt.cm, (t ? a.vcm : a.kcm) + cmo, kNChunk * 2 * kD * 2, bar);
     };
+
+    // ---- per-CTA set-up ------------------------------------------------
+    if (tid == 0) {
+        sm.h.qmax = 0.0f;
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(&sm.h.full_bar[s], 1);
+            sm.h.rel[s] = 0;
+            sm.h.last[s] = -1;
+        }
+        fence_mbar_init();
+        for (int x = 0; x < NS && x < 2 * np; ++x)   // the first pages arrive while the tables are set up
+            issue(x);
+    }
+    for (int i = tid; i < 256 * 32; i += kThreads) {
+        const int e = i >> 5, l = i & 31;
+        uint32_t v;
+        if (FULL) {
+            v = (uint32_t)__half_as_ushort(__float2half_rn(lev.full[e]));
+        } else {
+            const __half2 h = __floats2half2_rn(lev.anchor[e & 15], lev.anchor[e >> 4]);
+            v = *reinterpret_cast<const uint32_t *>(&h);
+        }
+        sm.lut[e * 64 + (FULL ? 32 : 0) + l] = v;
+    }
+    const float qscale = a.sm_scale * kLog2e;
+    const int64_t qrow0 = (int64_t)b * a.Hq + (int64_t)kvh * G;
+    float lq = 0.0f;
+    for (int i = tid; i < 8 * 2 * 32 * 4; i += kThreads) {
+        // element c of qf[s][r][l]
+        const int c = i & 3, l = (i >> 2) & 31, r = (i >> 7) & 1, s = i >> 8;
+        const int row = (l >> 2) + 8 * r;
+        const int d = 32 * (l & 3) + 4 * s + c;
+        float v = 0.0f;
+        if (row < G && (G16 || r == 0))
+            v = __uint_as_float((uint32_t)a.q[(qrow0 + row) * kD + d] << 16) * qscale;
+        reinterpret_cast<float *>(&sm.h.qf[s][r][l])[c] = v;
+        lq = fmaxf(lq, fabsf(v));
+    }
+    if (warp == 0)
+        tmem_alloc(&sm.h.tmem, kTmemCols);
+    tcgen05_fence_before();
+    __syncthreads();
+    tcgen05_fence_after();
+    atomicMax(reinterpret_cast<int *>(&sm.h.qmax), __float_as_int(lq));   // non-negative floats order as ints
+    // this warp's running outputs: lane quarter warp % 4, columns 64 (warp / 4) ..
+    // + 63; column 16 r + 4 mm + 2 side + e of half hf (32 hf + ..) holds row g + 8 r,
+    // channel 32 q + 16 side + 2 (4 hf + mm) + e
+    const uint32_t tO = sm.h.tmem + ((uint32_t)(32 * (warp & 3)) << 16) + 64u * (uint32_t)(warp >> 2);
+
+    // pages of the range past the context: scores -inf
+    if (a.scores) {
+        for (int lp = max(p_live, p_begin); lp < p_end; ++lp)
+            for (int i = tid; i < G * kPage; i += kThreads)
+                a.scores[(qrow0 + i / kPage) * score_stride + (int64_t)lp * kPage + i % kPage] = neg_inf();
+    }
+    __syncthreads();   // qmax complete
+
+    float m_run[R], l_run[R];                // per row: running max (base 2) and this lane's sum
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        m_run[r] = neg_inf();
+        l_run[r] = 0.0f;
+    }
+    {
+        float z[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            z[i] = 0.0f;
+        tmem_st32f(tO, z);
+        tmem_st32f(tO + 32, z);
+    }
+
     // lane 0, after the warp's last read of item x's slot
     auto release = [&](int x) {
         const int s = x % NS;
@@ -350,9 +375,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(AttnArgs a, Level
         }
         return mbar_wait_bounded(&sm.h.full_bar[s], (uint32_t)((x / NS) & 1), kWaitLimit);
     };
-    if (tid == 0)
-        for (int x = 0; x < NS && x < 2 * np; ++x)
-            issue(x);
 
     // ---- warp w: chunks w, w + kWarps, ... of the range (chunk c = chunk
     // c % 8 of page c / 8) ------------------------------------------------
@@ -369,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(AttnArgs a, Level
         const int lp = p_begin + i;
         const bool valid = phys_of(i) >= 0;
         const int nv = min(max(ctx - lp * kPage - j * kChunk, 0), kChunk);   // valid tokens of chunk j
-        if (!wait_item(xk)) {
+        if (__any_sync(0xFFFFFFFFu, !wait_item(xk))) {   // warp-uniform: the whole warp leaves together
             timed_out = true;
             break;
         }
@@ -383,7 +405,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(AttnArgs a, Level
             __syncwarp();
             if (lane == 0)
                 release(xk);
-            if (!wait_item(xk + 1)) {
+            if (__any_sync(0xFFFFFFFFu, !wait_item(xk + 1))) {
                 timed_out = true;
                 break;
             }
@@ -497,7 +519,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(AttnArgs a, Level
         // (weights up to 2^8 are exact in fp32 and fine in fp16), so the
         // running output is rarely rescaled.
         float P[R][4][2];                    // row r, n-tile nt: tokens 8 nt + 2q, + 1
-        float mref[R], mx[R], psum[R];
+        float mref[R], mx[R], psum[R], oscale[R];
         bool up = false;
 #pragma unroll
         for (int r = 0; r < R; ++r) {
@@ -541,7 +563,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(AttnArgs a, Level
                         make_float2((P[r][nt][0] + mref[r]) * kLn2, (P[r][nt][1] + mref[r]) * kLn2);
             }
         }
-        if (__any_sync(0xFFFFFFFFu, up)) {   // rare: move the reference to this chunk's maximum
+        const bool rescale = __any_sync(0xFFFFFFFFu, up);
+        if (rescale) {                       // rare: move the reference to this chunk's maximum
 #pragma unroll
             for (int r = 0; r < R; ++r) {
                 const bool first = m_run[r] == neg_inf();
@@ -550,16 +573,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(AttnArgs a, Level
                 const float alpha = first ? 0.0f : exp2_sm(-shift);
                 m_run[r] = mref[r] + shift;
                 l_run[r] *= alpha;
+                oscale[r] = alpha;           // applied to the outputs as they are loaded below
 #pragma unroll
                 for (int nt = 0; nt < 4; ++nt) {
                     P[r][nt][0] -= shift;
                     P[r][nt][1] -= shift;
-                }
-                const float2 al = make_float2(alpha, alpha);
-#pragma unroll
-                for (int m = 0; m < 8; ++m) {
-                    Olo[r][m] = __fmul2_rn(Olo[r][m], al);
-                    Ohi[r][m] = __fmul2_rn(Ohi[r][m], al);
                 }
             }
         }
@@ -596,7 +614,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(AttnArgs a, Level
         }
 
         // ---- V: affines and codes of chunk j, then release the slot -------
-        if (!wait_item(xk + 1)) {
+        if (__any_sync(0xFFFFFFFFu, !wait_item(xk + 1))) {
             timed_out = true;
             break;
         }
@@ -627,7 +645,21 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(AttnArgs a, Level
         // ---- P.V: n-tile 2m + e holds channel 16 n + 2m + e of column n ------
         float4 vb4l, vb4h, va4l, va4h;       // affines of this lane's channels for m, m + 1
 #pragma unroll
-        for (int m = 0; m < 8; ++m) {
+        for (int hf = 0; hf < 2; ++hf) {     // the running outputs of m = 4 hf .. 4 hf + 3, from tensor memory
+        float o[32];
+        tmem_wait_st32();
+        tmem_ld32f(tO + 32 * hf, o);
+        tmem_wait_ld32();
+        if (rescale) {
+#pragma unroll
+            for (int r = 0; r < R; ++r)
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    o[16 * r + i] *= oscale[r];
+        }
+#pragma unroll
+        for (int mm = 0; mm < 4; ++mm) {
+            const int m = 4 * hf + mm;
             const int wi = m >> 2;
             float C[2][4];
 #pragma unroll
@@ -711,9 +743,16 @@ case I:                                                                         
                     ch = make_float2(C[0][1] + C[0][3], C[1][1] + C[1][3]);
                 }
                 const float2 ps2 = make_float2(psum[r], psum[r]);
-                Olo[r][m] = __ffma2_rn(bl, cl, __ffma2_rn(al, ps2, Olo[r][m]));
-                Ohi[r][m] = __ffma2_rn(bh, ch, __ffma2_rn(ah, ps2, Ohi[r][m]));
+                float *ol = o + 16 * r + 4 * mm;
+                const float2 nl = __ffma2_rn(bl, cl, __ffma2_rn(al, ps2, make_float2(ol[0], ol[1])));
+                const float2 nh = __ffma2_rn(bh, ch, __ffma2_rn(ah, ps2, make_float2(ol[2], ol[3])));
+                ol[0] = nl.x;
+                ol[1] = nl.y;
+                ol[2] = nh.x;
+                ol[3] = nh.y;
             }
+        }
+        tmem_st32f(tO + 32 * hf, o);
         }
     }
     if (timed_out && a.dev_err && lane == 0)
@@ -749,34 +788,61 @@ case I:                                                                         
                 mg.m[j][h] = m_run[r];
                 mg.l[j][h] = l;
             }
+        }
+        tmem_wait_st32();
 #pragma unroll
-            for (int m = 0; m < 8; ++m) {
-                *reinterpret_cast<float2 *>(&mg.o[j][h][32 * q + 2 * m]) = Olo[r][m];
-                *reinterpret_cast<float2 *>(&mg.o[j][h][32 * q + 16 + 2 * m]) = Ohi[r][m];
-            }
+        for (int hf = 0; hf < 2; ++hf) {
+            float o[32];
+            tmem_ld32f(tO + 32 * hf, o);
+            tmem_wait_ld32();
+#pragma unroll
+            for (int r = 0; r < R; ++r)
+#pragma unroll
+                for (int mm = 0; mm < 4; ++mm) {
+                    const int h = g + 8 * r, m = 4 * hf + mm;
+                    const float *ol = o + 16 * r + 4 * mm;
+                    *reinterpret_cast<float2 *>(&mg.o[j][h][34 * q + 2 * m]) = make_float2(ol[0], ol[1]);
+                    *reinterpret_cast<float2 *>(&mg.o[j][h][34 * q + 16 + 2 * m]) = make_float2(ol[2], ol[3]);
+                }
+        }
+    }
+    tcgen05_fence_before();
+    __syncthreads();
+    if (warp == 0) {                         // every warp's tensor-memory reads are done
+        tcgen05_fence_after();
+        tmem_dealloc(sm.h.tmem, kTmemCols);
+    }
+    static_assert(kWarps == 16, "one 16-lane group per query head below");
+    if (tid < 16 * kWarps) {                 // lane group h: warp w's weight for query head h
+        const int h = tid >> 4, w = tid & 15;
+        const float mw = mg.m[w][h];
+        float M = mw;
+#pragma unroll
+        for (int o = 8; o >= 1; o >>= 1)
+            M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, o));
+        const float sc = M > neg_inf() ? exp2f(mw - M) : 0.0f;
+        float L = mg.l[w][h] * sc;
+#pragma unroll
+        for (int o = 8; o >= 1; o >>= 1)
+            L += __shfl_xor_sync(0xFFFFFFFFu, L, o);
+        mg.sc[h][w] = sc;
+        if (w == 0) {
+            mg.M[h] = M;
+            mg.L[h] = L;
         }
     }
     __syncthreads();
     for (int e = tid; e < G * kD; e += kThreads) {
         const int h = e / kD, d = e % kD;
-        float M = neg_inf();
+        float o = 0.0f;
 #pragma unroll
         for (int w = 0; w < kWarps; ++w)
-            M = fmaxf(M, mg.m[w][h]);
-        float L = 0.0f, o = 0.0f;
-        if (M > neg_inf()) {
-#pragma unroll
-            for (int w = 0; w < kWarps; ++w) {
-                const float sc = exp2f(mg.m[w][h] - M);
-                L = fmaf(mg.l[w][h], sc, L);
-                o = fmaf(mg.o[w][h][d], sc, o);
-            }
-        }
+            o = fmaf(mg.o[w][h][34 * (d >> 5) + (d & 31)], mg.sc[h][w], o);
         float *pp = a.part + ((qrow0 + h) * a.n_splits + split) * kPart;
         pp[d] = o;
         if (d == 0) {
-            pp[kD] = M;
-            pp[kD + 1] = L;
+            pp[kD] = mg.M[h];
+            pp[kD + 1] = mg.L[h];
         }
     }
 }
