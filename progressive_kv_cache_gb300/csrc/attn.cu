@@ -249,61 +249,51 @@ __global__ void __launch_bounds__(kThreads, 1) attn_split_kernel(AttnArgs a, Lev
 }
 
 // Log-sum-exp merge of the page ranges' partials (base-2 log domain): one block
-// per (request, query head), 128 threads. The maxima and the weights of all
-// partials are reduced once in parallel and kept in shared memory, so the
-// weighted sum over partials is a run of independent loads per channel.
+// per (request, query head), thread d owns channel d. One online pass over the
+// partials, 16 at a time: their loads are all issued before any is used, so a
+// merge of n ranges waits on about n / 16 rounds of memory latency.
 __global__ void __launch_bounds__(kD) attn_combine_kernel(const float *__restrict__ part, int n_splits,
                                                           float *__restrict__ out)
 {
-    extern __shared__ float wgt[];   // [n_splits]
-    __shared__ float red[kD / 32];
+    constexpr int U = 16;
     // launched as a programmatic dependent of the split kernel: everything
     // above this point overlaps its tail; the partials are read only after it
     // has completed and its writes are visible
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int64_t bh = blockIdx.x;
-    const int d = threadIdx.x, lane = d & 31, warp = d >> 5;
+    const int d = threadIdx.x;
     const float *pp = part + bh * n_splits * kPart;
     const float ninf = -__int_as_float(0x7F800000);
 
-    float mx = ninf;
-    for (int s = d; s < n_splits; s += kD)
-        if (pp[s * kPart + kD + 1] > 0.0f)
-            mx = fmaxf(mx, pp[s * kPart + kD]);
+    float M = ninf, L = 0.0f, o = 0.0f;
+    for (int s0 = 0; s0 < n_splits; s0 += U) {
+        float mv[U], lv[U], ov[U];
 #pragma unroll
-    for (int o = 16; o >= 1; o >>= 1)
-        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
-    if (lane == 0)
-        red[warp] = mx;
-    __syncthreads();
-    const float M = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
-    __syncthreads();
-
-    float lsum = 0.0f;
-    for (int s = d; s < n_splits; s += kD) {
-        const float l = pp[s * kPart + kD + 1];
-        const float w = (l > 0.0f && M > ninf) ? exp2f(pp[s * kPart + kD] - M) : 0.0f;
-        wgt[s] = w;
-        lsum = fmaf(l, w, lsum);
+        for (int u = 0; u < U; ++u) {
+            const bool in = s0 + u < n_splits;
+            const float *r = pp + (int64_t)(s0 + u) * kPart;
+            mv[u] = in ? r[kD] : ninf;
+            lv[u] = in ? r[kD + 1] : 0.0f;
+            ov[u] = in ? r[d] : 0.0f;
+        }
+        float Mb = M;
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            if (lv[u] > 0.0f)
+                Mb = fmaxf(Mb, mv[u]);
+        if (Mb > ninf) {
+            const float c = M > ninf ? exp2f(M - Mb) : 0.0f;   // earlier ranges, to the new maximum
+            L *= c;
+            o *= c;
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const float w = lv[u] > 0.0f ? exp2f(mv[u] - Mb) : 0.0f;
+                L = fmaf(lv[u], w, L);
+                o = fmaf(ov[u], w, o);
+            }
+            M = Mb;
+        }
     }
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1)
-        lsum += __shfl_xor_sync(0xFFFFFFFFu, lsum, o);
-    if (lane == 0)
-        red[warp] = lsum;
-    __syncthreads();
-    const float L = (red[0] + red[1]) + (red[2] + red[3]);
-
-    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-    int s = 0;
-    for (; s + 4 <= n_splits; s += 4) {
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-            acc[u] = fmaf(pp[(s + u) * kPart + d], wgt[s + u], acc[u]);
-    }
-    for (; s < n_splits; ++s)
-        acc[0] = fmaf(pp[s * kPart + d], wgt[s], acc[0]);
-    const float o = (acc[0] + acc[1]) + (acc[2] + acc[3]);
     out[bh * kD + d] = L > 0.0f ? o / L : 0.0f;
 }
 
@@ -338,7 +328,7 @@ void attn_split_plan(int batch, int kv_heads, int max_pages, int sms, int *n_spl
     }
     if (pps < 1)
         pps = 1;
-    if (max_pages / pps > 8192)   // the combine keeps one weight per range in shared memory
+    if (max_pages / pps > 8192)   // at most 8192 ranges (bounds the workspace and the combine)
         pps = (max_pages + 8191) / 8192;
     if (pps > max_pages)
         pps = max_pages > 0 ? max_pages : 1;
@@ -372,7 +362,7 @@ cudaError_t launch_attn_combine(const AttnArgs &a, cudaStream_t s)
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(a.B * a.Hq));
     cfg.blockDim = dim3(kD);
-    cfg.dynamicSmemBytes = (size_t)a.n_splits * sizeof(float);
+    cfg.dynamicSmemBytes = 0;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
