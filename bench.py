@@ -519,6 +519,102 @@ def append_report(args):
     print(json.dumps(line))
 
 
+def batched_report(args):
+    """Batched decode attention at the batched-decode workload: 32 requests
+    with seeded context lengths in [4K, 16K] (ragged last pages) on a seeded
+    random page table, 8 KV heads, 64 query heads (GQA group 8), one layer.
+    One call is one decode step of every request. Algorithmic bytes count the
+    tokens each request attends to: 168 B (anchor) or 296 B (full) per (token,
+    KV head). The oracle runs beside it on a sample of two requests."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    import progressive_kv_cache_gb300 as lx
+
+    w = S.WORKLOADS[4]
+    H, B, Hq = w.H, w.B, w.Hq
+    ctx_np, pool, table_np = S.batched_layout(w)
+    T = pool * 256
+    dev = torch.device("cuda")
+    gen = S.DeviceGenerator()
+    qkv = {}
+    x = torch.empty((1, H, T, D), dtype=torch.bfloat16, device=dev)
+    for s_ in (S.S_K, S.S_V):
+        gen.fill(x, w.key(s_), w.scales(s_))
+        qkv[s_] = lx.QuantizedKV.empty(1, H, T, dev)
+        lx.quantize_pages(x, qkv[s_])
+    del x
+    qb = w.queries_bf16()
+    qt = torch.from_numpy(qb.view(np.int16)).to(dev).view(torch.bfloat16)
+    table = torch.from_numpy(table_np).to(dev)
+    ctx = torch.from_numpy(ctx_np.astype(np.int32)).to(dev)
+    max_pages = table_np.shape[1]
+    ws = torch.empty(lx.decode_attn_workspace(B, Hq, max_pages), dtype=torch.uint8, device=dev)
+    out = torch.empty((B, Hq, D), dtype=torch.float32, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    sm = D ** -0.5
+    token_heads = int(ctx_np.sum()) * H
+    hbm, peak_kind = peaks()
+    modes = {}
+    for mode, name, per in ((lx.MODE_ANCHOR, "anchor", B_ATTN_ANCHOR), (lx.MODE_FULL, "full", B_ATTN_FULL)):
+        def call():
+            lx.decode_attn(qt, qkv[S.S_K], qkv[S.S_V], 0, table, ctx, sm, mode, out=out, workspace=ws,
+                           dev_err=err)
+        for _ in range(max(args.warmup, 3)):
+            call()
+        torch.cuda.synchronize()
+        reps = max(args.steps, 200)          # long enough for the clock sampler
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with ClockSampler(0) as clk:
+            e0.record()
+            for _ in range(reps):
+                call()
+            e1.record()
+            torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / reps
+        gbs = token_heads * per / (ms * 1e-3) / 1e9
+        modes[name] = {"ms": ms, "GB/s": gbs, "frac_of_measured_hbm": gbs / hbm,
+                       "request_steps_per_s": B / (ms * 1e-3), "kv_token_heads_per_s": token_heads / (ms * 1e-3),
+                       "clocks": clk.summary()}
+    if int(err.item()) != 0:
+        raise RuntimeError("lynx_decode_attn flagged the page table or a context length")
+    cpu = None
+    if not args.no_cpu_baseline:
+        import oracle as orc
+        orc.build()
+        n_s, ctx_s = 2, 2048
+        sc_k = S.channel_scales(w.seed, S.S_K, 1, 1, n_outliers=w.n_outliers, factor_log10=w.factor_log10)
+        sc_v = S.channel_scales(w.seed, S.S_V, 1, 1, n_outliers=w.n_outliers, factor_log10=w.factor_log10)
+        ks = orc.quantize(S.laplace_bf16(w.key(S.S_K), sc_k, 1, 1, ctx_s))
+        vs = orc.quantize(S.laplace_bf16(w.key(S.S_V), sc_v, 1, 1, ctx_s))
+        tb = np.tile(np.arange(ctx_s // 256, dtype=np.int32), (n_s, 1))
+        cl = np.full(n_s, ctx_s, np.int32)
+        qs = qb[:n_s, :Hq // H]
+        t0 = time.perf_counter()
+        reps = 0
+        while time.perf_counter() - t0 < 10.0:
+            orc.decode_attn(qs, ks, vs, 0, tb, cl, sm, False)
+            reps += 1
+        dt = time.perf_counter() - t0
+        cpu = {"value": reps * n_s * ctx_s * B_ATTN_ANCHOR / dt / 1e9, "unit": "GB/s", "cores": orc.num_threads(),
+               "kind": "oracle", "sample": f"anchor mode, 1 KV head x 8 query heads, {n_s} requests x {ctx_s} "
+                                           f"tokens, {reps} calls, {dt:.1f} s"}
+    a = modes["anchor"]
+    line = {"report": "batched", "metric": "batched decode attention: GB/s and decode steps/s vs HBM roofline (1 GB300)",
+            "value": a["GB/s"], "unit": "GB/s", "n_gpus": 1, "steps": max(args.steps, 200),
+            "warmup": max(args.warmup, 3), "ms_per_step": a["ms"], "higher_is_better": True,
+            "dtype": "4+4-bit planes, fp32 accumulation", "data": "synthetic",
+            "config": {"workload": f"{w.name}: {B} requests, contexts {int(ctx_np.min())}..{int(ctx_np.max())} "
+                                   f"tokens, {H} KV heads, {Hq} query heads, one layer",
+                       "token_heads_per_call": token_heads, "page_pool": pool, "max_pages": max_pages,
+                       "l2": f"{token_heads * B_ATTN_ANCHOR / 1e6:.0f} MB read per anchor call, larger than L2"},
+            "roofline": {"bound": "hbm", "kernel": "decode_attn_anchor", "achieved": a["GB/s"], "peak": hbm,
+                         "unit": "GB/s", "frac": a["GB/s"] / hbm, "peak_kind": peak_kind, "traffic": None},
+            "modes": modes, "cpu_baseline": cpu, "gpu_launches": 2 * 2 * max(args.steps, 200),
+            "clocks": a["clocks"]}
+    print(json.dumps(line))
+
+
 def split_stream_report(args):
     """Split-stream arrival (Lynx section 4) emulated on one GPU at the
     progressive-arrival workload's shape (8 layers x 8 KV heads x 64K tokens, 8
@@ -941,12 +1037,14 @@ def main():
                                        "decode_attn_full"], default=None,
                     help="time one kernel group only (for profiler captures on smaller cases)")
     ap.add_argument("--layers", type=int, default=None, help="layers of the cache (default: all 94)")
-    ap.add_argument("--report", choices=["progressive", "append", "split-stream", "verify", "ablation"], default=None,
+    ap.add_argument("--report", choices=["progressive", "append", "split-stream", "verify", "ablation", "batched"],
+                    default=None,
                     help="progressive: residual layers arriving one by one (8 layers, 64K tokens); "
                          "append: quantize-on-append of 32 requests' tail pages over 94 layers x 8 KV heads; "
                          "split-stream: anchors then residuals over an emulated link, decode on anchors first; "
                          "verify: multi-token verify attention (64 draft positions, 32K context); "
-                         "ablation: quantizer variants and uniform comparators, vNMSE and encoder GB/s")
+                         "ablation: quantizer variants and uniform comparators, vNMSE and encoder GB/s; "
+                         "batched: decode attention of 32 ragged requests, 8 KV heads, GQA group 8")
     ap.add_argument("--no-graph", action="store_true",
                     help="issue every library call from Python instead of replaying CUDA graphs of them")
     args = ap.parse_args()
@@ -968,6 +1066,8 @@ def main():
         verify_report(args)
     elif args.report == "ablation":
         ablation_report(args)
+    elif args.report == "batched":
+        batched_report(args)
     else:
         run_gpu(args)
 
