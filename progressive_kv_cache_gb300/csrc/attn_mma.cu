@@ -90,6 +90,8 @@ struct Head {
     int rel[NS];                              // releases of the slot's current item
     int last[NS];                             // last item issued into each slot (its tag)
     uint32_t tmem;                            // tensor-memory base of the running outputs
+    alignas(16) uint16_t qstage[16 * kD];     // the group's query rows as they arrive (bf16)
+    alignas(8) uint64_t q_bar;
     alignas(8) uint64_t full_bar[NS];
 };
 
@@ -276,7 +278,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(AttnArgs a, Level
     };
 
     // ---- per-CTA set-up ------------------------------------------------
+    const int64_t qrow0 = (int64_t)b * a.Hq + (int64_t)kvh * G;
     if (tid == 0) {
+        // the group's G query rows are contiguous: one copy, landing while the
+        // tables are set up
+        mbar_init(&sm.h.q_bar, 1);
+        fence_mbar_init();
+        mbar_arrive_expect_tx(&sm.h.q_bar, (uint32_t)G * kD * 2);
+        bulk_g2s(sm.h.qstage, a.q + qrow0 * kD, (uint32_t)G * kD * 2, &sm.h.q_bar);
         sm.h.qmax = 0.0f;
         for (int s = 0; s < NS; ++s) {
             mbar_init(&sm.h.full_bar[s], 1);
@@ -299,8 +308,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(AttnArgs a, Level
         sm.lut[e * 64 + (FULL ? 32 : 0) + l] = v;
     }
     const float qscale = a.sm_scale * kLog2e;
-    const int64_t qrow0 = (int64_t)b * a.Hq + (int64_t)kvh * G;
     float lq = 0.0f;
+    __syncthreads();                         // the query barrier is initialised
+    const bool q_ok = mbar_wait_bounded(&sm.h.q_bar, 0u, kWaitLimit);
+    if (!q_ok && a.dev_err)
+        atomicOr(a.dev_err, LYNX_DEVERR_TIMEOUT);
     for (int i = tid; i < 8 * 2 * 32 * 4; i += kThreads) {
         // element c of qf[s][r][l]
         const int c = i & 3, l = (i >> 2) & 31, r = (i >> 7) & 1, s = i >> 8;
@@ -308,7 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(AttnArgs a, Level
         const int d = 32 * (l & 3) + 4 * s + c;
         float v = 0.0f;
         if (row < G && (G16 || r == 0))
-            v = __uint_as_float((uint32_t)a.q[(qrow0 + row) * kD + d] << 16) * qscale;
+            v = __uint_as_float((uint32_t)sm.h.qstage[row * kD + d] << 16) * qscale;
         reinterpret_cast<float *>(&sm.h.qf[s][r][l])[c] = v;
         lq = fmaxf(lq, fabsf(v));
     }
@@ -761,7 +773,7 @@ case I:                                                                         
     if (tid == 0) {
         // every copy issued must land before the merge reuses the slots
         // (after a timeout some may still be in flight; bounded)
-        bool ok = true;
+        bool ok = mbar_wait_bounded(&sm.h.q_bar, 0u, kWaitLimit);
         for (int s = 0; s < NS; ++s)
             if (sm.h.last[s] >= 0 && !mbar_wait_bounded(&sm.h.full_bar[s], (uint32_t)((sm.h.last[s] / NS) & 1), kWaitLimit))
                 ok = false;
