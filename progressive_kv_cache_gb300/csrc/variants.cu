@@ -113,7 +113,9 @@ __device__ __forceinline__ void block_err(SmemV &sm, float e0, float e1, float e
     }
 }
 
-template <int C>
+// RECON: the launch writes a reconstruction (the stores cost the errors-only
+// study about 9 %, so that path is compiled without them)
+template <int C, bool RECON>
 __global__ void __launch_bounds__(kThreadsV) variant_kernel(const __grid_constant__ VariantArgs a)
 {
     extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -209,9 +211,9 @@ __global__ void __launch_bounds__(kThreadsV) variant_kernel(const __grid_constan
             const float la = ca > 0 ? sm.lv[ka] : (ca < 0 ? -sm.lv[ka] : 0.0f);
             const float x = bf16f(__ldg(xp + t * kD + d));
             const float xf = __fmaf_rn(bm, lf, am), xa = __fmaf_rn(bm, la, am);
-            if (a.x_full)
+            if (RECON && a.x_full)
                 a.x_full[o] = xf;
-            if (a.x_anchor)
+            if (RECON && a.x_anchor)
                 a.x_anchor[o] = xa;
             const float ef = __fsub_rn(xf, x), ea = __fsub_rn(xa, x);
             e0 = __fmaf_rn(x, x, e0);
@@ -224,6 +226,7 @@ __global__ void __launch_bounds__(kThreadsV) variant_kernel(const __grid_constan
 
 // The uniform INTb comparator: per (page, channel) min-max grid of 2^b levels,
 // code = floor((x - mn) * ((2^b - 1) / rng) + 1/2), every step in fp32.
+template <bool RECON>
 __global__ void __launch_bounds__(kThreadsV) uniform_kernel(const __grid_constant__ VariantArgs a)
 {
     extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -268,9 +271,9 @@ __global__ void __launch_bounds__(kThreadsV) uniform_kernel(const __grid_constan
             if (a.codes)
                 a.codes[(page * kPage + t) * kD + dd] = (int16_t)q;
             const float xr = __fmaf_rn(q, step, tmn);
-            if (a.x_full)
+            if (RECON && a.x_full)
                 a.x_full[(page * kPage + t) * kD + dd] = xr;
-            if (a.x_anchor)
+            if (RECON && a.x_anchor)
                 a.x_anchor[(page * kPage + t) * kD + dd] = xr;
             const float e = __fsub_rn(xr, x);
             e0 = __fmaf_rn(x, x, e0);
@@ -288,15 +291,32 @@ __global__ void __launch_bounds__(kThreadsV) uniform_kernel(const __grid_constan
         if (a.codes)
             a.codes[(page * kPage + t) * kD + d] = (int16_t)q;
         const float xr = __fmaf_rn(q, step, mn);
-        if (a.x_full)
+        if (RECON && a.x_full)
             a.x_full[(page * kPage + t) * kD + d] = xr;
-        if (a.x_anchor)
+        if (RECON && a.x_anchor)
             a.x_anchor[(page * kPage + t) * kD + d] = xr;
         const float e = __fsub_rn(xr, x);
         e0 = __fmaf_rn(x, x, e0);
         e1 = __fmaf_rn(e, e, e1);
     }
     block_err(sm, e0, e1, e1, a.err ? a.err + page * 3 : nullptr);
+}
+
+template <typename K>
+cudaError_t launch_one(K kernel, const VariantArgs &a, dim3 grid, size_t smem, cudaStream_t s)
+{
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess)
+        return e;
+    kernel<<<grid, kThreadsV, smem, s>>>(a);
+    return cudaGetLastError();
+}
+
+template <int C>
+cudaError_t launch_variant(const VariantArgs &a, dim3 grid, size_t smem, cudaStream_t s, bool recon)
+{
+    return recon ? launch_one(variant_kernel<C, true>, a, grid, smem, s)
+                 : launch_one(variant_kernel<C, false>, a, grid, smem, s);
 }
 
 } // namespace
@@ -321,13 +341,10 @@ cudaError_t launch_quantize_variant(const uint16_t *x, int64_t pages, const lynx
     a.ubits = v.uniform_bits;
     const size_t smem = sizeof(SmemV);
     const dim3 grid((unsigned)pages);
-    if (v.uniform_bits > 0) {
-        cudaError_t e = cudaFuncSetAttribute(uniform_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess)
-            return e;
-        uniform_kernel<<<grid, kThreadsV, smem, s>>>(a);
-        return cudaGetLastError();
-    }
+    const bool recon = x_anchor || x_full;
+    if (v.uniform_bits > 0)
+        return recon ? launch_one(uniform_kernel<true>, a, grid, smem, s)
+                     : launch_one(uniform_kernel<false>, a, grid, smem, s);
     // Tables from the written map, in fp64 (thresholds where the map crosses
     // k - 1/2, levels at k), rounded to fp32 and fp16.
     const int qm = (1 << (v.anchor_bits + v.residual_bits - 2)) - 1;
@@ -342,25 +359,14 @@ cudaError_t launch_quantize_variant(const uint16_t *x, int64_t pages, const lynx
     for (int k = 0; k <= qm + 1; ++k)
         a.lv[k] = __half2float(__double2half(al > 0.0 ? (std::pow(1.0 + al, (double)k / qm) - 1.0) / al
                                                       : (double)k / qm));
-    cudaError_t e;
     switch (v.chunk) {
     case 16:
-        if ((e = cudaFuncSetAttribute(variant_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)))
-            return e;
-        variant_kernel<16><<<grid, kThreadsV, smem, s>>>(a);
-        break;
+        return launch_variant<16>(a, grid, smem, s, recon);
     case 32:
-        if ((e = cudaFuncSetAttribute(variant_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)))
-            return e;
-        variant_kernel<32><<<grid, kThreadsV, smem, s>>>(a);
-        break;
+        return launch_variant<32>(a, grid, smem, s, recon);
     default:
-        if ((e = cudaFuncSetAttribute(variant_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)))
-            return e;
-        variant_kernel<64><<<grid, kThreadsV, smem, s>>>(a);
-        break;
+        return launch_variant<64>(a, grid, smem, s, recon);
     }
-    return cudaGetLastError();
 }
 
 } // namespace lynx
