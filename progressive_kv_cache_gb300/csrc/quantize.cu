@@ -101,12 +101,16 @@ __device__ __forceinline__ uint2 lds_u2(uint32_t addr)
 // (c + 7) & 0xFF (bits 8-31 zero), whose high nibble is the anchor and low
 // nibble the residual.
 // `tab_base` is the shared address of this lane's table replica, offset so
-// that the bucket number indexes it directly.
-__device__ __forceinline__ uint32_t code_byte(float w, uint32_t tab_base)
+// that the bucket number indexes it directly; `stride` is the byte distance
+// between buckets (kCopies * 8). It arrives as a kernel argument so that the
+// address is one integer multiply-add, which runs on the FMA pipe: with the
+// constant in view the compiler forms it with a shift-and-add on the ALU pipe,
+// the pipe this kernel saturates (5-6 % slower).
+__device__ __forceinline__ uint32_t code_byte(float w, uint32_t tab_base, uint32_t stride)
 {
     const float a = fabsf(w);
     const uint32_t bucket = __float_as_uint(__fadd_rn(a, __uint_as_float(kBucketOffsetBits))) >> 19;
-    const uint2 e = lds_u2(bucket * (kCopies * 8) + tab_base);
+    const uint2 e = lds_u2(bucket * stride + tab_base);
     // |w| >= T* exactly when pred(T*) - |w| < 0 (its sign bit); 2 * sign(w)
     // is bits 31-30 of w (bit 30 is 0 for |w| < 2); 0x4440 makes the permute
     // fill bytes 1-3 of the result with zeros
@@ -143,8 +147,8 @@ __device__ __forceinline__ float2 bf2_to_f2(uint32_t x)
 // metadata (mean, scale) of both channels as fp16x2 words.
 template <bool FULL>
 __device__ __forceinline__ void encode_chunk(const float2 (&u)[kChunk], int nc, float2 ulo, float2 uhi,
-                                             uint32_t tab_base, uint8_t *anc_row0, uint8_t *res_row0,
-                                             uint32_t &mu2, uint32_t &s2)
+                                             uint32_t tab_base, uint32_t stride, uint8_t *anc_row0,
+                                             uint8_t *res_row0, uint32_t &mu2, uint32_t &s2)
 {
     // chunk mean: stride-halving pairwise tree over 32 slots, absent slots +0
     const float2 zero = make_float2(0.0f, 0.0f);
@@ -191,8 +195,8 @@ __device__ __forceinline__ void encode_chunk(const float2 (&u)[kChunk], int nc, 
                 // w = v * inv_s, as one rounding of the product plus +0, which
                 // turns a -0 product into +0 (both code 0) and changes nothing else
                 const float2 w = __ffma2_rn(__fadd2_rn(u[i], negmu), inv_s, zero);
-                const uint32_t b0 = code_byte(w.x, tab_base);
-                const uint32_t b1 = code_byte(w.y, tab_base);
+                const uint32_t b0 = code_byte(w.x, tab_base, stride);
+                const uint32_t b1 = code_byte(w.y, tab_base, stride);
                 ab[k] = (b0 >> 4) | (b1 & 0xF0u);
                 rb[k] = (b0 & 0x0Fu) | ((b1 << 4) & 0xF0u);
             }
@@ -207,7 +211,8 @@ __device__ __forceinline__ void encode_chunk(const float2 (&u)[kChunk], int nc, 
     s2 = (uint32_t)__half_as_ushort(sh0) | ((uint32_t)__half_as_ushort(sh1) << 16);
 }
 
-__global__ void __launch_bounds__(kThreads, 1) quantize_kernel(Params p, CodeTable table)
+// tab_stride: kCopies * 8, passed at run time (see code_byte)
+__global__ void __launch_bounds__(kThreads, 1) quantize_kernel(Params p, CodeTable table, uint32_t tab_stride)
 {
     extern __shared__ __align__(128) unsigned char smem_raw[];
     Smem &sm = *reinterpret_cast<Smem *>(smem_raw);
@@ -336,9 +341,9 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_kernel(Params p, CodeTab
         uint8_t *res_row0 = sm.res + j * kChunk * (kD / 2) + pi;
         uint32_t mu2 = 0, s2 = 0;
         if (nc == kChunk) {
-            encode_chunk<true>(u, nc, ulo, uhi, tab_base, anc_row0, res_row0, mu2, s2);
+            encode_chunk<true>(u, nc, ulo, uhi, tab_base, tab_stride, anc_row0, res_row0, mu2, s2);
         } else if (nc > 0) {
-            encode_chunk<false>(u, nc, ulo, uhi, tab_base, anc_row0, res_row0, mu2, s2);
+            encode_chunk<false>(u, nc, ulo, uhi, tab_base, tab_stride, anc_row0, res_row0, mu2, s2);
         } else {
 #pragma unroll
             for (int i = 0; i < kChunk; ++i) {
@@ -385,7 +390,7 @@ __global__ void level_codes_kernel(const float *__restrict__ w, int64_t n, int8_
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
         const float v = w[i];
         const float c = v == v ? __fadd_rn(copysignf(fminf(fabsf(v), 1.99999988f), v), 0.0f) : 0.0f;
-        codes[i] = (int8_t)((int)(int8_t)code_byte(c, tab_base) - kBias);
+        codes[i] = (int8_t)((int)(int8_t)code_byte(c, tab_base, kCopies * 8) - kBias);
     }
 }
 
@@ -401,7 +406,7 @@ cudaError_t run_quantize(const Params &p, cudaStream_t s)
     if (e != cudaSuccess)
         return e;
     const int64_t grid = p.pages < sms ? p.pages : sms;
-    quantize_kernel<<<(unsigned)grid, kThreads, smem, s>>>(p, host_tables().code);
+    quantize_kernel<<<(unsigned)grid, kThreads, smem, s>>>(p, host_tables().code, (uint32_t)kCopies * 8u);
     return cudaGetLastError();
 }
 
