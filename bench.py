@@ -366,10 +366,19 @@ def e2e_measure(torch, lx, layers, steps, warmup):
     torch.cuda.synchronize()
     ms = a.elapsed_time(b) / steps
     total = sum(wl.algorithmic_bytes().values())
+    # the host link alone, for the record: one plain pinned copy each way of
+    # the K input (the e2e figure is bound by it)
+    link = {}
+    for name, dst, src in (("h2d_gbs", wl.x[K_], hx[K_]), ("d2h_gbs", hx[K_], wl.x[K_])):
+        a.record()
+        dst.copy_(src, non_blocking=True)
+        b.record()
+        torch.cuda.synchronize()
+        link[name] = src.numel() * src.element_size() / (a.elapsed_time(b) * 1e-3) / 1e9
     del wl, hx, hq, hout
     torch.cuda.empty_cache()
     return {"value": total / (ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "ms_per_step": ms, "layers": layers,
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms, "layers": layers, "link": link,
             "note": f"{layers} of the 94 layers per step (host buffers pinned), same path and byte accounting; "
                     "layer-pipelined: host-to-device, kernels and device-to-host of different layers overlap"}
 
