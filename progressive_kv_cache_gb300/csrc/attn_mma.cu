@@ -326,9 +326,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(AttnArgs a, Level
     }
     if (warp == 0)
         tmem_alloc(&sm.h.tmem, kTmemCols);
-    tcgen05_fence_before();
+    tc_fence_before();
     __syncthreads();
-    tcgen05_fence_after();
+    tc_fence_after();
     atomicMax(reinterpret_cast<int *>(&sm.h.qmax), __float_as_int(lq));   // non-negative floats order as ints
     // this warp's running outputs: lane quarter warp % 4, columns 64 (warp / 4) ..
     // + 63; column 16 r + 4 mm + 2 side + e of half hf (32 hf + ..) holds row g + 8 r,
@@ -659,9 +659,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(AttnArgs a, Level
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {     // the running outputs of m = 4 hf .. 4 hf + 3, from tensor memory
         float o[32];
-        tmem_wait_st32();
+        tmem_wait_st();
         tmem_ld32f(tO + 32 * hf, o);
-        tmem_wait_ld32();
+        tmem_wait_ld();
         if (rescale) {
 #pragma unroll
             for (int r = 0; r < R; ++r)
@@ -801,12 +801,12 @@ case I:                                                                         
                 mg.l[j][h] = l;
             }
         }
-        tmem_wait_st32();
+        tmem_wait_st();
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
             float o[32];
             tmem_ld32f(tO + 32 * hf, o);
-            tmem_wait_ld32();
+            tmem_wait_ld();
 #pragma unroll
             for (int r = 0; r < R; ++r)
 #pragma unroll
@@ -818,10 +818,10 @@ case I:                                                                         
                 }
         }
     }
-    tcgen05_fence_before();
+    tc_fence_before();
     __syncthreads();
     if (warp == 0) {                         // every warp's tensor-memory reads are done
-        tcgen05_fence_after();
+        tc_fence_after();
         tmem_dealloc(sm.h.tmem, kTmemCols);
     }
     static_assert(kWarps == 16, "one 16-lane group per query head below");
