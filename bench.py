@@ -889,6 +889,44 @@ def ablation_report(args):
         "cpu_baseline": cpu}))
 
 
+def realism(workloads=(2, 3, 4), pages=32):
+    """How concentrated the synthetic values are inside each page-channel's
+    range: for every (page, channel) of a sample, the width of the interval
+    holding the central 50 % of its 256 values (25th to 75th percentile by
+    rank), as a fraction of the page range max - min. The Lynx reading
+    (section 2, "Not all bits are equal") reports that on real KV half the
+    elements sit inside the middle 17 % of the value range. Host only: the
+    seeded generator gives the same values the GPU draws. Per workload: the
+    median and mean over the sampled page-channels of K and V, the median
+    over outlier and over ordinary channels, and the share at or below 17 %."""
+    import numpy as np
+    import lynx_synth as S
+    out = {}
+    for wi in workloads:
+        w = S.WORKLOADS[wi]
+        T = w.T if w.T else S.batched_layout(w)[1] * S.PAGE
+        fr, is_out = [], []
+        for s in (S.S_K, S.S_V):
+            sc = w.scales(s)
+            base = np.median(sc, axis=-1, keepdims=True)
+            for l, h in ((0, 0), (w.L - 1, w.H - 1)):
+                xb = S.laplace_bf16(w.key(s), sc, w.L, w.H, T, layers=[l], heads=[h], t1=pages * S.PAGE)
+                x = S.bf16_bits_to_f32(xb)[0, 0].reshape(pages, S.PAGE, S.D).astype(np.float64)
+                xs = np.sort(x, axis=1)
+                rng = xs[:, -1] - xs[:, 0]
+                mid = xs[:, 3 * S.PAGE // 4 - 1] - xs[:, S.PAGE // 4]
+                fr.append((mid / np.where(rng > 0, rng, 1)).ravel())
+                is_out.append(np.broadcast_to(sc[l, h] > 5 * base[l, h], (pages, S.D)).ravel())
+        fr, is_out = np.concatenate(fr), np.concatenate(is_out)
+        out[w.name] = dict(median=float(np.median(fr)), mean=float(fr.mean()),
+                           median_outlier_channels=float(np.median(fr[is_out])) if is_out.any() else None,
+                           median_other_channels=float(np.median(fr[~is_out])),
+                           share_at_or_below_17pct=float((fr <= 0.17).mean()),
+                           page_channels=int(fr.size))
+    return {"central_half_of_range": out, "page_reading": 0.17,
+            "definition": "(x_(192) - x_(64)) / (max - min) over the 256 tokens of a page-channel"}
+
+
 def run_gpu(args):
     import torch
     import torch.distributed as dist
@@ -1003,6 +1041,7 @@ def run_gpu(args):
             "e2e": e2e,
             "gpu_launches": wl_launches(args.steps, wl_layers, only),
             "clocks": clk.summary(),
+            "realism": {k: round(v["median"], 4) for k, v in realism()["central_half_of_range"].items()},
         }
         print(json.dumps(line))
     if world > 1:
@@ -1050,14 +1089,17 @@ def main():
                                        "decode_attn_full"], default=None,
                     help="time one kernel group only (for profiler captures on smaller cases)")
     ap.add_argument("--layers", type=int, default=None, help="layers of the cache (default: all 94)")
-    ap.add_argument("--report", choices=["progressive", "append", "split-stream", "verify", "ablation", "batched"],
+    ap.add_argument("--report", choices=["progressive", "append", "split-stream", "verify", "ablation", "batched",
+                                         "realism"],
                     default=None,
                     help="progressive: residual layers arriving one by one (8 layers, 64K tokens); "
                          "append: quantize-on-append of 32 requests' tail pages over 94 layers x 8 KV heads; "
                          "split-stream: anchors then residuals over an emulated link, decode on anchors first; "
                          "verify: multi-token verify attention (64 draft positions, 32K context); "
                          "ablation: quantizer variants and uniform comparators, vNMSE and encoder GB/s; "
-                         "batched: decode attention of 32 ragged requests, 8 KV heads, GQA group 8")
+                         "batched: decode attention of 32 ragged requests, 8 KV heads, GQA group 8; "
+                         "realism: share of each page-channel range holding the central half of the "
+                         "synthetic values (host only)")
     ap.add_argument("--no-graph", action="store_true",
                     help="issue every library call from Python instead of replaying CUDA graphs of them")
     args = ap.parse_args()
@@ -1081,6 +1123,8 @@ def main():
         ablation_report(args)
     elif args.report == "batched":
         batched_report(args)
+    elif args.report == "realism":
+        print(json.dumps(realism()))
     else:
         run_gpu(args)
 

@@ -39,6 +39,13 @@
  *            T_k = fp32 nearest(((1+alpha)^((k-1/2)/63) - 1)/alpha), alpha = 255;
  *            c = q for w >= 0, c = -max(q, 1) for w < 0      (c in -63..63)
  *   stage 4  b = c + 7; A = floor(b/16) in -4..4; r = b - 16A in 0..15.
+ * Statistics fp32 cannot carry (the pages are silent; the reading taken): a
+ *   NaN among a channel's valid values stores the channel's page minimum and
+ *   range as the quiet NaN 0x7FC00000 (any NaN range is stored as that
+ *   pattern); when the range or its reciprocal is not finite (a NaN or
+ *   infinite input, a range beyond fp32, a subnormal range whose reciprocal
+ *   overflows) every u of the channel is 0, so its chunk means and scales are
+ *   0 and its codes 0 (anchor 0, residual 7).
  * Decoders: Lv[k] = fp16 nearest(((1+alpha)^(k/63) - 1)/alpha), k = 0..64;
  *   anchor-only code 16A, full code 16A + r - 7 (magnitudes above 64, which
  *   the encoder never writes, saturate at Lv[64]);
@@ -196,9 +203,12 @@ lynx_status lynx_decode_attn(const void *q_bf16, const lynx_qkv *k, const lynx_q
  * split-K partials go to a fixed array of LYNX_NOALLOC_SCRATCH_BYTES inside
  * the library, which every GPU that loads the library holds until the process
  * exits. The call allocates nothing.
- *  - Returns LYNX_ERR_WORKSPACE, without launching, when this batch shape needs
- *    more than LYNX_NOALLOC_SCRATCH_BYTES (compare with
- *    lynx_decode_attn_workspace(batch, q_heads, max_pages)).
+ *  - Argument checks are those of lynx_decode_attn, in the same order. Then,
+ *    without launching, it returns LYNX_ERR_WORKSPACE when the split-K plan of
+ *    this shape (batch, q_heads, kv_heads, max_pages on this device) needs more
+ *    than LYNX_NOALLOC_SCRATCH_BYTES; lynx_decode_attn_workspace(batch,
+ *    q_heads, max_pages), the largest need over every kv_heads, is an upper
+ *    bound of it.
  *  - The first call on each device looks up the array's device address once
  *    (a host-side query); make that first call before any stream capture.
  *  - Every call on a device shares the one array, and it keeps whatever the

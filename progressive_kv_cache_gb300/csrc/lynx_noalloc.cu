@@ -52,9 +52,11 @@ extern "C" lynx_status lynx_decode_attn_noalloc(const void *q_bf16, const lynx_q
                                                 lynx_mode mode, float *out, float *scores, uint32_t *dev_err,
                                                 void *stream)
 {
-    if (batch > 0 && q_heads > 0 && max_pages > 0 &&
-        lynx_decode_attn_workspace(batch, q_heads, max_pages) > kNoAllocScratchBytes)
-        return LYNX_ERR_WORKSPACE;
+    // The scratch is offered to lynx_decode_attn as a workspace of
+    // kNoAllocScratchBytes: its own checks (arguments first, then the split
+    // plan of this very shape against the workspace size) run before anything
+    // is launched, so a shape whose partials do not fit is refused there with
+    // LYNX_ERR_WORKSPACE.
     void *scratch = nullptr;
     if (batch > 0 && q_heads > 0) {
         lynx_status st = scratch_for_current_device(&scratch);

@@ -64,22 +64,20 @@ U32 = 2.0 ** -24
 ATTN_SENS_C = 8.0
 
 
-def attn_tolerance(orc, qb, kref, vref, layer, table, ctx, sm_scale, full):
-    """Per-output bound |o_gpu - o| <= 2e-3 + C * E for an fp32 decode attention.
+def attn_sensitivity(orc, qb, kref, vref, layer, table, ctx, sm_scale, full):
+    """E[b,h,d] = u32 * sum_t p_t |v_td - o_d| * sm_scale * sum_d' |q_d'| |k_td'|.
 
-    E[b,h,d] = u32 * sum_t p_t |v_td - o_d| * sm_scale * sum_d' |q_d'| |k_td'| is
-    the first-order change of output (b,h,d) when every score carries a relative
-    fp32 rounding of its magnitude sum_d' |q k|: the error that even correctly
-    rounded fp32 scores leave when logits span hundreds (outlier channels in
-    both K and V). p, o, k, v are the oracle's fp64 quantities; C = 8 covers the
-    error growth of a 128-term fp32 dot product and the fp32 decode of k."""
+    The first-order change of output (b,h,d) when every score carries a
+    relative fp32 rounding of its magnitude sum_d' |q k|: the error that even
+    correctly rounded fp32 scores leave when logits span hundreds (outlier
+    channels in both K and V). p, o, k, v are the oracle's fp64 quantities."""
     K = orc.dequant(kref, full)[layer]
     V = orc.dequant(vref, full)[layer]
     q = (np.asarray(qb, np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
     B, Hq, _ = q.shape
     H = K.shape[0]
     G = Hq // H
-    tol = np.full((B, Hq, D), ATTN_ATOL)
+    E = np.zeros((B, Hq, D))
     for b in range(B):
         n = int(ctx[b])
         if n <= 0:
@@ -95,6 +93,40 @@ def attn_tolerance(orc, qb, kref, vref, layer, table, ctx, sm_scale, full):
             A = sm_scale * (np.abs(Q) @ np.abs(Kg).T)
             w = p * A * U32
             for h in range(G):
-                E = w[h] @ np.abs(Vg - o[h][None, :])
-                tol[b, g * G + h] += ATTN_SENS_C * E
-    return tol
+                E[b, g * G + h] = w[h] @ np.abs(Vg - o[h][None, :])
+    return E
+
+
+def attn_tolerance(orc, qb, kref, vref, layer, table, ctx, sm_scale, full):
+    """Per-output bound |o_gpu - o| <= 2e-3 + C * E for an fp32 decode attention
+    (E from attn_sensitivity; C = 8, derived from the kernels' score arithmetic
+    in the design notes and checked by the C each comparison actually needs)."""
+    return ATTN_ATOL + ATTN_SENS_C * attn_sensitivity(orc, qb, kref, vref, layer, table, ctx, sm_scale, full)
+
+
+# every comparison's record: (label, outputs, outputs above the flat 2e-3, max |err| among them,
+# largest C*E of the bound, C needed)
+ATTN_RECORDS = []
+
+
+def assert_attn_close(got, ref, E, label=""):
+    """|got - ref| <= 2e-3 + C E elementwise, with an audit of how much of the
+    sensitivity term is used: the outputs above the flat 2e-3, their largest
+    error, the largest C E of the bound, and the C those outputs need,
+    max (|err| - 2e-3) / E (0 when none exceeds 2e-3). The test fails unless
+    every output above 2e-3 lies where the sensitivity term covers it."""
+    got = np.asarray(got, np.float64)
+    err = np.abs(got - ref)
+    assert np.all(np.isfinite(got)), f"{label}: non-finite outputs"
+    tol = ATTN_ATOL + ATTN_SENS_C * E
+    over = err > ATTN_ATOL
+    n_over = int(over.sum())
+    c_need = float(((err[over] - ATTN_ATOL) / np.maximum(E[over], 1e-300)).max()) if n_over else 0.0
+    rec = (label, int(err.size), n_over, float(err[over].max()) if n_over else 0.0,
+           float((ATTN_SENS_C * E).max()), c_need)
+    ATTN_RECORDS.append(rec)
+    worst = np.unravel_index(np.argmax(err / tol), err.shape)
+    print(f"{label}: max |err| {err.max():.3g}; {n_over} of {err.size} outputs above 2e-3 (max {rec[3]:.3g}); "
+          f"largest C*E {rec[4]:.3g}; C needed {c_need:.3g} of {ATTN_SENS_C:g}; max err/tol {(err / tol).max():.3g}")
+    assert np.all(err <= tol), (label, float(err[worst]), float(tol[worst]), worst)
+    return rec

@@ -35,6 +35,14 @@ def test_exports_every_declared_symbol(lx):
         assert hasattr(lib, n), n
 
 
+def test_noalloc_scratch_size_matches_the_header(lx):
+    """The binding's copy of the no-alloc scratch size is the header's."""
+    src = open(HEADER).read()
+    m = re.search(r"#define\s+LYNX_NOALLOC_SCRATCH_BYTES\s+\(\(size_t\)(\d+)\s*<<\s*(\d+)\)", src)
+    assert m, "LYNX_NOALLOC_SCRATCH_BYTES not found"
+    assert lx.NOALLOC_SCRATCH_BYTES == int(m.group(1)) << int(m.group(2))
+
+
 def test_status_strings(lx):
     lib = lx.library()
     seen = set()

@@ -106,6 +106,18 @@ def test_unrepresentable_statistics(lx, orc):
     assert_planes_equal(_encode(lx, xb), orc.quantize(xb))
 
 
+@pytest.mark.parametrize("which", ["u", "tree", "w", "mean"])
+def test_contract_order_pages(lx, orc, which):
+    """The pages that tell the contract's operation order apart from the
+    plausible alternatives (u and w as products with a reciprocal, the
+    stride-halving chunk sum, mean = sum / n_c): bit-exact with the oracle."""
+    import test_oracle_contract_order as O
+    chunk = {"u": [0x400E] * 32, "tree": O.SEQ_CHUNK, "w": O.W_CHUNK,
+             "mean": [0x3D7F, 0x3D9E, 0x3F2B, 0x3B85, 0x3ECE, 0x0000, 0x3F33]}[which]
+    xb, valid = O._page(chunk)
+    assert_planes_equal(_encode(lx, xb, valid), orc.quantize(xb, valid))
+
+
 def test_qwen3_235b_like_layer_every_page(lx, orc):
     """4 KV heads x 32K tokens, K and V: every page bit-exact."""
     w = S.WORKLOADS[2]

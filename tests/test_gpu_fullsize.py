@@ -8,7 +8,7 @@ import pytest
 import torch
 
 import lynx_synth as S
-from gpu_helpers import assert_dequant_close, assert_planes_equal, attn_tolerance, bf16_dev, i32_dev
+from gpu_helpers import assert_dequant_close, assert_attn_close, assert_planes_equal, attn_sensitivity, bf16_dev, i32_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -95,7 +95,5 @@ def test_decode_attention_whole_layer(lx, orc, full_cache, layer):
     for mode in (0, 1):
         out = lx.decode_attn(bf16_dev(qb), kq, vq, layer, i32_dev(table), i32_dev(ctx), 128 ** -0.5, mode)
         ref = orc.decode_attn(qb, kr, vr, 0, table, ctx, 128 ** -0.5, mode == 1)
-        tol = attn_tolerance(orc, qb, kr, vr, 0, table, ctx, 128 ** -0.5, mode == 1)
-        err = np.abs(out.cpu().numpy() - ref)
-        print(f"layer {layer} mode {mode}: max |err| {err.max():.3g}, max err/tol {(err / tol).max():.3g}")
-        assert np.all(err <= tol), (mode, err.max())
+        E = attn_sensitivity(orc, qb, kr, vr, 0, table, ctx, 128 ** -0.5, mode == 1)
+        assert_attn_close(out.cpu().numpy(), ref, E, f"layer {layer} mode {mode}")

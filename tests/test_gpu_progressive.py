@@ -8,7 +8,7 @@ import pytest
 import torch
 
 import lynx_synth as S
-from gpu_helpers import assert_dequant_close, attn_tolerance
+from gpu_helpers import assert_attn_close, assert_dequant_close, attn_sensitivity
 
 pytestmark = pytest.mark.gpu
 
@@ -65,8 +65,6 @@ def test_refined_cache_and_attention_against_oracle(run, orc):
         ctx = np.array([W.T, W.T], np.int32)
         for mode, got in ((0, r["out_anchor"][l]), (1, r["outs"][l])):
             ref = orc.decode_attn(qb, kr, vr, 0, table, ctx, 128 ** -0.5, mode == 1)
-            tol = attn_tolerance(orc, qb, kr, vr, 0, table, ctx, 128 ** -0.5, mode == 1)
+            E = attn_sensitivity(orc, qb, kr, vr, 0, table, ctx, 128 ** -0.5, mode == 1)
             g = got[[0, 3]][:, qsel].cpu().numpy()
-            err = np.abs(g - ref)
-            print(f"layer {l} mode {mode}: max |err| {err.max():.3g}, max err/tol {(err / tol).max():.3g}")
-            assert np.all(err <= tol)
+            assert_attn_close(g, ref, E, f"progressive layer {l} mode {mode}")

@@ -7,7 +7,7 @@ import pytest
 import torch
 
 import lynx_synth as S
-from gpu_helpers import attn_tolerance, bf16_dev, i32_dev
+from gpu_helpers import assert_attn_close, attn_sensitivity, attn_tolerance, bf16_dev, i32_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -45,14 +45,10 @@ def _check(lx, orc, cache, qb, layer, table, ctx, mode, positions=None):
     full = mode == lx.MODE_FULL
     ref = orc.verify_attn(qb, kr, vr, layer, table, ctx, 128 ** -0.5, full)
     assert int(err.item()) == 0
-    worst = 0.0
     for i in (range(Tq) if positions is None else positions):
         n = np.maximum(np.asarray(ctx) - Tq + i + 1, 0)
-        tol = attn_tolerance(orc, qb[:, i], kr, vr, layer, table, n, 128 ** -0.5, full)
-        e = np.abs(out[:, i] - ref[:, i])
-        worst = max(worst, float((e / tol).max()))
-        assert np.all(e <= tol), (i, float(e.max()))
-    print(f"verify attention: worst err/tol {worst:.3g}")
+        E = attn_sensitivity(orc, qb[:, i], kr, vr, layer, table, n, 128 ** -0.5, full)
+        assert_attn_close(out[:, i], ref[:, i], E, f"verify position {i} mode {mode}")
     return out
 
 
@@ -116,6 +112,10 @@ def test_single_position_equals_decode_attention(lx, orc, mode):
     full = mode == lx.MODE_FULL
     ov = lx.verify_attn(bf16_dev(qb), kq, vq, 0, i32_dev(table), i32_dev(ctx), 128 ** -0.5, mode).cpu().numpy()[:, 0]
     od = lx.decode_attn(bf16_dev(qb[:, 0]), kq, vq, 0, i32_dev(table), i32_dev(ctx), 128 ** -0.5, mode).cpu().numpy()
+    E = attn_sensitivity(orc, qb[:, 0], kr, vr, 0, table, np.asarray(ctx), 128 ** -0.5, full)
+    ref = orc.decode_attn(qb[:, 0], kr, vr, 0, table, np.asarray(ctx), 128 ** -0.5, full)
+    assert_attn_close(ov, ref, E, f"verify one position mode {mode}")
+    assert_attn_close(od, ref, E, f"decode one position mode {mode}")
     tol = attn_tolerance(orc, qb[:, 0], kr, vr, 0, table, np.asarray(ctx), 128 ** -0.5, full)
     assert np.all(np.abs(ov - od) <= 2 * tol)
 

@@ -26,6 +26,14 @@ MUTANTS = {
     "mean over 32 slots": ("float mean = slot[0] / (float)nc;", "float mean = slot[0] / 32.0f;"),
     "anchor not at residual centre": ("    int c = 16 * A;\n    if (full)", "    int c = 16 * A + 7;\n    if (full)"),
     "residual bias dropped in decode": ("c = 16 * A + r - ORC_BIAS;", "c = 16 * A + r;"),
+    "chunk sum left to right": ("for (int h = ORC_CHUNK / 2; h >= 1; h /= 2)\n                    for (int i = 0; i < h; ++i)\n"
+                                "                        slot[i] = slot[i] + slot[i + h];",
+                                "for (int i = 1; i < ORC_CHUNK; ++i)\n                    slot[0] = slot[0] + slot[i];"),
+    "u by division": ("(bf16_to_f32(x[(size_t)t * ORC_D + d]) - mn) * inv_r;",
+                      "(bf16_to_f32(x[(size_t)t * ORC_D + d]) - mn) / rng;"),
+    "w by division": ("float w = v * inv_s;", "float w = sf > 0.0f ? v / sf : 0.0f;"),
+    "mean times the reciprocal count": ("float mean = slot[0] / (float)nc;",
+                                        "float mean = slot[0] * (1.0f / (float)nc);"),
     "GQA head mapping": ("const uint16_t *qh = q + ((size_t)b * Hq + (size_t)g * G + h) * ORC_D;",
                          "const uint16_t *qh = q + ((size_t)b * Hq + (size_t)h * H + g) * ORC_D;"),
 }
@@ -52,6 +60,7 @@ def _pins():
     import test_oracle_attention as A
     import test_oracle_encoder as E
     import test_oracle_map as M
+    import test_oracle_contract_order as O
     import test_oracle_tables as T
     return [
         lambda o: T.test_thresholds_sit_at_half_levels(o),
@@ -65,6 +74,10 @@ def _pins():
         lambda o: E.test_ragged_chunk_metadata_against_fp64_statistics(o),
         lambda o: E.test_reconstruction_within_half_a_log_step(o),
         lambda o: E.test_brute_force_code_selection(o, 11),
+        lambda o: O.test_u_is_a_product_with_the_reciprocal(o),
+        lambda o: O.test_chunk_sum_is_the_stride_halving_tree(o),
+        lambda o: O.test_w_is_a_product_with_the_reciprocal(o),
+        lambda o: O.test_mean_is_a_division_by_the_valid_count(o),
         lambda o: A.test_gqa_groups_are_contiguous(o),
         lambda o: A.test_matches_numpy_softmax_through_permuted_pages(o, True),
         lambda o: M.test_map_is_round_half_up_in_log_domain(o),

@@ -6,9 +6,11 @@ caller-provided workspace.
 
 Checked through the C ABI against lynx_decode_attn on the same inputs, on two
 calls in a row (the second must not see anything of the first through the
-shared array), within the attention tolerance of the parity tests, plus the
-rejection of a batch shape that needs more scratch than the array holds.
-This file is named so that pytest collects it last."""
+shared array). Both calls run the same kernels with the same split plan, so
+the outputs must be equal bit for bit; each is also checked against the
+oracle's fp64 decode attention within the attention tolerance of the parity
+tests. Plus the rejection of a batch shape that needs more scratch than the
+array holds. This file is named so that pytest collects it last."""
 import ctypes
 
 import numpy as np
@@ -16,7 +18,7 @@ import pytest
 import torch
 
 import lynx_synth as S
-from gpu_helpers import attn_tolerance, bf16_dev, i32_dev
+from gpu_helpers import assert_attn_close, attn_sensitivity, bf16_dev, i32_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -60,10 +62,10 @@ def test_noalloc_matches_workspace_entry_point_twice(lx, orc):
         assert st == lx.OK, lx.library().lynx_status_string(st)
         ref = lx.decode_attn(qt, kq, vq, layer, tt, ct, 128 ** -0.5, mode)
         torch.cuda.synchronize()
-        tol = attn_tolerance(orc, qb, kr, vr, layer, table, ctx, 128 ** -0.5, mode == 1)
-        err = np.abs(out.cpu().numpy() - ref.cpu().numpy())
-        assert np.all(np.isfinite(out.cpu().numpy()))
-        assert np.all(err <= tol), err.max()
+        assert torch.equal(out, ref)
+        want = orc.decode_attn(qb, kr, vr, layer, table, ctx, 128 ** -0.5, mode == 1)
+        E = attn_sensitivity(orc, qb, kr, vr, layer, table, ctx, 128 ** -0.5, mode == 1)
+        assert_attn_close(out.cpu().numpy(), want, E, f"no-alloc layer {layer} mode {mode}")
 
 
 def test_noalloc_rejects_shapes_beyond_its_scratch(lx):
