@@ -185,6 +185,10 @@ size_t lynx_decode_attn_workspace(int32_t batch, int32_t q_heads, int32_t max_pa
  *   workspace   device, ws_bytes >= lynx_decode_attn_workspace(batch, q_heads, max_pages)
  *   dev_err     device or NULL, one uint32 (LYNX_DEVERR_* bits OR-ed in)
  * q_heads must be a multiple of kv_heads with a group size of at most 32.
+ * Groups of up to 16 query heads run on a tensor-core kernel whose level
+ * table sits at a fixed shared-memory address; on a device whose dynamic
+ * shared-memory window does not start 1 KiB into the CTA's shared memory
+ * (measured once per device) the call returns LYNX_ERR_UNSUPPORTED.
  */
 lynx_status lynx_decode_attn(const void *q_bf16, const lynx_qkv *k, const lynx_qkv *v, int32_t layer,
                              const int32_t *page_table, const int32_t *ctx_lens, int32_t batch,

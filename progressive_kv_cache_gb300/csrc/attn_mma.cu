@@ -68,8 +68,8 @@ constexpr float kLn2 = 0.6931471805599453f;
 // on this part family). With that base the level table below starts at shared
 // address 0x10000, and the shared address of a table word is one byte permute
 // of the code byte and a per-lane constant. The base is measured once per
-// device (table_aligned()); with any other base the kernel adds the table's
-// address to every lookup instead.
+// device (table_aligned()); a device whose window starts elsewhere is refused
+// (the call returns LYNX_ERR_UNSUPPORTED), and the kernel checks it again.
 constexpr uint32_t kDynBase = 1024;
 constexpr uint32_t kPre = 0x10000 - kDynBase;
 
@@ -110,7 +110,7 @@ constexpr int kMrow = 4 * 34;                 // a merge row: four 32-channel bl
 struct Merge {                                // overlays the table and the planes after the page loop
     float m[kWarps][16];                      // per warp and query head
     float l[kWarps][16];
-    float o[kWarps][16][kMrow];               // channel d at 34 (d / 32) + d % 32: a warp's stores hit two banks each
+    float o4[4][16][kMrow];                   // per lane quarter: its four warps' weighted sum; channel d at 34 (d / 32) + d % 32
     float sc[16][kWarps];                     // per query head: each warp's weight 2^(m_w - M)
     float M[16], L[16];                       // per query head: the range's max and sum
 };
@@ -132,13 +132,20 @@ __device__ __forceinline__ void mma16816_z(float (&c)[4], const uint32_t (&a)[4]
                  : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(0.0f));
 }
 
-// (x0, x1) -> fp16 pairs hi and lo with hi + lo = (x0, x1) to ~22 bits.
+// (x0, x1) -> fp16 pairs hi and lo with hi + lo = (x0, x1) to ~22 bits. The
+// remainders x - hi are exact in fp32; each comes from one mixed-precision
+// multiply-add (fp16 operands, fp32 addend and result), with no separate
+// widening of hi.
 __device__ __forceinline__ void split2(float2 x, uint32_t &hi, uint32_t &lo)
 {
     const __half2 h = __floats2half2_rn(x.x, x.y);
-    const float2 r = __ffma2_rn(__half22float2(h), make_float2(-1.0f, -1.0f), x);
-    const __half2 l = __floats2half2_rn(r.x, r.y);
     hi = *reinterpret_cast<const uint32_t *>(&h);
+    float r0, r1;
+    asm("{\n\t.reg .b16 h0, h1, m1;\n\tmov.b32 {h0, h1}, %2;\n\tmov.b16 m1, 0xBC00;\n\t"
+        "fma.rn.f32.f16 %0, h0, m1, %3;\n\tfma.rn.f32.f16 %1, h1, m1, %4;\n\t}"
+        : "=f"(r0), "=f"(r1)
+        : "r"(hi), "f"(x.x), "f"(x.y));
+    const __half2 l = __floats2half2_rn(r0, r1);
     lo = *reinterpret_cast<const uint32_t *>(&l);
 }
 
@@ -153,14 +160,12 @@ __device__ __forceinline__ float exp2_sm(float x)
     return y;
 }
 
-// Table word of code byte I of w. AL: lanebase = table address | lane offset
-// and one permute forms the shared address; otherwise lanebase = lane offset
-// and the table's address is added.
-template <bool AL, int I>
-__device__ __forceinline__ uint32_t lut_ld(uint32_t w, uint32_t lanebase, uint32_t base)
+// Table word of code byte I of w: lanebase = the table's shared address |
+// this lane's column, and one permute puts the code byte in bits 8-15.
+template <int I>
+__device__ __forceinline__ uint32_t lut_ld(uint32_t w, uint32_t lanebase)
 {
-    const uint32_t addr =
-        AL ? __byte_perm(w, lanebase, 0x7604u | (I << 4)) : __byte_perm(w, lanebase, 0x5504u | (I << 4)) + base;
+    const uint32_t addr = __byte_perm(w, lanebase, 0x7604u | (I << 4));
     uint32_t v;
     asm("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
     return v;
@@ -221,7 +226,7 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar)
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
-template <bool G16, bool FULL, int NS, bool AL>
+template <bool G16, bool FULL, int NS>
 __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(AttnArgs a, LevelTable lev)
 {
     constexpr int R = G16 ? 2 : 1;          // query-head rows per lane: g (and g + 8)
@@ -232,6 +237,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(AttnArgs a, Level
     const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
     const int G = a.G;
     const int64_t T = (int64_t)a.pool_pages * kPage;
+
+    if (smem_u32(smem_raw) != kDynBase) {    // the table layout needs this window base (checked on the host too)
+        if (a.dev_err && tid == 0)
+            atomicOr(a.dev_err, LYNX_DEVERR_TIMEOUT);
+        return;
+    }
 
     int ctx = a.ctx[b];
     if (ctx < 0 || ctx > a.max_pages * kPage) {
@@ -392,7 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(AttnArgs a, Level
     // c % 8 of page c / 8) ------------------------------------------------
     const uint32_t lane4 = (uint32_t)lane << 2;
     const uint32_t lut_s = smem_u32(sm.lut);
-    const uint32_t lb = (FULL ? 128u : 0u) + lane4 + (AL ? lut_s : 0u);   // this lane's table column
+    const uint32_t lb = (FULL ? 128u : 0u) + lane4 + lut_s;   // this lane's table column
     float *kaf = sm.h.aff[warp][0], *kbf = sm.h.aff[warp][1];             // K's, then V's
     float *vaf = kaf, *vbf = kbf;
     const float qmax = sm.h.qmax;
@@ -501,19 +512,19 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(AttnArgs a, Level
                     const uint32_t rw = wi == 0 ? kr4[nt].x : wi == 1 ? kr4[nt].y : wi == 2 ? kr4[nt].z : kr4[nt].w;
                     const uint32_t ev = codes_even(aw, rw), od = codes_odd(aw, rw);
                     if (s & 1) {
-                        b0 = pack_lo(lut_ld<AL, 2>(ev, lb, lut_s), lut_ld<AL, 2>(od, lb, lut_s));
-                        b1 = pack_lo(lut_ld<AL, 3>(ev, lb, lut_s), lut_ld<AL, 3>(od, lb, lut_s));
+                        b0 = pack_lo(lut_ld<2>(ev, lb), lut_ld<2>(od, lb));
+                        b1 = pack_lo(lut_ld<3>(ev, lb), lut_ld<3>(od, lb));
                     } else {
-                        b0 = pack_lo(lut_ld<AL, 0>(ev, lb, lut_s), lut_ld<AL, 0>(od, lb, lut_s));
-                        b1 = pack_lo(lut_ld<AL, 1>(ev, lb, lut_s), lut_ld<AL, 1>(od, lb, lut_s));
+                        b0 = pack_lo(lut_ld<0>(ev, lb), lut_ld<0>(od, lb));
+                        b1 = pack_lo(lut_ld<1>(ev, lb), lut_ld<1>(od, lb));
                     }
                 } else {
                     if (s & 1) {
-                        b0 = lut_ld<AL, 2>(aw, lb, lut_s);
-                        b1 = lut_ld<AL, 3>(aw, lb, lut_s);
+                        b0 = lut_ld<2>(aw, lb);
+                        b1 = lut_ld<3>(aw, lb);
                     } else {
-                        b0 = lut_ld<AL, 0>(aw, lb, lut_s);
-                        b1 = lut_ld<AL, 1>(aw, lb, lut_s);
+                        b0 = lut_ld<0>(aw, lb);
+                        b1 = lut_ld<1>(aw, lb);
                     }
                 }
                 if (s == 0)
@@ -689,10 +700,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mma_kernel(AttnArgs a, Level
                     switch (m & 3) {
 #define LYNX_V_FULL(I)                                                                                                 \
 case I:                                                                                                            \
-    bl0 = pack_lo(lut_ld<AL, I>(e0, lb, lut_s), lut_ld<AL, I>(e1, lb, lut_s));                                      \
-    bl1 = pack_lo(lut_ld<AL, I>(e2, lb, lut_s), lut_ld<AL, I>(e3, lb, lut_s));                                      \
-    bo0 = pack_lo(lut_ld<AL, I>(o0, lb, lut_s), lut_ld<AL, I>(o1, lb, lut_s));                                      \
-    bo1 = pack_lo(lut_ld<AL, I>(o2, lb, lut_s), lut_ld<AL, I>(o3, lb, lut_s));                                      \
+    bl0 = pack_lo(lut_ld<I>(e0, lb), lut_ld<I>(e1, lb));                                      \
+    bl1 = pack_lo(lut_ld<I>(e2, lb), lut_ld<I>(e3, lb));                                      \
+    bo0 = pack_lo(lut_ld<I>(o0, lb), lut_ld<I>(o1, lb));                                      \
+    bo1 = pack_lo(lut_ld<I>(o2, lb), lut_ld<I>(o3, lb));                                      \
     break;
                         LYNX_V_FULL(0)
                         LYNX_V_FULL(1)
@@ -707,10 +718,10 @@ case I:                                                                         
                     switch (m & 3) {
 #define LYNX_V_ANCHOR(I)                                                                                               \
 case I:                                                                                                            \
-    bl0 = lut_ld<AL, I>(e01, lb, lut_s);                                                                          \
-    bl1 = lut_ld<AL, I>(e23, lb, lut_s);                                                                          \
-    bo0 = lut_ld<AL, I>(o01, lb, lut_s);                                                                          \
-    bo1 = lut_ld<AL, I>(o23, lb, lut_s);                                                                          \
+    bl0 = lut_ld<I>(e01, lb);                                                                          \
+    bl1 = lut_ld<I>(e23, lb);                                                                          \
+    bo0 = lut_ld<I>(o01, lb);                                                                          \
+    bo1 = lut_ld<I>(o23, lb);                                                                          \
     break;
                         LYNX_V_ANCHOR(0)
                         LYNX_V_ANCHOR(1)
@@ -788,44 +799,20 @@ case I:                                                                         
     // ---- merge the chunks' states, write this range's partial ------------
     __syncthreads();   // every copy has landed and every table and plane read is done: the merge area overlays them
     Merge &mg = *reinterpret_cast<Merge *>(sm.lut);
-    {
-        const int j = warp;
 #pragma unroll
-        for (int r = 0; r < R; ++r) {
-            const int h = g + 8 * r;
-            float l = l_run[r];
-            l += __shfl_xor_sync(0xFFFFFFFFu, l, 1);
-            l += __shfl_xor_sync(0xFFFFFFFFu, l, 2);
-            if (q == 0) {
-                mg.m[j][h] = m_run[r];
-                mg.l[j][h] = l;
-            }
-        }
-        tmem_wait_st();
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-            float o[32];
-            tmem_ld32f(tO + 32 * hf, o);
-            tmem_wait_ld();
-#pragma unroll
-            for (int r = 0; r < R; ++r)
-#pragma unroll
-                for (int mm = 0; mm < 4; ++mm) {
-                    const int h = g + 8 * r, m = 4 * hf + mm;
-                    const float *ol = o + 16 * r + 4 * mm;
-                    *reinterpret_cast<float2 *>(&mg.o[j][h][34 * q + 2 * m]) = make_float2(ol[0], ol[1]);
-                    *reinterpret_cast<float2 *>(&mg.o[j][h][34 * q + 16 + 2 * m]) = make_float2(ol[2], ol[3]);
-                }
+    for (int r = 0; r < R; ++r) {            // (1) every warp's (max, sum) per query head
+        const int h = g + 8 * r;
+        float l = l_run[r];
+        l += __shfl_xor_sync(0xFFFFFFFFu, l, 1);
+        l += __shfl_xor_sync(0xFFFFFFFFu, l, 2);
+        if (q == 0) {
+            mg.m[warp][h] = m_run[r];
+            mg.l[warp][h] = l;
         }
     }
-    tc_fence_before();
     __syncthreads();
-    if (warp == 0) {                         // every warp's tensor-memory reads are done
-        tc_fence_after();
-        tmem_dealloc(sm.h.tmem, kTmemCols);
-    }
     static_assert(kWarps == 16, "one 16-lane group per query head below");
-    if (tid < 16 * kWarps) {                 // lane group h: warp w's weight for query head h
+    if (tid < 16 * kWarps) {                 // (2) lane group h: warp w's weight for query head h
         const int h = tid >> 4, w = tid & 15;
         const float mw = mg.m[w][h];
         float M = mw;
@@ -843,13 +830,50 @@ case I:                                                                         
             mg.L[h] = L;
         }
     }
+    tmem_wait_st();                          // this warp's last output stores are done
+    tc_fence_before();
     __syncthreads();
-    for (int e = tid; e < G * kD; e += kThreads) {
-        const int h = e / kD, d = e % kD;
-        float o = 0.0f;
+    tc_fence_after();
+    {
+        // (3) inside each lane quarter: warp (quarter q4, part cb) sums slice cb
+        // (16 columns) of the quarter's four warps' blocks, weighted. A lane holds
+        // the same (g, q) positions in every warp of its quarter; slice cb is
+        // half cb / 2 and row group cb % 2 of the block layout above
+        const int q4 = warp & 3, cb = warp >> 2, hf = cb >> 1, r = cb & 1, h = g + 8 * r;
+        if (G16 || r == 0) {
+            const uint32_t tq = sm.h.tmem + ((uint32_t)(32 * q4) << 16) + 16u * (uint32_t)cb;
+            float acc[16];
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w)
-            o = fmaf(mg.o[w][h][34 * (d >> 5) + (d & 31)], mg.sc[h][w], o);
+            for (int i = 0; i < 16; ++i)
+                acc[i] = 0.0f;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {    // warp q4 + 4k: its block starts at column 64k
+                float v[16];
+                tmem_ld16(tq + 64u * (uint32_t)k, v);
+                tmem_wait_ld();
+                const float s = mg.sc[h][q4 + 4 * k];
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    acc[i] = fmaf(v[i], s, acc[i]);
+            }
+#pragma unroll
+            for (int mm = 0; mm < 4; ++mm) { // column 4 mm + 2 side + e: channel 32 q + 16 side + 2 (4 hf + mm) + e
+                const int m = 4 * hf + mm;
+                *reinterpret_cast<float2 *>(&mg.o4[q4][h][34 * q + 2 * m]) = make_float2(acc[4 * mm], acc[4 * mm + 1]);
+                *reinterpret_cast<float2 *>(&mg.o4[q4][h][34 * q + 16 + 2 * m]) =
+                    make_float2(acc[4 * mm + 2], acc[4 * mm + 3]);
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {                         // every warp's tensor-memory reads are done
+        tc_fence_after();
+        tmem_dealloc(sm.h.tmem, kTmemCols);
+    }
+    for (int e = tid; e < G * kD; e += kThreads) {   // (4) the four quarters' sums
+        const int h = e / kD, d = e % kD, c = 34 * (d >> 5) + (d & 31);
+        const float o = (mg.o4[0][h][c] + mg.o4[1][h][c]) + (mg.o4[2][h][c] + mg.o4[3][h][c]);
         float *pp = a.part + ((qrow0 + h) * a.n_splits + split) * kPart;
         pp[d] = o;
         if (d == 0) {
@@ -859,7 +883,7 @@ case I:                                                                         
     }
 }
 
-template <bool G16, bool FULL, int NS, bool AL>
+template <bool G16, bool FULL, int NS>
 cudaError_t run(const AttnArgs &a, cudaStream_t s)
 {
     static_assert(sizeof(Head<NS>) <= kPre, "everything ahead of the table fits below 0x10000");
@@ -867,19 +891,13 @@ cudaError_t run(const AttnArgs &a, cudaStream_t s)
                   "merge area overlays the table and the planes");
     static_assert(sizeof(Smem<FULL, NS>) <= 227 * 1024, "shared memory per CTA");
     const size_t smem = sizeof(Smem<FULL, NS>);
-    cudaError_t e = cudaFuncSetAttribute(attn_mma_kernel<G16, FULL, NS, AL>,
+    cudaError_t e = cudaFuncSetAttribute(attn_mma_kernel<G16, FULL, NS>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess)
         return e;
     dim3 grid((unsigned)a.n_splits, (unsigned)a.H, (unsigned)a.B);
-    attn_mma_kernel<G16, FULL, NS, AL><<<grid, kThreads, smem, s>>>(a, host_tables().lev);
+    attn_mma_kernel<G16, FULL, NS><<<grid, kThreads, smem, s>>>(a, host_tables().lev);
     return cudaGetLastError();
-}
-
-template <bool G16, bool FULL, int NS>
-cudaError_t run_aligned_or_not(const AttnArgs &a, cudaStream_t s, bool al)
-{
-    return al ? run<G16, FULL, NS, true>(a, s) : run<G16, FULL, NS, false>(a, s);
 }
 
 __device__ uint32_t g_dyn_base;
@@ -917,10 +935,11 @@ bool table_aligned()
 cudaError_t launch_attn_mma(const AttnArgs &a, cudaStream_t s)
 {
     // slots hold one tensor's page: 16 KiB of codes in anchor mode, 32 KiB in full mode
-    const bool al = table_aligned();
+    if (!table_aligned())
+        return cudaErrorNotSupported;
     if (a.G <= 8)
-        return a.full ? run_aligned_or_not<false, true, 3>(a, s, al) : run_aligned_or_not<false, false, 6>(a, s, al);
-    return a.full ? run_aligned_or_not<true, true, 3>(a, s, al) : run_aligned_or_not<true, false, 6>(a, s, al);
+        return a.full ? run<false, true, 3>(a, s) : run<false, false, 6>(a, s);
+    return a.full ? run<true, true, 3>(a, s) : run<true, false, 6>(a, s);
 }
 
 } // namespace lynx

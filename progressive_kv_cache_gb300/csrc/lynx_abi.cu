@@ -26,7 +26,10 @@ lynx_status check_qkv(const lynx_qkv *t, bool need_residual)
     return LYNX_OK;
 }
 
-lynx_status from_cuda(cudaError_t e) { return e == cudaSuccess ? LYNX_OK : LYNX_ERR_CUDA; }
+lynx_status from_cuda(cudaError_t e)
+{
+    return e == cudaSuccess ? LYNX_OK : e == cudaErrorNotSupported ? LYNX_ERR_UNSUPPORTED : LYNX_ERR_CUDA;
+}
 
 } // namespace
 
