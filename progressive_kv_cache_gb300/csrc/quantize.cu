@@ -131,10 +131,18 @@ __device__ __forceinline__ uint32_t bf2_max(uint32_t a, uint32_t b)
     return *reinterpret_cast<uint32_t *>(&r);
 }
 
-// A bf16x2 word as float2 (x = low half).
-__device__ __forceinline__ float2 bf2_to_f2(uint32_t x)
+// (x0 - m0, x1 - m1) for the bf16 pair x, each one fp32 operation rounded to
+// nearest: x * 1 + (-m) with bf16 operands and an fp32 addend, whose product is
+// exact, so the result is the rounded difference itself; the bf16 values need
+// no separate widening.
+__device__ __forceinline__ float2 sub_bf2(uint32_t x, float2 negm)
 {
-    return make_float2(__uint_as_float(x << 16), __uint_as_float(x & 0xFFFF0000u));
+    float r0, r1;
+    asm("{\n\t.reg .b16 l, h, one;\n\tmov.b32 {l, h}, %2;\n\tmov.b16 one, 0x3F80;\n\t"
+        "fma.rn.f32.bf16 %0, l, one, %3;\n\tfma.rn.f32.bf16 %1, h, one, %4;\n\t}"
+        : "=f"(r0), "=f"(r1)
+        : "r"(x), "f"(negm.x), "f"(negm.y));
+    return make_float2(r0, r1);
 }
 
 // Stages 2-4 for this thread's two channels of one chunk, held as float2
@@ -331,9 +339,9 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_kernel(Params p, CodeTab
             const float2 ir = make_float2(ir0, ir1);
 #pragma unroll
             for (int i = 0; i < kChunk; ++i)
-                u[i] = __fmul2_rn(__fadd2_rn(bf2_to_f2(xw[i]), negmn), ir);
-            ulo = __fmul2_rn(__fadd2_rn(bf2_to_f2(cmn2), negmn), ir);
-            uhi = __fmul2_rn(__fadd2_rn(bf2_to_f2(cmx2), negmn), ir);
+                u[i] = __fmul2_rn(sub_bf2(xw[i], negmn), ir);
+            ulo = __fmul2_rn(sub_bf2(cmn2, negmn), ir);
+            uhi = __fmul2_rn(sub_bf2(cmx2, negmn), ir);
         }
 
         // (c) stages 2-4
