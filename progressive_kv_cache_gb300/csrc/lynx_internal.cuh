@@ -23,14 +23,16 @@ constexpr double kAlpha = 255.0;
 
 // Stage-3 bucket table. The code of w depends only on |w| through the count
 // q = #{k : |w| >= T_k}, and the table finds q with one lookup and one
-// compare: the bucket of |w| is bits(fp32(|w| + 2^-13)) >> 19, a monotone
+// integer add: the bucket of |w| is bits(fp32(|w| + 2^-13)) >> 19, a monotone
 // function of |w| with 16 buckets per octave of |w| + 2^-13, each narrower
 // than the gap between two consecutive thresholds, so at most one threshold
 // T* lies in a bucket (the builder checks this). |w| in [0, 2) gives buckets
 // kBucketBase .. kBucketBase + kNBucket - 1 with no clamp. Each entry holds
-// the bits of the float just below T* (+inf when the bucket holds none), so
-// that |w| >= T* exactly when pred(T*) - |w| is negative, and the four
-// possible stored bytes (c + 7) & 0xFF, selected by 2*sign(w) + (|w| >= T*):
+// K = 2^30 - bits(T*) (0 when the bucket holds none) and the four possible
+// stored bytes (c + 7) & 0xFF. For |w| < 2, bits(|w|) < 2^30, and for
+// non-negative floats bits(|w|) >= bits(T*) exactly when |w| >= T*, so
+// bits(w) + K never carries into bit 31 and its bits 31-30 are
+// 2 * sign(w) + (|w| >= T*), the index of the stored byte:
 //   byte 0: w >= 0 below T*   byte 1: w >= 0 at or above T*
 //   byte 2: w < 0 below T*    byte 3: w < 0 at or above T*
 // (sign(w) is the sign bit: the encoder turns -0 into +0 first).

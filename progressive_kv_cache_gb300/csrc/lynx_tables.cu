@@ -75,8 +75,11 @@ void build(HostTables &t)
         const int q1 = q0 + 1 > kQMax ? kQMax : q0 + 1;
         const int n0 = -(q0 > 1 ? q0 : 1), n1 = -(q1 > 1 ? q1 : 1);
         const uint32_t bytes = byte_of(q0) | (byte_of(q1) << 8) | (byte_of(n0) << 16) | (byte_of(n1) << 24);
-        const uint32_t below = inside ? f32_bits(t.thr[kin]) - 1u : 0x7F800000u;
-        t.code.e[i] = make_uint2(below, bytes);
+        // 2^30 - bits(T*) > 0 since T* <= 1 (bits below 2^30)
+        const uint32_t k_add = inside ? (1u << 30) - f32_bits(t.thr[kin]) : 0u;
+        if (inside && !(f32_bits(t.thr[kin]) < (1u << 30)))
+            t.ok = false;
+        t.code.e[i] = make_uint2(k_add, bytes);
     }
 
     // decoder levels

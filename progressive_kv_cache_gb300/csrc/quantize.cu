@@ -15,15 +15,16 @@
 // of the numeric contract runs inside one thread's registers. Stage 3 is one
 // lookup in a 16-way replicated bucket table (a conflict-free 8-byte load per
 // element) whose entry carries the four possible stored bytes, then one
-// compare and one byte permute. The packed planes are staged in shared memory
+// integer add and one byte permute. The packed planes are staged in shared memory
 // and leave with two 16 KiB bulk stores; the metadata goes out with direct
 // 4/8-byte stores.
 //
 // The kernel is bound by instruction issue, so the per-element work is kept
 // short: the bucket index needs no clamp (|w| + 2^-13 always lands in the
-// table), the threshold test is the sign of pred(T*) - |w|, and the chunk's
-// max |v| comes from its two extremes instead of a max over all elements (v
-// is a monotone function of x, so the extremes of x give the extremes of v).
+// table), the threshold test and the sign of w come out of one integer add
+// as the byte index, and the chunk's max |v| comes from its two extremes
+// instead of a max over all elements (v is a monotone function of x, so the
+// extremes of x give the extremes of v).
 // Codes are computed for a group of tokens before the group's stores: a table
 // load may not move above an earlier store to shared memory, so interleaving
 // them would serialise the tokens.
@@ -97,25 +98,23 @@ __device__ __forceinline__ uint2 lds_u2(uint32_t addr)
     return v;
 }
 
-// Stage 3 + the +7 bias for one value w (|w| < 2, never -0): the stored byte
-// (c + 7) & 0xFF (bits 8-31 zero), whose high nibble is the anchor and low
-// nibble the residual.
+// Stage 3 + the +7 bias for one value w (|w| < 2, never -0): a word whose
+// low byte is the stored byte (c + 7) & 0xFF, whose high nibble is the anchor
+// and low nibble the residual (bits 8-31 are not defined).
 // `tab_base` is the shared address of this lane's table replica, offset so
 // that the bucket number indexes it directly; `stride` is the byte distance
-// between buckets (kCopies * 8). It arrives as a kernel argument so that the
-// address is one integer multiply-add, which runs on the FMA pipe: with the
-// constant in view the compiler forms it with a shift-and-add on the ALU pipe,
-// the pipe this kernel saturates (5-6 % slower).
-__device__ __forceinline__ uint32_t code_byte(float w, uint32_t tab_base, uint32_t stride)
+// between buckets (kCopies * 8) and `one` is 1. Both arrive as kernel
+// arguments so that the bucket address and the threshold test are integer
+// multiply-adds, which run on the FMA pipe: with the constants in view the
+// compiler forms them with shifts and adds on the ALU pipe, the pipe this
+// kernel saturates.
+__device__ __forceinline__ uint32_t code_byte(float w, uint32_t tab_base, uint32_t stride, uint32_t one)
 {
-    const float a = fabsf(w);
-    const uint32_t bucket = __float_as_uint(__fadd_rn(a, __uint_as_float(kBucketOffsetBits))) >> 19;
+    const uint32_t bucket = __float_as_uint(__fadd_rn(fabsf(w), __uint_as_float(kBucketOffsetBits))) >> 19;
     const uint2 e = lds_u2(bucket * stride + tab_base);
-    // |w| >= T* exactly when pred(T*) - |w| < 0 (its sign bit); 2 * sign(w)
-    // is bits 31-30 of w (bit 30 is 0 for |w| < 2); 0x4440 makes the permute
-    // fill bytes 1-3 of the result with zeros
-    const uint32_t d = __float_as_uint(__fsub_rn(__uint_as_float(e.x), a));
-    return __byte_perm(e.y, 0u, (d >> 31) + (__float_as_uint(w) >> 30) + 0x4440u);
+    // bits 31-30 of bits(w) + K are 2 * sign(w) + (|w| >= T*): the byte index
+    const uint32_t t = __float_as_uint(w) * one + e.x;
+    return __byte_perm(e.y, 0u, t >> 30);
 }
 
 // bf16x2 min / max that propagate NaN (a NaN value marks its channel)
@@ -155,7 +154,7 @@ __device__ __forceinline__ float2 sub_bf2(uint32_t x, float2 negm)
 // metadata (mean, scale) of both channels as fp16x2 words.
 template <bool FULL>
 __device__ __forceinline__ void encode_chunk(const float2 (&u)[kChunk], int nc, float2 ulo, float2 uhi,
-                                             uint32_t tab_base, uint32_t stride, uint8_t *anc_row0,
+                                             uint32_t tab_base, uint32_t stride, uint32_t one, uint8_t *anc_row0,
                                              uint8_t *res_row0, uint32_t &mu2, uint32_t &s2)
 {
     // chunk mean: stride-halving pairwise tree over 32 slots, absent slots +0
@@ -203,10 +202,12 @@ __device__ __forceinline__ void encode_chunk(const float2 (&u)[kChunk], int nc, 
                 // w = v * inv_s, as one rounding of the product plus +0, which
                 // turns a -0 product into +0 (both code 0) and changes nothing else
                 const float2 w = __ffma2_rn(__fadd2_rn(u[i], negmu), inv_s, zero);
-                const uint32_t b0 = code_byte(w.x, tab_base, stride);
-                const uint32_t b1 = code_byte(w.y, tab_base, stride);
-                ab[k] = (b0 >> 4) | (b1 & 0xF0u);
-                rb[k] = (b0 & 0x0Fu) | ((b1 << 4) & 0xF0u);
+                const uint32_t b0 = code_byte(w.x, tab_base, stride, one);
+                const uint32_t b1 = code_byte(w.y, tab_base, stride, one);
+                // low bytes: the anchors and the residuals of the pair (bits
+                // 8-31 are not stored)
+                ab[k] = ((b0 >> 4) & 0x0Fu) | (b1 & ~0x0Fu);
+                rb[k] = (b0 & 0x0Fu) | (b1 << 4);
             }
         }
 #pragma unroll
@@ -219,8 +220,9 @@ __device__ __forceinline__ void encode_chunk(const float2 (&u)[kChunk], int nc, 
     s2 = (uint32_t)__half_as_ushort(sh0) | ((uint32_t)__half_as_ushort(sh1) << 16);
 }
 
-// tab_stride: kCopies * 8, passed at run time (see code_byte)
-__global__ void __launch_bounds__(kThreads, 1) quantize_kernel(Params p, CodeTable table, uint32_t tab_stride)
+// tab_stride: kCopies * 8, and one: 1, passed at run time (see code_byte)
+__global__ void __launch_bounds__(kThreads, 1) quantize_kernel(Params p, CodeTable table, uint32_t tab_stride,
+                                                               uint32_t one)
 {
     extern __shared__ __align__(128) unsigned char smem_raw[];
     Smem &sm = *reinterpret_cast<Smem *>(smem_raw);
@@ -277,12 +279,20 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_kernel(Params p, CodeTab
         for (int i = 0; i < kChunk; ++i)
             xw[i] = *reinterpret_cast<const uint32_t *>(xs + i * kD);
         uint32_t cmn2 = 0x7F807F80u, cmx2 = 0xFF80FF80u;   // +inf, -inf pairs
+        if (nc == kChunk) {
 #pragma unroll
-        for (int i = 0; i < kChunk; ++i)
-            if (i < nc) {
+            for (int i = 0; i < kChunk; ++i) {
                 cmn2 = bf2_min(cmn2, xw[i]);
                 cmx2 = bf2_max(cmx2, xw[i]);
             }
+        } else {
+#pragma unroll
+            for (int i = 0; i < kChunk; ++i)
+                if (i < nc) {
+                    cmn2 = bf2_min(cmn2, xw[i]);
+                    cmx2 = bf2_max(cmx2, xw[i]);
+                }
+        }
         sm.pmin[j][pi] = cmn2;
         sm.pmax[j][pi] = cmx2;
         if (tid == 0)
@@ -349,9 +359,9 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_kernel(Params p, CodeTab
         uint8_t *res_row0 = sm.res + j * kChunk * (kD / 2) + pi;
         uint32_t mu2 = 0, s2 = 0;
         if (nc == kChunk) {
-            encode_chunk<true>(u, nc, ulo, uhi, tab_base, tab_stride, anc_row0, res_row0, mu2, s2);
+            encode_chunk<true>(u, nc, ulo, uhi, tab_base, tab_stride, one, anc_row0, res_row0, mu2, s2);
         } else if (nc > 0) {
-            encode_chunk<false>(u, nc, ulo, uhi, tab_base, tab_stride, anc_row0, res_row0, mu2, s2);
+            encode_chunk<false>(u, nc, ulo, uhi, tab_base, tab_stride, one, anc_row0, res_row0, mu2, s2);
         } else {
 #pragma unroll
             for (int i = 0; i < kChunk; ++i) {
@@ -398,7 +408,7 @@ __global__ void level_codes_kernel(const float *__restrict__ w, int64_t n, int8_
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
         const float v = w[i];
         const float c = v == v ? __fadd_rn(copysignf(fminf(fabsf(v), 1.99999988f), v), 0.0f) : 0.0f;
-        codes[i] = (int8_t)((int)(int8_t)code_byte(c, tab_base, kCopies * 8) - kBias);
+        codes[i] = (int8_t)((int)(int8_t)code_byte(c, tab_base, kCopies * 8, 1u) - kBias);
     }
 }
 
@@ -414,7 +424,7 @@ cudaError_t run_quantize(const Params &p, cudaStream_t s)
     if (e != cudaSuccess)
         return e;
     const int64_t grid = p.pages < sms ? p.pages : sms;
-    quantize_kernel<<<(unsigned)grid, kThreads, smem, s>>>(p, host_tables().code, (uint32_t)kCopies * 8u);
+    quantize_kernel<<<(unsigned)grid, kThreads, smem, s>>>(p, host_tables().code, (uint32_t)kCopies * 8u, 1u);
     return cudaGetLastError();
 }
 
