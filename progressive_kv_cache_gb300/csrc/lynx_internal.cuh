@@ -26,8 +26,8 @@ constexpr double kAlpha = 255.0;
 // integer add: the bucket of |w| is bits(fp32(|w| + 2^-13)) >> 19, a monotone
 // function of |w| with 16 buckets per octave of |w| + 2^-13, each narrower
 // than the gap between two consecutive thresholds, so at most one threshold
-// T* lies in a bucket (the builder checks this). |w| in [0, 2) gives buckets
-// kBucketBase .. kBucketBase + kNBucket - 1 with no clamp. Each entry holds
+// T* lies in a bucket (the builder checks this). |w| in [0, 2 - 2^-13) gives
+// buckets kBucketBase .. kBucketBase + kNBucket - 1 with no clamp. Each entry holds
 // K = 2^30 - bits(T*) (0 when the bucket holds none) and the four possible
 // stored bytes (c + 7) & 0xFF. For |w| < 2, bits(|w|) < 2^30, and for
 // non-negative floats bits(|w|) >= bits(T*) exactly when |w| >= T*, so
@@ -37,7 +37,7 @@ constexpr double kAlpha = 255.0;
 //   byte 2: w < 0 below T*    byte 3: w < 0 at or above T*
 // (sign(w) is the sign bit: the encoder turns -0 into +0 first).
 constexpr uint32_t kBucketBase = (127u - 13u) << 4;   // bucket of 2^-13
-constexpr int kNBucket = 15 * 16;                      // |w| + 2^-13 in [2^-13, 4)
+constexpr int kNBucket = 14 * 16;                      // |w| + 2^-13 in [2^-13, 2)
 constexpr uint32_t kBucketOffsetBits = (127u - 13u) << 23;   // 2^-13
 
 struct CodeTable {

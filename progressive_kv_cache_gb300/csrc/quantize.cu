@@ -15,7 +15,10 @@
 // of the numeric contract runs inside one thread's registers. Stage 3 is one
 // lookup in a 16-way replicated bucket table (a conflict-free 8-byte load per
 // element) whose entry carries the four possible stored bytes, then one
-// integer add and one byte permute. The packed planes are staged in shared memory
+// integer add and one byte permute; the odd channel of a pair reads a second
+// table with the nibbles of each byte swapped, so that one more permute
+// merges the pair and the two plane bytes are a shift and a logic operation
+// away. The packed planes are staged in shared memory
 // and leave with two 16 KiB bulk stores; the metadata goes out with direct
 // 4/8-byte stores.
 //
@@ -41,6 +44,7 @@ constexpr int kThreads = 512;
 constexpr int kCopies = 16;                            // table replicas (one per half-warp lane)
 constexpr uint32_t kPageBytes = kPage * kD * 2;       // 64 KiB of bf16
 constexpr uint32_t kPlaneBytes = kPage * kD / 2;      // 16 KiB per plane and page
+constexpr uint32_t kTabBytes = kNBucket * kCopies * 8; // one replicated table
 constexpr uint32_t kWaitLimit = 1u << 22;
 constexpr uint32_t kQNaN = 0x7FC00000u;
 constexpr int kGroup = 16;                           // tokens whose codes are computed before their stores
@@ -54,7 +58,9 @@ struct Smem {
     uint8_t res[kPage * kD / 2];       // staged residual plane of the page
     uint32_t pmin[kNChunk][kD / 2];    // bf16x2 chunk minima of channel pairs
     uint32_t pmax[kNChunk][kD / 2];
-    uint2 tab[kNBucket * kCopies];
+    // [0]: the stored bytes; [1]: the same bytes with their nibbles swapped
+    // (the odd channel of a pair)
+    uint2 tab[2][kNBucket * kCopies];
     alignas(8) uint64_t bar[2];
 };
 
@@ -98,23 +104,48 @@ __device__ __forceinline__ uint2 lds_u2(uint32_t addr)
     return v;
 }
 
-// Stage 3 + the +7 bias for one value w (|w| < 2, never -0): a word whose
-// low byte is the stored byte (c + 7) & 0xFF, whose high nibble is the anchor
-// and low nibble the residual (bits 8-31 are not defined).
-// `tab_base` is the shared address of this lane's table replica, offset so
-// that the bucket number indexes it directly; `stride` is the byte distance
-// between buckets (kCopies * 8) and `one` is 1. Both arrive as kernel
-// arguments so that the bucket address and the threshold test are integer
-// multiply-adds, which run on the FMA pipe: with the constants in view the
-// compiler forms them with shifts and adds on the ALU pipe, the pipe this
-// kernel saturates.
-__device__ __forceinline__ uint32_t code_byte(float w, uint32_t tab_base, uint32_t stride, uint32_t one)
+// Bucket-table entry of w (|w| < 2) in table TAB. `tab_base` is the shared
+// address of this lane's replica of table 0, offset so that the bucket number
+// indexes it directly; `stride` is the byte distance between buckets
+// (kCopies * 8). It arrives as a kernel argument so that the address is one
+// integer multiply-add, which runs on the FMA pipe: with the constant in view
+// the compiler forms it with a shift and an add on the ALU pipe, the busier one.
+template <int TAB>
+__device__ __forceinline__ uint2 entry_of(float w, uint32_t tab_base, uint32_t stride)
 {
     const uint32_t bucket = __float_as_uint(__fadd_rn(fabsf(w), __uint_as_float(kBucketOffsetBits))) >> 19;
-    const uint2 e = lds_u2(bucket * stride + tab_base);
-    // bits 31-30 of bits(w) + K are 2 * sign(w) + (|w| >= T*): the byte index
-    const uint32_t t = __float_as_uint(w) * one + e.x;
-    return __byte_perm(e.y, 0u, t >> 30);
+    return lds_u2(bucket * stride + tab_base + TAB * kTabBytes);
+}
+
+// Index of the stored byte in the entry: bits 31-30 of bits(w) + K, which are
+// 2 * sign(w) + (|w| >= T*). `one` is 1, a kernel argument for the same reason
+// as the stride: the add is then a multiply-add on the FMA pipe.
+__device__ __forceinline__ uint32_t byte_index(float w, uint32_t k, uint32_t one)
+{
+    return (__float_as_uint(w) * one + k) >> 30;
+}
+
+// Stage 3 + the +7 bias for one value w (|w| < 2, never -0): a word whose low
+// byte is the stored byte (c + 7) & 0xFF, anchor in the high nibble and
+// residual in the low one (bits 8-31 are not defined).
+__device__ __forceinline__ uint32_t code_byte(float w, uint32_t tab_base, uint32_t stride, uint32_t one)
+{
+    const uint2 e = entry_of<0>(w, tab_base, stride);
+    return __byte_perm(e.y, 0u, byte_index(w, e.x, one));
+}
+
+// The same for the pair (w0, w1) of channels 2pi, 2pi + 1: byte 0 of the
+// result is the stored byte of w0 (A0 << 4 | r0) and byte 1 that of w1 with
+// its nibbles swapped (r1 << 4 | A1), read from the second table; the second
+// permute merges the two (selector nibble 1 = 4 takes byte 0 of b1). Then the
+// anchor byte A1 << 4 | A0 is the result shifted right by 4, and the residual
+// byte r1 << 4 | r0 one logic operation away (bits 16-31 are not defined).
+__device__ __forceinline__ uint32_t code_pair(float w0, float w1, uint32_t tab_base, uint32_t stride, uint32_t one)
+{
+    const uint2 e0 = entry_of<0>(w0, tab_base, stride);
+    const uint2 e1 = entry_of<1>(w1, tab_base, stride);
+    const uint32_t b1 = __byte_perm(e1.y, 0u, byte_index(w1, e1.x, one));
+    return __byte_perm(e0.y, b1, byte_index(w0, e0.x, one) + 0x40u);
 }
 
 // bf16x2 min / max that propagate NaN (a NaN value marks its channel)
@@ -202,12 +233,11 @@ __device__ __forceinline__ void encode_chunk(const float2 (&u)[kChunk], int nc, 
                 // w = v * inv_s, as one rounding of the product plus +0, which
                 // turns a -0 product into +0 (both code 0) and changes nothing else
                 const float2 w = __ffma2_rn(__fadd2_rn(u[i], negmu), inv_s, zero);
-                const uint32_t b0 = code_byte(w.x, tab_base, stride, one);
-                const uint32_t b1 = code_byte(w.y, tab_base, stride, one);
+                const uint32_t z = code_pair(w.x, w.y, tab_base, stride, one);
                 // low bytes: the anchors and the residuals of the pair (bits
                 // 8-31 are not stored)
-                ab[k] = ((b0 >> 4) & 0x0Fu) | (b1 & ~0x0Fu);
-                rb[k] = (b0 & 0x0Fu) | (b1 << 4);
+                ab[k] = z >> 4;
+                rb[k] = (z & 0x0Fu) | ((z >> 8) & ~0x0Fu);
             }
         }
 #pragma unroll
@@ -231,15 +261,18 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_kernel(Params p, CodeTab
     const int j = warp >> 1;                       // chunk of this warp
     const int pi = (warp & 1) * 32 + lane;         // channel pair: channels 2pi, 2pi+1
 
-    for (int i = tid; i < kNBucket * kCopies; i += kThreads)
-        sm.tab[i] = table.e[i / kCopies];
+    for (int i = tid; i < kNBucket * kCopies; i += kThreads) {
+        const uint2 e = table.e[i / kCopies];
+        sm.tab[0][i] = e;
+        sm.tab[1][i] = make_uint2(e.x, ((e.y >> 4) & 0x0F0F0F0Fu) | ((e.y << 4) & 0xF0F0F0F0u));
+    }
     if (tid == 0) {
         mbar_init(&sm.bar[0], 1);
         mbar_init(&sm.bar[1], 1);
         fence_mbar_init();
     }
     __syncthreads();
-    const uint32_t tab_base = smem_u32(&sm.tab[lane & (kCopies - 1)]) - kBucketBase * (kCopies * 8);
+    const uint32_t tab_base = smem_u32(&sm.tab[0][lane & (kCopies - 1)]) - kBucketBase * (kCopies * 8);
 
     const int64_t first = blockIdx.x, stride = gridDim.x;
     if (tid == 0 && first < p.pages) {
@@ -259,12 +292,6 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_kernel(Params p, CodeTab
             prefetched = true;
         }
         const bool ok = mbar_wait_bounded(&sm.bar[buf], (uint32_t)(k >> 1) & 1u, kWaitLimit);
-        if (__syncthreads_or(!ok)) {
-            // the copy never landed: stop, after letting any copy in flight finish
-            if (tid == 0 && prefetched)
-                mbar_wait_bounded(&sm.bar[buf ^ 1], (uint32_t)((k + 1) >> 1) & 1u, kWaitLimit);
-            break;
-        }
 
         const int n = valid_of(p, page);
         const int64_t dst = dst_of(p, page);
@@ -297,7 +324,14 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_kernel(Params p, CodeTab
         sm.pmax[j][pi] = cmx2;
         if (tid == 0)
             bulk_wait_read_all();   // the previous page's planes have left the staging tile
-        __syncthreads();
+        // (a thread whose wait gave up read a page that never landed; nothing
+        // of it is used)
+        if (__syncthreads_or(!ok)) {
+            // the copy never landed: stop, after letting any copy in flight finish
+            if (tid == 0 && prefetched)
+                mbar_wait_bounded(&sm.bar[buf ^ 1], (uint32_t)((k + 1) >> 1) & 1u, kWaitLimit);
+            break;
+        }
 
         // (b) stage 1 over the page
         uint32_t mn2 = sm.pmin[0][pi], mx2 = sm.pmax[0][pi];
@@ -394,9 +428,10 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_kernel(Params p, CodeTab
 }
 
 // The encoder's stage-3 path on arbitrary values (a diagnostic): the same
-// table and code_byte(), with |w| clamped below 2, -0 turned into +0 and NaN
-// into 0 first, so that any input stays inside the table (the encoder itself
-// sees only finite w with |w| <= 1 + 2^-23, never -0).
+// table and code_byte(), with |w| clamped to 1.5 (every |w| >= T_63 < 1 has
+// the same code), -0 turned into +0 and NaN into 0 first, so that any input
+// stays inside the table (the encoder itself sees only finite w with
+// |w| <= 1 + 2^-23, never -0).
 __global__ void level_codes_kernel(const float *__restrict__ w, int64_t n, int8_t *__restrict__ codes,
                                    CodeTable table)
 {
@@ -407,7 +442,7 @@ __global__ void level_codes_kernel(const float *__restrict__ w, int64_t n, int8_
     const uint32_t tab_base = smem_u32(&tab[threadIdx.x & (kCopies - 1)]) - kBucketBase * (kCopies * 8);
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
         const float v = w[i];
-        const float c = v == v ? __fadd_rn(copysignf(fminf(fabsf(v), 1.99999988f), v), 0.0f) : 0.0f;
+        const float c = v == v ? __fadd_rn(copysignf(fminf(fabsf(v), 1.5f), v), 0.0f) : 0.0f;
         codes[i] = (int8_t)((int)(int8_t)code_byte(c, tab_base, kCopies * 8, 1u) - kBias);
     }
 }
