@@ -166,13 +166,20 @@ __device__ __forceinline__ float exp2_sm(float x)
     return y;
 }
 
-// (x0, x1) -> fp16 pairs hi and lo with hi + lo = (x0, x1) to ~22 bits.
+// (x0, x1) -> fp16 pairs hi and lo with hi + lo = (x0, x1) to ~22 bits. The
+// remainders x - hi are exact in fp32; each comes from one mixed-precision
+// multiply-add (fp16 operands, fp32 addend and result), with no separate
+// widening of hi.
 __device__ __forceinline__ void split2(float2 x, uint32_t &hi, uint32_t &lo)
 {
     const __half2 h = __floats2half2_rn(x.x, x.y);
-    const float2 r = __ffma2_rn(__half22float2(h), make_float2(-1.0f, -1.0f), x);
-    const __half2 l = __floats2half2_rn(r.x, r.y);
     hi = *reinterpret_cast<const uint32_t *>(&h);
+    float r0, r1;
+    asm("{\n\t.reg .b16 h0, h1, m1;\n\tmov.b32 {h0, h1}, %2;\n\tmov.b16 m1, 0xBC00;\n\t"
+        "fma.rn.f32.f16 %0, h0, m1, %3;\n\tfma.rn.f32.f16 %1, h1, m1, %4;\n\t}"
+        : "=f"(r0), "=f"(r1)
+        : "r"(hi), "f"(x.x), "f"(x.y));
+    const __half2 l = __floats2half2_rn(r0, r1);
     lo = *reinterpret_cast<const uint32_t *>(&l);
 }
 
