@@ -18,16 +18,19 @@
 // integer add and one byte permute; the odd channel of a pair reads a second
 // table with the nibbles of each byte swapped, so that one more permute
 // merges the pair and the two plane bytes are a shift and a logic operation
-// away. The packed planes are staged in shared memory
-// and leave with two 16 KiB bulk stores; the metadata goes out with direct
-// 4/8-byte stores.
+// away. The packed planes are staged in shared memory and leave with two
+// 16 KiB bulk stores; the metadata goes out with direct 4/8-byte stores.
+// Two barriers a page: after the chunk extremes (which also carries the
+// outcome of the bounded wait for the page) and before the bulk stores.
 //
 // The kernel is bound by instruction issue, so the per-element work is kept
 // short: the bucket index needs no clamp (|w| + 2^-13 always lands in the
 // table), the threshold test and the sign of w come out of one integer add
 // as the byte index, and the chunk's max |v| comes from its two extremes
 // instead of a max over all elements (v is a monotone function of x, so the
-// extremes of x give the extremes of v).
+// extremes of x give the extremes of v). Storing the planes straight to
+// global memory (no staging, one barrier a page) needs fewer instructions
+// but stalls on the load/store unit and runs slower.
 // Codes are computed for a group of tokens before the group's stores: a table
 // load may not move above an earlier store to shared memory, so interleaving
 // them would serialise the tokens.
