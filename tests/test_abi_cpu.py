@@ -234,3 +234,44 @@ def test_dense_attn_rejects_bad_arguments(lx):
     assert call(q=ctypes.c_void_p(0x400001)) == lx.ERR_ALIGN
     assert call(B=0) == lx.OK                                # nothing to do, no launch
     assert call(Hq=0, q=None) == lx.OK
+
+
+def test_stage3_integer_index_scheme(lx, orc):
+    """The encoder's stage-3 lookup, emulated from the library's thresholds:
+    16 buckets per octave of |w| + 2^-13 hold at most one threshold T*, and
+    bits 31-30 of bits(w) + (2^30 - bits(T*)) (0 when a bucket holds none) are
+    2 sign(w) + (|w| >= T*), the index of the stored code among the four an
+    entry carries. The result is compared with the oracle's direct count of
+    thresholds, near every threshold (both signs, 64 fp32 steps each side),
+    at every bucket edge, and on a dense uniform sample of [-1, 1]."""
+    thr, _ = lx.host_tables()
+    thr = np.asarray(thr, np.float32)
+    off = np.float32(2.0 ** -13)
+    base = (127 - 13) << 4
+
+    def bucket(a):
+        return ((np.asarray(a, np.float32) + off).view(np.uint32) >> 19).astype(np.int64) - base
+
+    tb = bucket(thr[1:])
+    nb = 14 * 16
+    assert tb.min() >= 0 and tb.max() < nb
+    assert len(np.unique(tb)) == len(tb)       # at most one threshold per bucket
+    q0 = np.searchsorted(np.sort(tb), np.arange(nb), side="left")   # thresholds in lower buckets
+    k_add = np.zeros(nb, np.uint64)
+    k_add[tb] = (1 << 30) - thr[1:].view(np.uint32).astype(np.uint64)
+    q1 = np.minimum(q0 + 1, 63)
+    entry = np.stack([q0, q1, -np.maximum(q0, 1), -np.maximum(q1, 1)], axis=1)
+
+    near = (thr[1:].view(np.int32)[:, None] + np.arange(-64, 65)[None, :]).ravel().view(np.float32)
+    edges = ((np.arange(nb, dtype=np.uint32) + base) << 19).view(np.float32) - off
+    edges = np.concatenate([edges, np.nextafter(edges, np.float32(0)), np.nextafter(edges, np.float32(2))])
+    edges = edges[(edges >= 0) & (edges <= 1)]
+    rng = np.random.default_rng(7)
+    mag = np.concatenate([near, edges, rng.random(1 << 20, dtype=np.float32), np.float32([0.0, 1.0])])
+    w = np.concatenate([mag, -mag[mag > 0]]).astype(np.float32)
+
+    b = bucket(np.abs(w))
+    assert b.min() >= 0 and b.max() < nb
+    t = (w.view(np.uint32).astype(np.uint64) + k_add[b]) & 0xFFFFFFFF
+    got = entry[b, (t >> 30).astype(np.int64)]
+    assert np.array_equal(got, orc.codes(w).astype(np.int64))
