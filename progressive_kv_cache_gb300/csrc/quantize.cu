@@ -50,7 +50,8 @@ constexpr uint32_t kPlaneBytes = kPage * kD / 2;      // 16 KiB per plane and pa
 constexpr uint32_t kTabBytes = kNBucket * kCopies * 8; // one replicated table
 constexpr uint32_t kWaitLimit = 1u << 22;
 constexpr uint32_t kQNaN = 0x7FC00000u;
-constexpr int kGroup = 16;                           // tokens whose codes are computed before their stores
+constexpr int kGroup = 8;                            // tokens whose codes are computed before their stores
+                                                     // (measured: 8 runs 2.5 % faster than 16 or 32, 1.5 % than 4)
 static_assert(kGroup > 0 && kChunk % kGroup == 0, "groups must tile the chunk");
 constexpr float kF32Max = 3.40282347e38f;
 
