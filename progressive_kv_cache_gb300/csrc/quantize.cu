@@ -60,8 +60,7 @@ struct Smem {
     uint16_t x[2][kPage * kD];         // double-buffered input page
     uint8_t anc[kPage * kD / 2];       // staged anchor plane of the page
     uint8_t res[kPage * kD / 2];       // staged residual plane of the page
-    uint32_t pmin[kNChunk][kD / 2];    // bf16x2 chunk minima of channel pairs
-    uint32_t pmax[kNChunk][kD / 2];
+    uint2 pmm[kNChunk][kD / 2];        // bf16x2 chunk (minima, maxima) of channel pairs
     // [0]: the stored bytes; [1]: the same bytes with their nibbles swapped
     // (the odd channel of a pair)
     uint2 tab[2][kNBucket * kCopies];
@@ -324,8 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_kernel(Params p, CodeTab
                     cmx2 = bf2_max(cmx2, xw[i]);
                 }
         }
-        sm.pmin[j][pi] = cmn2;
-        sm.pmax[j][pi] = cmx2;
+        sm.pmm[j][pi] = make_uint2(cmn2, cmx2);
         if (tid == 0)
             bulk_wait_read_all();   // the previous page's planes have left the staging tile
         // (a thread whose wait gave up read a page that never landed; nothing
@@ -338,11 +336,12 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_kernel(Params p, CodeTab
         }
 
         // (b) stage 1 over the page
-        uint32_t mn2 = sm.pmin[0][pi], mx2 = sm.pmax[0][pi];
+        uint32_t mn2 = sm.pmm[0][pi].x, mx2 = sm.pmm[0][pi].y;
 #pragma unroll
         for (int jj = 1; jj < kNChunk; ++jj) {
-            mn2 = bf2_min(mn2, sm.pmin[jj][pi]);
-            mx2 = bf2_max(mx2, sm.pmax[jj][pi]);
+            const uint2 e = sm.pmm[jj][pi];
+            mn2 = bf2_min(mn2, e.x);
+            mx2 = bf2_max(mx2, e.y);
         }
         float mn0 = bf16_lo(mn2), mn1 = bf16_hi(mn2), mx0 = bf16_lo(mx2), mx1 = bf16_hi(mx2);
         if (n == 0)
