@@ -178,6 +178,21 @@ __device__ __forceinline__ float2 sub_bf2(uint32_t x, float2 negm)
     return make_float2(r0, r1);
 }
 
+// 1/s, correctly rounded, for the chunk scale s: an fp16 value (an 11-bit
+// significand, 2^-24 <= s < 2). The hardware approximation r, then one Newton
+// step written as two fused multiply-adds, r + r (1 - s r). With an 11-bit
+// significand the exact 1/s = 2^k / M (M < 2^11) lies at least 2^-35
+// (relative) from any midpoint between two fp32 values, while the step leaves
+// an error near (1 - s r)^2 <= 2^-44, so the final rounding is the correct
+// one (checked exhaustively for every positive fp16 value and every starting
+// point within 2 ulp).
+__device__ __forceinline__ float rcp_of_fp16(float s)
+{
+    float r;
+    asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(s));
+    return __fmaf_rn(r, __fmaf_rn(-s, r, 1.0f), r);
+}
+
 // Stages 2-4 for this thread's two channels of one chunk, held as float2
 // lanes (x = channel 2pi, y = channel 2pi + 1) so that each packed fp32
 // instruction performs the contract's operation for both channels (every lane
@@ -219,7 +234,7 @@ __device__ __forceinline__ void encode_chunk(const float2 (&u)[kChunk], int nc, 
     const float s0 = fmaxf(fabsf(vlo.x), fabsf(vhi.x)), s1 = fmaxf(fabsf(vlo.y), fabsf(vhi.y));
     const __half sh0 = __float2half_ru(s0), sh1 = __float2half_ru(s1);
     const float sf0 = __half2float(sh0), sf1 = __half2float(sh1);
-    const float2 inv_s = make_float2(sf0 > 0.0f ? __frcp_rn(sf0) : 0.0f, sf1 > 0.0f ? __frcp_rn(sf1) : 0.0f);
+    const float2 inv_s = make_float2(sf0 > 0.0f ? rcp_of_fp16(sf0) : 0.0f, sf1 > 0.0f ? rcp_of_fp16(sf1) : 0.0f);
 
     // groups of kGroup tokens: all lookups of a group, then its stores (a
     // table load may not move above an earlier store to shared memory, so
