@@ -224,8 +224,8 @@ __device__ __forceinline__ void encode_chunk(const float2 (&u)[kChunk], int nc, 
         const float ncf = (float)nc;
         mean = make_float2(__fdiv_rn(t[0].x, ncf), __fdiv_rn(t[0].y, ncf));
     }
-    const __half mh0 = __float2half_rn(mean.x);
-    const __half mh1 = __float2half_rn(mean.y);
+    const __half2 mh = __floats2half2_rn(mean.x, mean.y);   // one packed conversion
+    const __half mh0 = __low2half(mh), mh1 = __high2half(mh);
     const float2 negmu = make_float2(-__half2float(mh0), -__half2float(mh1));
 
     // max |v| over the chunk: v = u - mu is non-decreasing in u, so it is
@@ -303,7 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_kernel(Params p, CodeTab
         const int buf = k & 1;
         const int64_t next = page + stride;
         bool prefetched = false;
-        if (tid == 0 && next < p.pages) {
+        if (warp == 0 && lane == 0 && next < p.pages) {
             fence_proxy_async_smem();
             mbar_arrive_expect_tx(&sm.bar[buf ^ 1], kPageBytes);
             bulk_g2s(sm.x[buf ^ 1], p.x + next * (int64_t)(kPage * kD), kPageBytes, &sm.bar[buf ^ 1]);
@@ -339,7 +339,7 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_kernel(Params p, CodeTab
                 }
         }
         sm.pmm[j][pi] = make_uint2(cmn2, cmx2);
-        if (tid == 0)
+        if (warp == 0 && lane == 0)
             bulk_wait_read_all();   // the previous page's planes have left the staging tile
         // (a thread whose wait gave up read a page that never landed; nothing
         // of it is used)
@@ -438,7 +438,7 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_kernel(Params p, CodeTab
         // fence lies on the causality path from each write to the copy); a
         // fence in every thread before the barrier costs 1.7 %
         __syncthreads();
-        if (tid == 0 && dst >= 0) {
+        if (warp == 0 && lane == 0 && dst >= 0) {
             fence_proxy_async_smem();
             bulk_s2g(p.anc + dst * (int64_t)kPlaneBytes, sm.anc, kPlaneBytes);
             bulk_s2g(p.res + dst * (int64_t)kPlaneBytes, sm.res, kPlaneBytes);
