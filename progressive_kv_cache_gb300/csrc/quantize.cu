@@ -145,8 +145,11 @@ __device__ __forceinline__ uint32_t code_byte(float w, uint32_t tab_base, uint32
 // byte r1 << 4 | r0 one logic operation away (bits 16-31 are not defined).
 __device__ __forceinline__ uint32_t code_pair(float w0, float w1, uint32_t tab_base, uint32_t stride, uint32_t one)
 {
-    const uint2 e0 = entry_of<0>(w0, tab_base, stride);
-    const uint2 e1 = entry_of<1>(w1, tab_base, stride);
+    // both buckets' sums |w| + 2^-13 in one packed add (each lane one IEEE add)
+    const float off = __uint_as_float(kBucketOffsetBits);
+    const float2 sum = __fadd2_rn(make_float2(fabsf(w0), fabsf(w1)), make_float2(off, off));
+    const uint2 e0 = lds_u2((__float_as_uint(sum.x) >> 19) * stride + tab_base);
+    const uint2 e1 = lds_u2((__float_as_uint(sum.y) >> 19) * stride + tab_base + kTabBytes);
     const uint32_t b1 = __byte_perm(e1.y, 0u, byte_index(w1, e1.x, one));
     return __byte_perm(e0.y, b1, byte_index(w0, e0.x, one) + 0x40u);
 }
