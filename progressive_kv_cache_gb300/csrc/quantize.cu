@@ -364,11 +364,14 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_kernel(Params p, CodeTab
         float mn0 = bf16_lo(mn2), mn1 = bf16_hi(mn2), mx0 = bf16_lo(mx2), mx1 = bf16_hi(mx2);
         if (n == 0)
             mn0 = mn1 = mx0 = mx1 = 0.0f;
-        mn0 = __fadd_rn(mn0, 0.0f);   // a zero extreme is +0
-        mn1 = __fadd_rn(mn1, 0.0f);
-        mx0 = __fadd_rn(mx0, 0.0f);
-        mx1 = __fadd_rn(mx1, 0.0f);
-        float rg0 = __fsub_rn(mx0, mn0), rg1 = __fsub_rn(mx1, mn1);
+        // a zero extreme is +0 (each lane of the packed operations is one
+        // IEEE operation, and x - y is x + (-y))
+        const float2 mnz = __fadd2_rn(make_float2(mn0, mn1), make_float2(0.0f, 0.0f));
+        const float2 mxz = __fadd2_rn(make_float2(mx0, mx1), make_float2(0.0f, 0.0f));
+        mn0 = mnz.x;
+        mn1 = mnz.y;
+        const float2 rg2 = __fadd2_rn(mxz, make_float2(-mnz.x, -mnz.y));
+        float rg0 = rg2.x, rg1 = rg2.y;
         // a NaN value (min and max NaN) stores min and range as the quiet NaN;
         // so does any NaN range
         if (mn0 != mn0)
