@@ -72,6 +72,32 @@ def test_group_16_block_of_64(lx, orc, mode):
 
 
 @pytest.mark.parametrize("mode", [0, 1])
+def test_report_shape_sampled_positions(lx, orc, mode):
+    """The verify report's workload and launch configuration: 4 KV heads x 32K
+    tokens, 64 query heads, 64 draft positions (eight row blocks x four page
+    ranges of 32 pages). Sampled positions are checked against the oracle's
+    decode step over each one's visible prefix, which is what the oracle's
+    verify attention computes position by position."""
+    w = S.WORKLOADS[2]
+    cache = _cache(lx, orc, w, 1, w.H, w.T)
+    (kq, kr), (vq, vr) = cache[S.S_K], cache[S.S_V]
+    Tq, Hq = 64, 64
+    qb = _queries(w, 1, Tq, Hq)
+    table = np.arange(w.pages, dtype=np.int32)[None]
+    ctx = np.array([w.T])
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = lx.verify_attn(bf16_dev(qb), kq, vq, 0, i32_dev(table), i32_dev(ctx), 128 ** -0.5, mode,
+                         dev_err=err).cpu().numpy()
+    assert int(err.item()) == 0
+    full = mode == lx.MODE_FULL
+    for i in (0, 21, 63):
+        n = ctx - Tq + i + 1
+        ref = orc.decode_attn(qb[:, i], kr, vr, 0, table, n, 128 ** -0.5, full)
+        E = attn_sensitivity(orc, qb[:, i], kr, vr, 0, table, n, 128 ** -0.5, full)
+        assert_attn_close(out[:, i], ref, E, f"verify 32K position {i} mode {mode}")
+
+
+@pytest.mark.parametrize("mode", [0, 1])
 def test_batched_ragged_permuted(lx, orc, mode):
     """The batched-decode layout (ragged contexts, permuted pages, 8 KV heads x
     8 query heads each) for 6 of its requests, 16 draft positions."""
