@@ -114,6 +114,9 @@ typedef struct {
  *               invalid tokens store code 0 (anchor 0, residual 7). Counts
  *               outside 0..256 are clamped.
  *   out         planes and metadata written; residual must be non-NULL.
+ * Returns LYNX_ERR_UNSUPPORTED when layers * kv_heads * tokens / 256 exceeds
+ * 2^31 / 256 pages (the kernel addresses rows with 32-bit tile coordinates)
+ * or the driver provides no tensor-map encoder.
  */
 lynx_status lynx_quantize_pages(const void *x_bf16, const int32_t *page_valid, const lynx_qkv *out,
                                 void *stream);
@@ -135,6 +138,8 @@ lynx_status lynx_quantize_pages(const void *x_bf16, const int32_t *page_valid, c
  *              (residual non-NULL); only the destination pages are written
  *   dev_err    device or NULL, one uint32
  * Tails naming the same physical page race on it: pass distinct pages.
+ * Returns LYNX_ERR_UNSUPPORTED under the same limits as lynx_quantize_pages
+ * (for the n tails' pages and for the pool's).
  */
 lynx_status lynx_quantize_append(const void *tail_bf16, const int32_t *phys_page, const int32_t *valid,
                                  int32_t n, const lynx_qkv *out, uint32_t *dev_err, void *stream);

@@ -7,21 +7,27 @@
 // alpha-law log map onto 127 levels with sign-aware mapping of negatives;
 // (4) the +7 round-half-down bias and the 4-bit anchor / 4-bit residual cut.
 //
-// Layout of the work: a persistent CTA (one per SM, 16 warps) walks pages;
-// each page (256 x 128 bf16 = 64 KiB, contiguous in [L][H][T][128]) is
-// prefetched into one of two shared-memory buffers with a single bulk copy
-// while the previous page is encoded. Warp w owns chunk w/2 (32 tokens) and
-// half the channels; lane l owns one channel pair, so the chunk reduction tree
+// Layout of the work: the unit of work is one channel half of a page (256
+// tokens x 64 channels; the statistics are per channel, so the two halves of
+// a page are independent). Persistent CTAs of 8 warps, two per SM, walk the
+// units; a unit arrives by one 2D tensor copy (TMA, rows of 128 bytes out of
+// the page's 256) into a single input buffer, which is refilled with the next
+// unit as soon as the current one is in registers, and the two CTAs of an SM
+// run out of step, so that one's barriers and latency-bound stretches overlap
+// the other's stage 3 (one 16-warp CTA per page with a double-buffered input
+// keeps all warps in the same phase and runs 1.8 % slower). Warp w owns chunk
+// w (32 tokens); lane l owns one channel pair, so the chunk reduction tree
 // of the numeric contract runs inside one thread's registers. Stage 3 is one
 // lookup in a 16-way replicated bucket table (a conflict-free 8-byte load per
 // element) whose entry carries the four possible stored bytes, then one
 // integer add and one byte permute; the odd channel of a pair reads a second
 // table with the nibbles of each byte swapped, so that one more permute
 // merges the pair and the two plane bytes are a shift and a logic operation
-// away. The packed planes are staged in shared memory and leave with two
-// 16 KiB bulk stores; the metadata goes out with direct 4/8-byte stores.
-// Two barriers a page: after the chunk extremes (which also carries the
-// outcome of the bounded wait for the page) and before the bulk stores.
+// away. The packed planes are staged in shared memory and leave with two 2D
+// tensor stores of 8 KiB (256 rows of 32 bytes); the metadata goes out with
+// direct 4/8-byte stores. Two barriers a unit: after the chunk extremes (which
+// also carries the outcome of the bounded wait for the unit) and before the
+// tensor stores.
 //
 // The kernel is bound by instruction issue, so the per-element work is kept
 // short: the bucket index needs no clamp (|w| + 2^-13 always lands in the
@@ -36,6 +42,11 @@
 // them would serialise the tokens.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <climits>
+#include <mutex>
 
 #include "lynx_internal.cuh"
 #include "lynx_ptx.cuh"
@@ -43,28 +54,30 @@
 namespace lynx {
 namespace {
 
-constexpr int kThreads = 512;
+constexpr int kHalf = kD / 2;                          // channels of one work unit
+constexpr int kRowB = kHalf / 2;                       // plane bytes of one token in a unit
+constexpr int kThreads = kNChunk * 32;                 // a warp per chunk, a lane per channel pair
 constexpr int kCopies = 16;                            // table replicas (one per half-warp lane)
-constexpr uint32_t kPageBytes = kPage * kD * 2;       // 64 KiB of bf16
-constexpr uint32_t kPlaneBytes = kPage * kD / 2;      // 16 KiB per plane and page
+constexpr uint32_t kUnitBytes = kPage * kHalf * 2;    // 32 KiB of bf16
 constexpr uint32_t kTabBytes = kNBucket * kCopies * 8; // one replicated table
 constexpr uint32_t kWaitLimit = 1u << 22;
 constexpr uint32_t kQNaN = 0x7FC00000u;
-constexpr int kGroup = 8;                            // tokens whose codes are computed before their stores
-                                                     // (measured: 8 runs 2.5 % faster than 16 or 32, 1.5 % than 4)
+constexpr int kGroup = 16;                           // tokens whose codes are computed before their stores
+                                                     // (measured: 16 runs 0.7 % faster than 8, 0.5 % than 32
+                                                     // and 3.2 % than 4)
 static_assert(kGroup > 0 && kChunk % kGroup == 0, "groups must tile the chunk");
 constexpr float kF32Max = 3.40282347e38f;
 
 
 struct Smem {
-    uint16_t x[2][kPage * kD];         // double-buffered input page
-    uint8_t anc[kPage * kD / 2];       // staged anchor plane of the page
-    uint8_t res[kPage * kD / 2];       // staged residual plane of the page
-    uint2 pmm[kNChunk][kD / 2];        // bf16x2 chunk (minima, maxima) of channel pairs
+    uint16_t x[kPage * kHalf];         // the unit's input: 256 tokens x 64 channels
+    uint8_t anc[kPage * kRowB];        // staged anchor plane of the unit
+    uint8_t res[kPage * kRowB];        // staged residual plane of the unit
+    uint2 pmm[kNChunk][kHalf / 2];     // bf16x2 chunk (minima, maxima) of channel pairs
     // [0]: the stored bytes; [1]: the same bytes with their nibbles swapped
     // (the odd channel of a pair)
     uint2 tab[2][kNBucket * kCopies];
-    alignas(8) uint64_t bar[2];
+    alignas(8) uint64_t bar;
 };
 
 struct Params {
@@ -263,24 +276,51 @@ __device__ __forceinline__ void encode_chunk(const float2 (&u)[kChunk], int nc, 
         }
 #pragma unroll
         for (int k = 0; k < kGroup; ++k) {
-            anc_row0[(g0 + k) * (kD / 2)] = (uint8_t)ab[k];
-            res_row0[(g0 + k) * (kD / 2)] = (uint8_t)rb[k];
+            anc_row0[(g0 + k) * kRowB] = (uint8_t)ab[k];
+            res_row0[(g0 + k) * kRowB] = (uint8_t)rb[k];
         }
     }
     mu2 = (uint32_t)__half_as_ushort(mh0) | ((uint32_t)__half_as_ushort(mh1) << 16);
     s2 = (uint32_t)__half_as_ushort(sh0) | ((uint32_t)__half_as_ushort(sh1) << 16);
 }
 
+// One 2D tiled tensor copy global -> shared, completing on an mbarrier
+// (coordinates: innermost first, in elements).
+__device__ __forceinline__ void tile_g2s(void *dst, const CUtensorMap *map, int c0, int c1, uint64_t *bar)
+{
+    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+                 "%3}], [%4];" ::"r"(smem_u32(dst)),
+                 "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+                 : "memory");
+}
+
+// One 2D tiled tensor copy shared -> global, tracked by the issuing thread's
+// bulk groups.
+__device__ __forceinline__ void tile_s2g(const CUtensorMap *map, int c0, int c1, const void *src)
+{
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c0), "r"(c1), "r"(smem_u32(src))
+                 : "memory");
+}
+
+// Work unit u = (page u / 2, channel half u % 2). A CTA of 8 warps takes
+// units blockIdx.x, blockIdx.x + gridDim.x, ...; two CTAs share an SM and run
+// out of step, so that one's barrier and latency-bound stretches (the chunk
+// extremes, the page statistics) overlap the other's stage 3. The input
+// buffer is refilled with the next unit as soon as every value of the current
+// one is in registers (after the first barrier).
 // tab_stride: kCopies * 8, and one: 1, passed at run time (see code_byte)
-__global__ void __launch_bounds__(kThreads, 1) quantize_kernel(Params p, CodeTable table, uint32_t tab_stride,
-                                                               uint32_t one)
+__global__ void __launch_bounds__(kThreads, 2) quantize_kernel(Params p, const __grid_constant__ CUtensorMap xmap,
+                                                               const __grid_constant__ CUtensorMap amap,
+                                                               const __grid_constant__ CUtensorMap rmap,
+                                                               CodeTable table, uint32_t tab_stride, uint32_t one)
 {
     extern __shared__ __align__(128) unsigned char smem_raw[];
     Smem &sm = *reinterpret_cast<Smem *>(smem_raw);
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
-    const int j = warp >> 1;                       // chunk of this warp
-    const int pi = (warp & 1) * 32 + lane;         // channel pair: channels 2pi, 2pi+1
+    const int j = warp;                            // chunk of this warp; lane: channel pair of the half
 
     for (int i = tid; i < kNBucket * kCopies; i += kThreads) {
         const uint2 e = table.e[i / kCopies];
@@ -288,31 +328,25 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_kernel(Params p, CodeTab
         sm.tab[1][i] = make_uint2(e.x, ((e.y >> 4) & 0x0F0F0F0Fu) | ((e.y << 4) & 0xF0F0F0F0u));
     }
     if (tid == 0) {
-        mbar_init(&sm.bar[0], 1);
-        mbar_init(&sm.bar[1], 1);
+        mbar_init(&sm.bar, 1);
         fence_mbar_init();
     }
     __syncthreads();
     const uint32_t tab_base = smem_u32(&sm.tab[0][lane & (kCopies - 1)]) - kBucketBase * (kCopies * 8);
 
+    const int64_t units = 2 * p.pages;
     const int64_t first = blockIdx.x, stride = gridDim.x;
-    if (tid == 0 && first < p.pages) {
-        mbar_arrive_expect_tx(&sm.bar[0], kPageBytes);
-        bulk_g2s(sm.x[0], p.x + first * (int64_t)(kPage * kD), kPageBytes, &sm.bar[0]);
+    if (tid == 0 && first < units) {
+        mbar_arrive_expect_tx(&sm.bar, kUnitBytes);
+        tile_g2s(sm.x, &xmap, (int)(first & 1) * kHalf, (int)(first >> 1) * kPage, &sm.bar);
     }
 
     int k = 0;
-    for (int64_t page = first; page < p.pages; page += stride, ++k) {
-        const int buf = k & 1;
-        const int64_t next = page + stride;
-        bool prefetched = false;
-        if (warp == 0 && lane == 0 && next < p.pages) {
-            fence_proxy_async_smem();
-            mbar_arrive_expect_tx(&sm.bar[buf ^ 1], kPageBytes);
-            bulk_g2s(sm.x[buf ^ 1], p.x + next * (int64_t)(kPage * kD), kPageBytes, &sm.bar[buf ^ 1]);
-            prefetched = true;
-        }
-        const bool ok = mbar_wait_bounded(&sm.bar[buf], (uint32_t)(k >> 1) & 1u, kWaitLimit);
+    for (int64_t unit = first; unit < units; unit += stride, ++k) {
+        const int64_t page = unit >> 1, next = unit + stride;
+        const int half = (int)(unit & 1);
+        const int pi = half * (kHalf / 2) + lane;  // channel pair of the page: channels 2pi, 2pi+1
+        const bool ok = mbar_wait_bounded(&sm.bar, (uint32_t)k & 1u, kWaitLimit);
 
         const int n = valid_of(p, page);
         const int64_t dst = dst_of(p, page);
@@ -321,11 +355,11 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_kernel(Params p, CodeTab
         const int nc = min(max(n - j * kChunk, 0), kChunk);
 
         // (a) this thread's 32 tokens x 2 channels, and their chunk min/max
-        const uint16_t *xs = sm.x[buf] + j * kChunk * kD + 2 * pi;
+        const uint16_t *xs = sm.x + j * kChunk * kHalf + 2 * lane;
         uint32_t xw[kChunk];
 #pragma unroll
         for (int i = 0; i < kChunk; ++i)
-            xw[i] = *reinterpret_cast<const uint32_t *>(xs + i * kD);
+            xw[i] = *reinterpret_cast<const uint32_t *>(xs + i * kHalf);
         uint32_t cmn2 = 0x7F807F80u, cmx2 = 0xFF80FF80u;   // +inf, -inf pairs
         if (nc == kChunk) {
 #pragma unroll
@@ -341,23 +375,31 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_kernel(Params p, CodeTab
                     cmx2 = bf2_max(cmx2, xw[i]);
                 }
         }
-        sm.pmm[j][pi] = make_uint2(cmn2, cmx2);
+        sm.pmm[j][lane] = make_uint2(cmn2, cmx2);
         if (warp == 0 && lane == 0)
-            bulk_wait_read_all();   // the previous page's planes have left the staging tile
-        // (a thread whose wait gave up read a page that never landed; nothing
+            bulk_wait_read_all();   // the previous unit's planes have left the staging tile
+        // (a thread whose wait gave up read a unit that never landed; nothing
         // of it is used)
         if (__syncthreads_or(!ok)) {
-            // the copy never landed: stop, after letting any copy in flight finish
-            if (tid == 0 && prefetched)
-                mbar_wait_bounded(&sm.bar[buf ^ 1], (uint32_t)((k + 1) >> 1) & 1u, kWaitLimit);
+            // the copy never landed: stop, after waiting once more for it
+            if (tid == 0)
+                mbar_wait_bounded(&sm.bar, (uint32_t)k & 1u, kWaitLimit);
             break;
         }
+        // every value of the unit is in registers: refill the buffer with the
+        // next unit (the reads reach thread 0 through the barrier; its proxy
+        // fence orders them before the copy's writes)
+        if (warp == 0 && lane == 0 && next < units) {
+            fence_proxy_async_smem();
+            mbar_arrive_expect_tx(&sm.bar, kUnitBytes);
+            tile_g2s(sm.x, &xmap, (int)(next & 1) * kHalf, (int)(next >> 1) * kPage, &sm.bar);
+        }
 
-        // (b) stage 1 over the page
-        uint32_t mn2 = sm.pmm[0][pi].x, mx2 = sm.pmm[0][pi].y;
+        // (b) stage 1 over the unit's page
+        uint32_t mn2 = sm.pmm[0][lane].x, mx2 = sm.pmm[0][lane].y;
 #pragma unroll
         for (int jj = 1; jj < kNChunk; ++jj) {
-            const uint2 e = sm.pmm[jj][pi];
+            const uint2 e = sm.pmm[jj][lane];
             mn2 = bf2_min(mn2, e.x);
             mx2 = bf2_max(mx2, e.y);
         }
@@ -413,8 +455,8 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_kernel(Params p, CodeTab
         }
 
         // (c) stages 2-4
-        uint8_t *anc_row0 = sm.anc + j * kChunk * (kD / 2) + pi;
-        uint8_t *res_row0 = sm.res + j * kChunk * (kD / 2) + pi;
+        uint8_t *anc_row0 = sm.anc + j * kChunk * kRowB + lane;
+        uint8_t *res_row0 = sm.res + j * kChunk * kRowB + lane;
         uint32_t mu2 = 0, s2 = 0;
         if (nc == kChunk) {
             encode_chunk<true>(u, nc, ulo, uhi, tab_base, tab_stride, one, anc_row0, res_row0, mu2, s2);
@@ -423,12 +465,12 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_kernel(Params p, CodeTab
         } else {
 #pragma unroll
             for (int i = 0; i < kChunk; ++i) {
-                anc_row0[i * (kD / 2)] = 0x00u;
-                res_row0[i * (kD / 2)] = 0x77u;
+                anc_row0[i * kRowB] = 0x00u;
+                res_row0[i * kRowB] = 0x77u;
             }
         }
 
-        // metadata: page (min, range) from chunk 0's warps; chunk (mean, scale) from every thread
+        // metadata: page (min, range) from chunk 0's warp; chunk (mean, scale) from every thread
         if (j == 0 && dst >= 0) {
             float *pm = p.pm + dst * (int64_t)(2 * kD) + 2 * pi;
             *reinterpret_cast<float2 *>(pm) = make_float2(mn0, mn1);
@@ -440,14 +482,13 @@ __global__ void __launch_bounds__(kThreads, 1) quantize_kernel(Params p, CodeTab
             *reinterpret_cast<uint32_t *>(cm + kD) = s2;
         }
         // every thread's plane bytes reach thread 0 through the barrier, and
-        // its proxy fence then orders them before the bulk copies' reads (the
-        // fence lies on the causality path from each write to the copy); a
-        // fence in every thread before the barrier costs 1.7 %
+        // its proxy fence then orders them before the tensor copies' reads
+        // (the fence lies on the causality path from each write to the copy)
         __syncthreads();
         if (warp == 0 && lane == 0 && dst >= 0) {
             fence_proxy_async_smem();
-            bulk_s2g(p.anc + dst * (int64_t)kPlaneBytes, sm.anc, kPlaneBytes);
-            bulk_s2g(p.res + dst * (int64_t)kPlaneBytes, sm.res, kPlaneBytes);
+            tile_s2g(&amap, half * kRowB, (int)dst * kPage, sm.anc);
+            tile_s2g(&rmap, half * kRowB, (int)dst * kPage, sm.res);
             bulk_commit();
         }
     }
@@ -475,19 +516,81 @@ __global__ void level_codes_kernel(const float *__restrict__ w, int64_t n, int8_
     }
 }
 
-cudaError_t run_quantize(const Params &p, cudaStream_t s)
+// cuTensorMapEncodeTiled, through the runtime's driver entry point (no link
+// against the driver library); NULL when the driver does not provide it.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+// A 2D row-major map of `rows` rows of `width` elements, copied in boxes of
+// box_w x 256 rows (no swizzle, no interleave).
+bool encode_rows(PFN_cuTensorMapEncodeTiled_v12000 fn, CUtensorMap *m, CUtensorMapDataType dt, const void *base,
+                 uint64_t width, uint64_t row_bytes, uint64_t rows, uint32_t box_w)
+{
+    const cuuint64_t dims[2] = {width, rows};
+    const cuuint64_t strides[1] = {row_bytes};
+    const cuuint32_t box[2] = {box_w, (cuuint32_t)kPage};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, dt, 2, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// CTAs per SM the encoder runs at (2 when shared memory and registers allow).
+int quantize_ctas_per_sm(size_t smem)
+{
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, quantize_kernel, kThreads, smem) != cudaSuccess)
+        return 0;
+    return n;
+}
+
+// dst_pages: pages of the destination planes (one after another)
+cudaError_t run_quantize(const Params &p, int64_t dst_pages, cudaStream_t s)
 {
     if (p.pages == 0)
         return cudaSuccess;
+    // tile coordinates are 32-bit row numbers
+    if (p.pages > INT32_MAX / kPage || dst_pages > INT32_MAX / kPage)
+        return cudaErrorNotSupported;
     const int sms = device_sm_count();
     if (sms <= 0)
         return cudaErrorNoDevice;
+    const PFN_cuTensorMapEncodeTiled_v12000 fn = tensor_map_encoder();
+    if (!fn)
+        return cudaErrorNotSupported;
+    CUtensorMap xmap, amap, rmap;
+    if (!encode_rows(fn, &xmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.x, kD, kD * 2, (uint64_t)p.pages * kPage, kHalf) ||
+        !encode_rows(fn, &amap, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.anc, kD / 2, kD / 2, (uint64_t)dst_pages * kPage,
+                     kRowB) ||
+        !encode_rows(fn, &rmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.res, kD / 2, kD / 2, (uint64_t)dst_pages * kPage,
+                     kRowB))
+        return cudaErrorInvalidValue;
     const size_t smem = sizeof(Smem);
     cudaError_t e = cudaFuncSetAttribute(quantize_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(quantize_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess)
         return e;
-    const int64_t grid = p.pages < sms ? p.pages : sms;
-    quantize_kernel<<<(unsigned)grid, kThreads, smem, s>>>(p, host_tables().code, (uint32_t)kCopies * 8u, 1u);
+    const int per_sm = quantize_ctas_per_sm(smem);
+    if (per_sm <= 0)
+        return cudaErrorNotSupported;
+    const int64_t units = 2 * p.pages, cap = (int64_t)sms * per_sm;
+    const int64_t grid = units < cap ? units : cap;
+    quantize_kernel<<<(unsigned)grid, kThreads, smem, s>>>(p, xmap, amap, rmap, host_tables().code,
+                                                           (uint32_t)kCopies * 8u, 1u);
     return cudaGetLastError();
 }
 
@@ -496,9 +599,9 @@ cudaError_t run_quantize(const Params &p, cudaStream_t s)
 cudaError_t launch_quantize(const uint16_t *x, const int32_t *page_valid, const lynx_qkv &o, cudaStream_t s)
 {
     const int P = o.tokens / kPage;
-    Params p{x, page_valid, o.anchor, o.residual, o.page_meta, o.chunk_meta,
-             (int64_t)o.layers * o.kv_heads * P, P, nullptr, nullptr, 1, nullptr};
-    return run_quantize(p, s);
+    const int64_t pages = (int64_t)o.layers * o.kv_heads * P;
+    Params p{x, page_valid, o.anchor, o.residual, o.page_meta, o.chunk_meta, pages, P, nullptr, nullptr, 1, nullptr};
+    return run_quantize(p, pages, s);
 }
 
 cudaError_t launch_quantize_append(const uint16_t *tail, const int32_t *dst_page, const int32_t *valid, int n,
@@ -507,7 +610,7 @@ cudaError_t launch_quantize_append(const uint16_t *tail, const int32_t *dst_page
     const int LH = o.layers * o.kv_heads;
     Params p{tail, nullptr, o.anchor, o.residual, o.page_meta, o.chunk_meta,
              (int64_t)n * LH, o.tokens / kPage, dst_page, valid, LH > 0 ? LH : 1, dev_err};
-    return run_quantize(p, s);
+    return run_quantize(p, (int64_t)LH * (o.tokens / kPage), s);
 }
 
 cudaError_t launch_level_codes(const float *w, int64_t n, int8_t *codes, cudaStream_t s)
