@@ -82,6 +82,9 @@ def test_quantize_rejects_bad_arguments(lx):
     assert _q(lx, _qkv(lx), x=0x400008) == lx.ERR_ALIGN
     assert _q(lx, _qkv(lx, base=0x10004)) == lx.ERR_ALIGN
     assert _q(lx, _qkv(lx), pv=0x500002) == lx.ERR_ALIGN
+    # 2^23 pages: more rows than 32-bit tile coordinates address (refused
+    # before anything reaches a device)
+    assert _q(lx, _qkv(lx, L=1024, H=32, T=65536)) == lx.ERR_UNSUPPORTED
 
 
 def test_dequant_and_refine_reject_bad_arguments(lx):
