@@ -12,10 +12,11 @@
 // a page are independent). Persistent CTAs of 8 warps, two per SM, walk the
 // units; a unit arrives by one 2D tensor copy (TMA, rows of 128 bytes out of
 // the page's 256) into a single input buffer, which is refilled with the next
-// unit as soon as the current one is in registers, and the two CTAs of an SM
-// run out of step, so that one's barriers and latency-bound stretches overlap
-// the other's stage 3 (one 16-warp CTA per page with a double-buffered input
-// keeps all warps in the same phase and runs 1.8 % slower). Warp w owns chunk
+// unit (already on its way to L2) as soon as the current one is in registers,
+// and the two CTAs of an SM run out of step, so that one's barriers and
+// latency-bound stretches overlap the other's stage 3 (one 16-warp CTA per
+// page with a double-buffered input keeps all warps in the same phase and
+// runs 1.8 % slower). Warp w owns chunk
 // w (32 tokens); lane l owns one channel pair, so the chunk reduction tree
 // of the numeric contract runs inside one thread's registers. Stage 3 is one
 // lookup in a 16-way replicated bucket table (a conflict-free 8-byte load per
@@ -294,6 +295,15 @@ __device__ __forceinline__ void tile_g2s(void *dst, const CUtensorMap *map, int 
                  : "memory");
 }
 
+// Prefetch one 2D tile into L2.
+__device__ __forceinline__ void tile_prefetch_l2(const CUtensorMap *map, int c0, int c1)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c0), "r"(c1)
+                 : "memory");
+}
+
 // One 2D tiled tensor copy shared -> global, tracked by the issuing thread's
 // bulk groups.
 __device__ __forceinline__ void tile_s2g(const CUtensorMap *map, int c0, int c1, const void *src)
@@ -346,6 +356,10 @@ __global__ void __launch_bounds__(kThreads, 2) quantize_kernel(Params p, const _
         const int64_t page = unit >> 1, next = unit + stride;
         const int half = (int)(unit & 1);
         const int pi = half * (kHalf / 2) + lane;  // channel pair of the page: channels 2pi, 2pi+1
+        // the next unit's tile heads for L2 now; its copy into shared memory
+        // follows after this unit's first barrier (0.4 % faster)
+        if (warp == 0 && lane == 0 && next < units)
+            tile_prefetch_l2(&xmap, (int)(next & 1) * kHalf, (int)(next >> 1) * kPage);
         const bool ok = mbar_wait_bounded(&sm.bar, (uint32_t)k & 1u, kWaitLimit);
 
         const int n = valid_of(p, page);
