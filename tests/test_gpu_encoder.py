@@ -68,42 +68,57 @@ def test_ragged_multi_layer(lx, orc, valid):
     assert_planes_equal(_encode(lx, xb, pv), orc.quantize(xb, pv))
 
 
-def test_special_values(lx, orc):
+# c0: first channel of the planted pattern (0: the page's first channel half,
+# 100: the second; the encoder handles the two halves of a page separately)
+@pytest.mark.parametrize("c0", [0, 100])
+def test_special_values(lx, orc, c0):
     """Constant channels, signed-zero extremes, huge and tiny magnitudes."""
     w = S.Workload("t", 78, L=1, H=1, T=512, n_outliers_fixed=3)
     xf = S.bf16_bits_to_f32(S.laplace_bf16(w.key(S.S_V), w.scales(S.S_V), 1, 1, 512)).copy()
-    xf[..., 0] = 2.5
-    xf[..., 1] = 0.0
-    xf[..., 2] = np.abs(xf[..., 2])
-    xf[0, 0, 5, 2] = 0.0
-    xf[..., 3] *= 1e30
-    xf[..., 4] *= 1e-30
-    xf[0, 0, 0:32, 5] = 7.0           # a constant chunk inside a varying channel
+    xf[..., c0 + 0] = 2.5
+    xf[..., c0 + 1] = 0.0
+    xf[..., c0 + 2] = np.abs(xf[..., c0 + 2])
+    xf[0, 0, 5, c0 + 2] = 0.0
+    xf[..., c0 + 3] *= 1e30
+    xf[..., c0 + 4] *= 1e-30
+    xf[0, 0, 0:32, c0 + 5] = 7.0      # a constant chunk inside a varying channel
     xb = S.f32_to_bf16_bits(xf)
-    xb[0, 0, 7, 1] = 0x8000            # -0 among +0
-    xb[0, 0, 9, 2] = 0x8000
+    xb[0, 0, 7, c0 + 1] = 0x8000       # -0 among +0
+    xb[0, 0, 9, c0 + 2] = 0x8000
     assert_planes_equal(_encode(lx, xb), orc.quantize(xb))
 
 
-def test_unrepresentable_statistics(lx, orc):
+@pytest.mark.parametrize("c0", [0, 100])
+def test_unrepresentable_statistics(lx, orc, c0):
     """NaN, infinite, overflowing-range and subnormal-range channels (coded as
     constant, NaN statistics stored as the quiet NaN) next to ordinary ones, in
     every chunk position; bit-exact, metadata included."""
     w = S.Workload("t", 79, L=1, H=2, T=512, n_outliers_fixed=3)
     xf = S.bf16_bits_to_f32(S.laplace_bf16(w.key(S.S_K), w.scales(S.S_K), 1, 2, 512)).copy()
-    xf[0, 0, 9, 4] = np.inf
-    xf[0, 1, 300, 4] = -np.inf
-    xf[0, 0, :, 5] = 1.0
-    xf[0, 0, 3, 5], xf[0, 0, 200, 5] = -3.0e38, 3.0e38
-    xf[0, 1, :256, 6] = 0.0
-    xf[0, 1, 17, 6] = 2.0 ** -130
-    xf[0, 1, 256:, 8] = 0.0
-    xf[0, 1, 296, 8] = 2.0 ** -126
+    xf[0, 0, 9, c0 + 4] = np.inf
+    xf[0, 1, 300, c0 + 4] = -np.inf
+    xf[0, 0, :, c0 + 5] = 1.0
+    xf[0, 0, 3, c0 + 5], xf[0, 0, 200, c0 + 5] = -3.0e38, 3.0e38
+    xf[0, 1, :256, c0 + 6] = 0.0
+    xf[0, 1, 17, c0 + 6] = 2.0 ** -130
+    xf[0, 1, 256:, c0 + 8] = 0.0
+    xf[0, 1, 296, c0 + 8] = 2.0 ** -126
     xb = S.f32_to_bf16_bits(xf)
-    xb[0, 0, 5, 3] = 0x7FC1
-    xb[0, 1, 511, 7] = 0xFF80           # -inf in the last token
-    xb[0, 1, 260, 9] = 0xFFC0           # negative NaN
+    xb[0, 0, 5, c0 + 3] = 0x7FC1
+    xb[0, 1, 511, c0 + 7] = 0xFF80      # -inf in the last token
+    xb[0, 1, 260, c0 + 9] = 0xFFC0      # negative NaN
     assert_planes_equal(_encode(lx, xb), orc.quantize(xb))
+
+
+def test_page_count_around_the_grid(lx, orc):
+    """153 pages (306 channel-half units): a little more work than one round of
+    two CTAs per SM on a 152-SM part, so that a few CTAs take a second unit,
+    with a ragged last page; bit-exact."""
+    w = S.Workload("t", 80, L=1, H=1, T=153 * 256, n_outliers_fixed=4)
+    xb = S.laplace_bf16(w.key(S.S_K), w.scales(S.S_K), 1, 1, 153 * 256)
+    pv = np.full(153, 256, np.int32)
+    pv[-1] = 77
+    assert_planes_equal(_encode(lx, xb, pv), orc.quantize(xb, pv))
 
 
 @pytest.mark.parametrize("which", ["u", "tree", "w", "mean"])
