@@ -114,6 +114,9 @@ typedef struct {
  *               invalid tokens store code 0 (anchor 0, residual 7). Counts
  *               outside 0..256 are clamped.
  *   out         planes and metadata written; residual must be non-NULL.
+ * The call has no device-error word: a page copy that never lands (every wait
+ * in the kernel is bounded) ends the kernel early without a report, leaving
+ * later pages unwritten; lynx_quantize_append reports the same event.
  * Returns LYNX_ERR_UNSUPPORTED when layers * kv_heads * tokens / 256 exceeds
  * 2^31 / 256 pages (the kernel addresses rows with 32-bit tile coordinates)
  * or the driver provides no tensor-map encoder.
@@ -136,7 +139,8 @@ lynx_status lynx_quantize_pages(const void *x_bf16, const int32_t *page_valid, c
  *   valid      device, [n] int32 valid-token counts (clamped to 0..256)
  *   out        the pool: planes and metadata of every layer and KV head
  *              (residual non-NULL); only the destination pages are written
- *   dev_err    device or NULL, one uint32
+ *   dev_err    device or NULL, one uint32 (LYNX_DEVERR_PAGE, and LYNX_DEVERR_TIMEOUT
+ *              when a tail's copy into the kernel never landed)
  * Tails naming the same physical page race on it: pass distinct pages.
  * Returns LYNX_ERR_UNSUPPORTED under the same limits as lynx_quantize_pages
  * (for the n tails' pages and for the pool's).

@@ -395,9 +395,13 @@ __global__ void __launch_bounds__(kThreads, 2) quantize_kernel(Params p, const _
         // (a thread whose wait gave up read a unit that never landed; nothing
         // of it is used)
         if (__syncthreads_or(!ok)) {
-            // the copy never landed: stop, after waiting once more for it
-            if (tid == 0)
+            // the copy never landed: report it (appending), and stop after
+            // waiting once more for it
+            if (tid == 0) {
+                if (p.dev_err)
+                    atomicOr(p.dev_err, LYNX_DEVERR_TIMEOUT);
                 mbar_wait_bounded(&sm.bar, (uint32_t)k & 1u, kWaitLimit);
+            }
             break;
         }
         // every value of the unit is in registers: refill the buffer with the
