@@ -47,3 +47,48 @@ def test_reference_arm_prints_once_under_two_ranks():
     assert r.returncode == 0, r.stderr[-2000:]
     lines = _json_lines(r.stdout)
     assert len(lines) == 1 and lines[0]["impl"] == "reference" and lines[0]["n_gpus"] == 2
+
+
+# Algorithmic bytes per unit of each kernel group the bench reports traffic for
+# (the encoder and the refine read bf16 or planes and write planes, metadata or
+# bf16; decode attention reads codes and metadata per token and KV head).
+ALGORITHMIC = {"quantize": 3.15625, "refine": 3.15625, "dequant_anchor": 2.65625,
+               "decode_attn_full": 296.0, "decode_attn_anchor": 168.0}
+
+
+def _bench_module():
+    import importlib.util
+    spec = importlib.util.spec_from_file_location("bench_under_test", os.path.join(ROOT, "bench.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod
+
+
+def test_traffic_records_are_near_the_algorithmic_bytes():
+    """Each committed DRAM capture moves within 10 % of the kernel's algorithmic
+    bytes (far above would mean re-reads; far below, a capture of the wrong
+    launch)."""
+    with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+        recs = {k: v for k, v in json.load(f).items() if isinstance(v, dict)}
+    assert set(recs) == set(ALGORITHMIC)
+    for k, r in recs.items():
+        assert r["bytes_per_unit"] > 0
+        ratio = r["bytes_per_unit"] / ALGORITHMIC[k]
+        assert 0.9 <= ratio <= 1.1, (k, ratio)
+        assert "--clock-control none" in r["command"]
+
+
+def test_measured_traffic_is_null_once_the_source_changes(tmp_path):
+    bench = _bench_module()
+    src = tmp_path / "k.cu"
+    src.write_text("__global__ void k() {}\n")
+    import hashlib
+    (tmp_path / "profiles").mkdir()
+    rec = {"g": {"kernel": "k", "source": "k.cu", "sha256": hashlib.sha256(src.read_bytes()).hexdigest(),
+                 "unit": "element", "bytes_per_unit": 3.0}}
+    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps(rec))
+    bench.ROOT = str(tmp_path)
+    assert bench.measured_traffic("g", 2e9) == pytest.approx(6.0)      # GB per launch
+    assert bench.measured_traffic("other", 2e9) is None
+    src.write_text("__global__ void k() { }\n")                       # the kernel changed
+    assert bench.measured_traffic("g", 2e9) is None
