@@ -588,12 +588,13 @@ cudaError_t run_quantize(const Params &p, int64_t dst_pages, cudaStream_t s)
     const PFN_cuTensorMapEncodeTiled_v12000 fn = tensor_map_encoder();
     if (!fn)
         return cudaErrorNotSupported;
+    // an empty pool (appending into 0 pages: every tail is outside it, skipped
+    // and flagged) still needs well-formed plane maps; no store ever uses them
+    const uint64_t plane_rows = (uint64_t)(dst_pages > 0 ? dst_pages : 1) * kPage;
     CUtensorMap xmap, amap, rmap;
     if (!encode_rows(fn, &xmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.x, kD, kD * 2, (uint64_t)p.pages * kPage, kHalf) ||
-        !encode_rows(fn, &amap, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.anc, kD / 2, kD / 2, (uint64_t)dst_pages * kPage,
-                     kRowB) ||
-        !encode_rows(fn, &rmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.res, kD / 2, kD / 2, (uint64_t)dst_pages * kPage,
-                     kRowB))
+        !encode_rows(fn, &amap, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.anc, kD / 2, kD / 2, plane_rows, kRowB) ||
+        !encode_rows(fn, &rmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.res, kD / 2, kD / 2, plane_rows, kRowB))
         return cudaErrorInvalidValue;
     const size_t smem = sizeof(Smem);
     cudaError_t e = cudaFuncSetAttribute(quantize_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

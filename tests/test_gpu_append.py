@@ -86,6 +86,26 @@ def test_out_of_pool_pages_are_skipped_and_flagged(lx, orc):
             assert_planes_equal(_page(after, 0, h, p), _page(before, 0, h, p))
 
 
+def test_empty_pool_flags_every_tail(lx):
+    """A pool of 0 pages (tokens = 0, through the raw ABI, whose pointers must
+    only be non-NULL and aligned): every tail is outside it, so the call
+    succeeds, writes nothing and sets the page bit."""
+    import ctypes
+    tails = bf16_dev(_tails(2, 1, 2, S.S_K))
+    scratch = torch.zeros(1024, dtype=torch.uint8, device="cuda")
+    base = scratch.data_ptr()
+    d = lx.LynxQKV(1, 2, 0, 128, base, base + 256, base + 512, base + 768)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    phys, valid = i32_dev([0, 3]), i32_dev([256, 7])
+    st = lx.library().lynx_quantize_append(ctypes.c_void_p(tails.data_ptr()), ctypes.c_void_p(phys.data_ptr()),
+                                            ctypes.c_void_p(valid.data_ptr()), 2, ctypes.byref(d),
+                                            ctypes.c_void_p(err.data_ptr()), None)
+    torch.cuda.synchronize()
+    assert st == lx.OK
+    assert int(err.item()) == 1
+    assert int(scratch.count_nonzero().item()) == 0
+
+
 def test_batched_decode_tails_full_size(lx, orc):
     """The batched-decode workload's growing last pages (32 requests, ragged
     contexts, seeded physical pages) over 8 layers x 8 KV heads; sampled pages
